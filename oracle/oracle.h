@@ -1,0 +1,73 @@
+/*
+ * oracle.h -- scalar f64 CPU oracle for RMSNorm, the post-norm-then-add shape
+ * and the dual-epsilon sandwich tail.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This code is the reference that the CUDA path is
+ * checked against; it is never part of the product path.  Only the tests, the
+ * smoke check and the benchmark's CPU-baseline leg may load it.  It shares no
+ * code, header, helper or constant with the CUDA library.
+ *
+ * Sources (page titles and sections):
+ *   [P1] "Chapter 12 -- RMSNorm and the dual-epsilon sandwich", section 12.1
+ *        (definition), 12.3 (worked example), 12.4.3 (the dual-eps tail:
+ *        hidden += rms_norm(src, eps1) * w1; output = rms_norm(hidden, eps2) * w2),
+ *        12.4.4 (the split route's f32 publication boundary between the norms).
+ *   [P4] "RMSNorm Layer - Root Mean Square Normalization" (Hesper API docs),
+ *        rmsNormThenAddKernel / rmsNormThenAddBatchKernel:
+ *        output = RMSNorm(layer_out) * scale + residual.
+ *
+ * Layout: every row operand is a contiguous row-major [rows x n] array of
+ * double, row r at base + r*n; gamma is [n] and shared by all rows.  Inputs
+ * of narrower types (f32, bf16) are widened to double by the caller, which is
+ * exact.  Accumulation is a plain sequential double sum in column order.
+ *
+ * Parity status: every function below is pinned by CPU tests against the
+ * pages' worked example, closed forms, a library routine in f64, exact
+ * rational arithmetic on tiny inputs and structural invariants.
+ */
+#ifndef MRN_ORACLE_H
+#define MRN_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* y[r,j] = x[r,j] * (1 / sqrt(mean_j(x[r,:]^2) + eps)) * gamma[j]      [P1 12.1] */
+void oracle_rmsnorm(const double *x, const double *gamma, double *y,
+                    int64_t rows, int64_t n, double eps);
+
+/* out[r,j] = RMSNorm(x[r,:]; eps)[j] * gamma[j] + residual[r,j]      [P4 ThenAdd] */
+void oracle_rmsnorm_then_add(const double *x, const double *gamma,
+                             const double *residual, double *out,
+                             int64_t rows, int64_t n, double eps);
+
+/*
+ * Dual-epsilon sandwich tail                                   [P1 12.4.3]
+ *   out_stream = RMSNorm(block_out; eps_post) * gamma_post + residual
+ *   normed     = RMSNorm(out_stream; eps_pre) * gamma_pre
+ * When stream_bf16 is non-zero, out_stream is rounded to bf16 (round to
+ * nearest, ties to even) before it is stored and before the second norm
+ * reads it: the stored stream is what the second norm sees, as on the split
+ * route's publication boundary [P1 12.4.4].
+ */
+void oracle_norm_residual_norm(const double *block_out, const double *residual,
+                               const double *gamma_post, const double *gamma_pre,
+                               double *out_stream, double *normed,
+                               int64_t rows, int64_t n,
+                               double eps_post, double eps_pre, int stream_bf16);
+
+/* Round a double to the nearest bf16 (ties to even); returns the bit pattern. */
+uint16_t oracle_bf16_from_double(double v);
+/* Exact value of a bf16 bit pattern. */
+double oracle_double_from_bf16(uint16_t bits);
+/* Array forms of the two conversions above. */
+void oracle_bf16_round_array(const double *v, uint16_t *bits, int64_t count);
+void oracle_bf16_widen_array(const uint16_t *bits, double *v, int64_t count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MRN_ORACLE_H */

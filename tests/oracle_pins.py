@@ -1,0 +1,424 @@
+"""Pins of the CPU oracle to facts other than the oracle itself.
+
+Each ``check_*`` function takes an ``oracle.Oracle`` (the real one, or a mutant
+compiled from an edited copy of its source) and raises AssertionError when the
+oracle disagrees with:
+
+* the worked example printed on "Chapter 12 -- RMSNorm and the dual-epsilon
+  sandwich", section 12.3 (``golden/rmsnorm_worked_example.txt``);
+* closed forms: a constant row, the two-element rows, the epsilon-dominated
+  limit, the exact scale law y(a x; a^2 eps) = y(x; eps), a residual-free
+  sandwich over rows of known mean square;
+* library routines in float64: ``torch.nn.functional.rms_norm`` (the routine the
+  dormouse page pins against, its section 6) and ``layer_norm`` on mean-centred
+  rows (the identity mean(x^2) = sigma^2 + mu^2 of section 12.2);
+* exact rational / 50-digit decimal arithmetic on tiny inputs;
+* structural invariants (row and column permutations);
+* torch's float32 -> bfloat16 conversion for the bf16 rounding routine.
+
+``ALL_CHECKS`` lists them; the mutation test runs every check against each
+planted mistake and expects at least one to fail.
+"""
+from __future__ import annotations
+
+import os
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import torch
+import torch.nn.functional as F
+
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def load_golden(name: str) -> dict:
+    """Parse ``<key> <values...> | <tol>`` lines into {key: (array, tol)}."""
+    out = {}
+    with open(os.path.join(GOLDEN_DIR, name)) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, tol = line.split("|")
+            parts = lhs.split()
+            out[parts[0]] = (np.array([float(v) for v in parts[1:]]), float(tol))
+    return out
+
+
+def _rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _assert_close(got, want, tol, what):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    err = np.abs(got - want)
+    bad = err > tol
+    assert not np.any(bad), (f"{what}: max err {err.max():.3e} > tol; "
+                             f"got {got[bad][:4]} want {want[bad][:4]}")
+
+
+def _assert_rel(got, want, rel, what, floor=0.0):
+    want = np.asarray(want, dtype=np.float64)
+    _assert_close(got, want, rel * np.abs(want) + floor, what)
+
+
+def _torch_rms(x, gamma, eps):
+    t = torch.from_numpy(np.asarray(x, dtype=np.float64))
+    w = torch.from_numpy(np.asarray(gamma, dtype=np.float64))
+    return F.rms_norm(t, (t.shape[-1],), weight=w, eps=float(eps)).numpy()
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm
+# ---------------------------------------------------------------------------
+def check_worked_example(orc):
+    """Section 12.3: x = [3, 4, 0, 0], eps = 1e-5, with both gammas printed."""
+    g = load_golden("rmsnorm_worked_example.txt")
+    eps = g["eps"][0][0]
+    x = g["x"][0][None, :]
+    y1 = orc.rmsnorm(x, g["gamma_ones"][0], eps)[0]
+    y2 = orc.rmsnorm(x, g["gamma_shaped"][0], eps)[0]
+    inv = y1[0] / x[0, 0]
+    rms = 1.0 / inv
+    mean_sq = rms * rms - eps
+    _assert_close(inv, g["inv_rms"][0][0], g["inv_rms"][1], "inv_rms")
+    _assert_close(rms, g["rms"][0][0], g["rms"][1], "rms")
+    _assert_close(mean_sq, g["mean_sq"][0][0], 1e-12, "mean of squares")
+    _assert_close(mean_sq * 4, g["sum_sq"][0][0], 1e-11, "sum of squares")
+    _assert_close(y1, g["y_gamma_ones"][0], g["y_gamma_ones"][1], "y, gamma = 1")
+    _assert_close(np.mean(y1 * y1), g["mean_sq_y_gamma_ones"][0][0],
+                  g["mean_sq_y_gamma_ones"][1], "mean(y^2), gamma = 1")
+    _assert_close(y2, g["y_gamma_shaped"][0], g["y_gamma_shaped"][1], "y, gamma shaped")
+
+
+def check_constant_rows(orc):
+    """x = c in every column  =>  y_j = c / sqrt(c^2 + eps) * gamma_j."""
+    g = _rng(11)
+    for n in (1, 2, 7, 64, 6656):
+        gamma = 1.0 + 0.1 * g.standard_normal(n)
+        for c in (1e-3, -0.5, 3.0, 1e3):
+            for eps in (1e-5, 1e-8):
+                x = np.full((2, n), c)
+                y = orc.rmsnorm(x, gamma, eps)
+                want = c / np.sqrt(c * c + eps) * gamma
+                _assert_rel(y, np.broadcast_to(want, y.shape), 1e-12,
+                            f"constant row c={c} n={n} eps={eps}")
+
+
+def check_two_element_rows(orc):
+    """n = 2 by hand: [3, 4] -> [3, 4] / sqrt(12.5 + eps); [1, -1] -> +-1/sqrt(1 + eps)."""
+    eps = 1e-5
+    x = np.array([[3.0, 4.0], [1.0, -1.0], [0.0, 0.0], [-4.0, 3.0]])
+    for rows in (1, 2, 3, 4):
+        y = orc.rmsnorm(x[:rows], np.ones(2), eps)
+        want = np.array([[3.0, 4.0] / np.sqrt(12.5 + eps),
+                         [1.0, -1.0] / np.sqrt(1.0 + eps),
+                         [0.0, 0.0],
+                         [-4.0, 3.0] / np.sqrt(12.5 + eps)])[:rows]
+        _assert_rel(y, want, 1e-15, f"n=2 rows={rows}")
+        if rows >= 3:
+            assert np.all(y[2] == 0.0), "a zero row must give exact zeros"
+
+
+def check_scale_law(orc):
+    """y(a x; a^2 eps) = y(x; eps) exactly in real arithmetic; and y(a x; eps) ~ y(x; eps)
+    when eps << mean(x^2), within eps / (2 mean(x^2))."""
+    g = _rng(12)
+    x = g.standard_normal((5, 300))
+    gamma = 1.0 + 0.1 * g.standard_normal(300)
+    eps = 1e-5
+    base = orc.rmsnorm(x, gamma, eps)
+    for a in (1e-3, 0.5, 10.0, 1e4):
+        _assert_rel(orc.rmsnorm(a * x, gamma, a * a * eps), base, 1e-13,
+                    f"exact scale law a={a}")
+    for a in (3.0, 100.0):
+        # mean squares here are ~1, so the eps effect is below ~1e-5 / 2 * 1.1
+        _assert_rel(orc.rmsnorm(a * x, gamma, eps), base, 0.6e-5 * 1.2,
+                    f"approximate scale invariance a={a}")
+
+
+def check_eps_dominated(orc):
+    """mean(x^2) << eps  =>  y ~ x * gamma / sqrt(eps) (relative deviation ~ ms/(2 eps))."""
+    g = _rng(13)
+    x = 1e-9 * g.standard_normal((3, 512))
+    gamma = 1.0 + 0.1 * g.standard_normal(512)
+    for eps in (1e-5, 1e-8):
+        y = orc.rmsnorm(x, gamma, eps)
+        _assert_rel(y, x * gamma / np.sqrt(eps), 1e-9, f"eps-dominated eps={eps}")
+
+
+def check_rms_of_output(orc):
+    """With gamma = 1 the output has mean square ms / (ms + eps) (section 12.3 check:
+    rms(y) = 1 for eps -> 0)."""
+    g = _rng(14)
+    x = np.vstack([c * g.standard_normal(1000) for c in (1e-3, 1.0, 30.0)])
+    eps = 1e-5
+    y = orc.rmsnorm(x, np.ones(1000), eps)
+    for r in range(x.shape[0]):
+        xs = [Fraction(v) for v in x[r]]
+        ms = float(sum(v * v for v in xs) / len(xs))
+        _assert_rel(np.mean(y[r] * y[r]), ms / (ms + eps), 1e-13, f"mean(y^2) row {r}")
+
+
+def check_against_torch_rms_norm(orc):
+    """torch.nn.functional.rms_norm in float64, several shapes and epsilons."""
+    g = _rng(15)
+    for rows, n in ((3, 5), (4, 6656), (2, 65536), (7, 2)):
+        x = g.standard_normal((rows, n)) * 10.0 ** g.uniform(-3, 2, size=(rows, 1))
+        gamma = 1.0 + 0.1 * g.standard_normal(n)
+        for eps in (1e-5, 1e-6, 1e-8):
+            _assert_rel(orc.rmsnorm(x, gamma, eps), _torch_rms(x, gamma, eps), 1e-12,
+                        f"torch rms_norm rows={rows} n={n} eps={eps}", floor=1e-300)
+
+
+def check_layer_norm_identity(orc):
+    """Mean-centred rows: RMSNorm == LayerNorm without bias; and in general
+    rms = sqrt(sigma^2 + mu^2) (section 12.2, 'A useful identity')."""
+    g = _rng(16)
+    n = 777
+    x = g.standard_normal((4, n)) * 3.0
+    gamma = 1.0 + 0.1 * g.standard_normal(n)
+    eps = 1e-5
+    xc = x - x.mean(axis=1, keepdims=True)
+    ln = F.layer_norm(torch.from_numpy(xc), (n,), weight=torch.from_numpy(gamma),
+                      bias=None, eps=eps).numpy()
+    _assert_rel(orc.rmsnorm(xc, gamma, eps), ln, 1e-12, "layer_norm on centred rows",
+                floor=1e-15)
+    t = torch.from_numpy(x + 0.7)
+    var, mu = torch.var_mean(t, dim=1, unbiased=False, keepdim=True)
+    want = (t / torch.sqrt(var + mu * mu + eps) * torch.from_numpy(gamma)).numpy()
+    _assert_rel(orc.rmsnorm(x + 0.7, gamma, eps), want, 1e-12, "sigma^2 + mu^2 identity")
+
+
+def _decimal_inv_rms(row, eps):
+    ss = sum(Fraction(v) * Fraction(v) for v in row)
+    d = ss / len(row) + Fraction(eps)
+    return Decimal(1) / (Decimal(d.numerator) / Decimal(d.denominator)).sqrt()
+
+
+def check_exact_small(orc):
+    """n <= 8: compare with exact rationals and a 50-digit decimal square root."""
+    getcontext().prec = 50
+    g = _rng(17)
+    for n in range(1, 9):
+        x = g.standard_normal((3, n))
+        res = g.standard_normal((3, n))
+        gamma = 1.0 + 0.1 * g.standard_normal(n)
+        gamma2 = 1.0 + 0.1 * g.standard_normal(n)
+        eps, eps2 = 1e-5, 1e-8
+        y = orc.rmsnorm(x, gamma, eps)
+        t = orc.rmsnorm_then_add(x, gamma, res, eps)
+        s, o = orc.norm_residual_norm(x, res, gamma, gamma2, eps2, eps)
+        for r in range(3):
+            inv = _decimal_inv_rms(x[r], eps)
+            p = [Decimal(x[r, j]) * inv * Decimal(gamma[j]) for j in range(n)]
+            want_y = np.array([float(v) for v in p])
+            want_t = np.array([float(p[j] + Decimal(res[r, j])) for j in range(n)])
+            _assert_rel(y[r], want_y, 4e-15, f"exact rmsnorm n={n}", floor=1e-300)
+            scale_t = np.abs(want_y) + np.abs(res[r])
+            _assert_close(t[r], want_t, 4e-15 * scale_t, f"exact then-add n={n}")
+            inv_post = _decimal_inv_rms(x[r], eps2)
+            st = [Decimal(x[r, j]) * inv_post * Decimal(gamma[j]) + Decimal(res[r, j])
+                  for j in range(n)]
+            want_s = np.array([float(v) for v in st])
+            _assert_close(s[r], want_s, 4e-15 * scale_t + 1e-300, f"exact stream n={n}")
+            # second norm of the stored stream
+            inv_pre = _decimal_inv_rms(s[r], eps)
+            want_o = np.array([float(Decimal(s[r, j]) * inv_pre * Decimal(gamma2[j]))
+                               for j in range(n)])
+            _assert_rel(o[r], want_o, 4e-15, f"exact normed n={n}", floor=1e-300)
+
+
+def check_row_and_column_permutations(orc):
+    """Rows are independent (row permutation permutes outputs bit for bit);
+    permuting columns together with gamma permutes the outputs."""
+    g = _rng(18)
+    x = g.standard_normal((9, 130))
+    res = g.standard_normal((9, 130))
+    gamma = 1.0 + 0.1 * g.standard_normal(130)
+    eps = 1e-5
+    pr = g.permutation(9)
+    pc = g.permutation(130)
+    y = orc.rmsnorm_then_add(x, gamma, res, eps)
+    assert np.array_equal(orc.rmsnorm_then_add(x[pr], gamma, res[pr], eps), y[pr]), \
+        "row permutation"
+    _assert_rel(orc.rmsnorm_then_add(x[:, pc], gamma[pc], res[:, pc], eps), y[:, pc],
+                1e-13, "column permutation", floor=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# post-norm then add (Hesper rmsNormThenAddKernel) and the sandwich tail
+# ---------------------------------------------------------------------------
+def check_then_add_against_torch(orc):
+    g = _rng(19)
+    for rows, n in ((5, 6656), (3, 7), (64, 128)):
+        x = g.standard_normal((rows, n)) * 10.0 ** g.uniform(-2, 2, size=(rows, 1))
+        res = g.standard_normal((rows, n))
+        gamma = 1.0 + 0.1 * g.standard_normal(n)
+        p = _torch_rms(x, gamma, 1e-6)
+        got = orc.rmsnorm_then_add(x, gamma, res, 1e-6)
+        _assert_close(got, p + res, 1e-12 * (np.abs(p) + np.abs(res)),
+                      f"then-add rows={rows} n={n}")
+    # zero rows give the residual exactly
+    x[1:3] = 0.0
+    got = orc.rmsnorm_then_add(x, gamma, res, 1e-6)
+    assert np.array_equal(got[1:3], res[1:3]), "zero rows must return the residual"
+
+
+def _torch_sandwich(b, r, gp, gq, eps_post, eps_pre):
+    s = _torch_rms(b, gp, eps_post) + r
+    return s, _torch_rms(s, gq, eps_pre)
+
+
+def check_sandwich_against_torch(orc):
+    """Section 12.4.3 as two library norms and an add, in float64."""
+    g = _rng(20)
+    rows, n = 6, 6656
+    b = 2.0 * g.standard_normal((rows, n)) * 10.0 ** g.uniform(-2, 1, size=(rows, 1))
+    r = g.standard_normal((rows, n))
+    gp = 1.0 + 0.1 * g.standard_normal(n)
+    gq = 1.0 + 0.1 * g.standard_normal(n)
+    s, o = orc.norm_residual_norm(b, r, gp, gq, 1e-8, 1e-5)
+    ts, to = _torch_sandwich(b, r, gp, gq, 1e-8, 1e-5)
+    p = _torch_rms(b, gp, 1e-8)
+    _assert_close(s, ts, 1e-12 * (np.abs(p) + np.abs(r)), "sandwich stream vs torch")
+    _assert_rel(o, _torch_rms(s, gq, 1e-5), 1e-12, "sandwich normed vs torch(stream)",
+                floor=1e-300)
+
+
+def check_sandwich_epsilon_routing(orc):
+    """A case where each epsilon is visible: the block output has mean square
+    1e-8 (so eps_post = 1e-8 halves the first norm's scale) and the stream is
+    small enough (mean square ~1e-6) that eps_pre = 1e-5 dominates the second.
+    Swapping the epsilons moves both outputs by more than 10%."""
+    g = _rng(21)
+    rows, n = 4, 4096
+    b = 1e-4 * np.where(g.random((rows, n)) < 0.5, -1.0, 1.0)   # mean square exactly 1e-8
+    r = 1e-3 * g.standard_normal((rows, n))
+    gp = 1e-3 * (1.0 + 0.1 * g.standard_normal(n))
+    gq = 1.0 + 0.1 * g.standard_normal(n)
+    s, o = orc.norm_residual_norm(b, r, gp, gq, 1e-8, 1e-5)
+    ts, to = _torch_sandwich(b, r, gp, gq, 1e-8, 1e-5)
+    _assert_close(s, ts, 1e-12 * (np.abs(ts) + np.abs(r)), "routing case stream")
+    _assert_rel(o, _torch_rms(s, gq, 1e-5), 1e-12, "routing case normed", floor=1e-300)
+    ws, wo = _torch_sandwich(b, r, gp, gq, 1e-5, 1e-8)       # epsilons swapped
+    assert np.max(np.abs(ws - ts)) > 0.1 * np.max(np.abs(ts - r)), "swap invisible (stream)"
+    assert np.max(np.abs(wo - to)) > 0.1 * np.max(np.abs(to)), "swap invisible (normed)"
+
+
+def check_sandwich_closed_form(orc):
+    """residual = 0, gamma_post = 1, block_out = +-c with mean square c^2:
+    stream_j = b_j / sqrt(c^2 + eps_post), its mean square m = c^2/(c^2 + eps_post),
+    normed_j = stream_j / sqrt(m + eps_pre) * gamma_pre_j."""
+    g = _rng(22)
+    n = 1000
+    gq = 1.0 + 0.1 * g.standard_normal(n)
+    for c in (1e-4, 1e-2, 5.0):
+        b = c * np.where(g.random((3, n)) < 0.5, -1.0, 1.0)
+        s, o = orc.norm_residual_norm(b, np.zeros_like(b), np.ones(n), gq, 1e-8, 1e-5)
+        want_s = b / np.sqrt(c * c + 1e-8)
+        m = c * c / (c * c + 1e-8)
+        want_o = want_s / np.sqrt(m + 1e-5) * gq
+        _assert_rel(s, want_s, 1e-13, f"closed-form stream c={c}")
+        _assert_rel(o, want_o, 1e-13, f"closed-form normed c={c}")
+
+
+def check_sandwich_degenerate(orc):
+    """gamma_post = 0 or block_out = 0 leaves the stream equal to the residual."""
+    g = _rng(23)
+    b = g.standard_normal((3, 50))
+    r = g.standard_normal((3, 50))
+    gq = 1.0 + 0.1 * g.standard_normal(50)
+    s, o = orc.norm_residual_norm(b, r, np.zeros(50), gq, 1e-8, 1e-5)
+    assert np.array_equal(s, r), "gamma_post = 0"
+    s, o = orc.norm_residual_norm(np.zeros_like(b), r, gq, gq, 1e-8, 1e-5)
+    assert np.array_equal(s, r), "block_out = 0"
+    _assert_rel(o, _torch_rms(r, gq, 1e-5), 1e-12, "normed of the bare residual")
+
+
+# ---------------------------------------------------------------------------
+# bf16 conversions
+# ---------------------------------------------------------------------------
+def _torch_bf16_bits(f32):
+    t = torch.from_numpy(np.ascontiguousarray(f32, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def check_bf16_widen_all_patterns(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.double_from_bf16(bits)
+    want = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan), "NaN patterns"
+    assert np.array_equal(got[~nan], want[~nan]), "bf16 widening"
+    back = orc.bf16_from_double(got[~nan])
+    assert np.array_equal(back, bits[~nan]), "round trip of every finite/inf pattern"
+
+
+def check_bf16_round_against_torch(orc):
+    g = _rng(24)
+    raw = g.integers(0, 2 ** 32, size=200000, dtype=np.uint64).astype(np.uint32)
+    f = raw.view(np.float32)
+    f = f[~np.isnan(f)]
+    assert np.array_equal(orc.bf16_from_double(f.astype(np.float64)), _torch_bf16_bits(f)), \
+        "random float32 patterns"
+    # exact midpoints between neighbouring bf16 values (representable in f32): ties
+    lo = g.integers(0, 0x7F7F, size=50000).astype(np.uint16)
+    vlo = orc.double_from_bf16(lo)
+    vhi = orc.double_from_bf16(lo + 1)
+    mid = ((vlo + vhi) / 2).astype(np.float32)
+    assert np.array_equal(mid.astype(np.float64), (vlo + vhi) / 2)
+    for sgn in (1.0, -1.0):
+        m = sgn * mid
+        assert np.array_equal(orc.bf16_from_double(m.astype(np.float64)), _torch_bf16_bits(m)), \
+            "ties to even"
+    special = np.array([np.inf, -np.inf, 3.4e38, -3.4e38, 0.0, -0.0, 2.0 ** -134,
+                        1.5 * 2.0 ** -133], dtype=np.float32)
+    assert np.array_equal(orc.bf16_from_double(special.astype(np.float64)),
+                          _torch_bf16_bits(special)), "specials"
+    assert orc.bf16_from_double([np.nan])[0] & 0x7FFF > 0x7F80, "NaN stays NaN"
+
+
+def check_bf16_sandwich_stream(orc):
+    """stream_bf16: the stored stream is the bf16 rounding of the f64 stream and the
+    second norm reads the rounded values (section 12.4.4)."""
+    g = _rng(25)
+    rows, n = 4, 300
+    b = g.standard_normal((rows, n))
+    r = g.standard_normal((rows, n))
+    gp = 1.0 + 0.1 * g.standard_normal(n)
+    gq = 1.0 + 0.1 * g.standard_normal(n)
+    s, o = orc.norm_residual_norm(b, r, gp, gq, 1e-8, 1e-5, stream_bf16=True)
+    ts, _ = _torch_sandwich(b, r, gp, gq, 1e-8, 1e-5)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ts), 2.0 ** -126))) - 7)
+    _assert_close(s, ts, 0.5 * ulp * (1 + 1e-9), "stream within half a bf16 ulp")
+    bits = orc.bf16_from_double(s)
+    assert np.array_equal(orc.double_from_bf16(bits), s), "stream is bf16-representable"
+    _assert_rel(o, _torch_rms(s, gq, 1e-5), 1e-12, "normed of the rounded stream",
+                floor=1e-300)
+    s32, _ = orc.norm_residual_norm(b, r, gp, gq, 1e-8, 1e-5, stream_bf16=False)
+    assert not np.array_equal(s32, s), "rounding must change the stream"
+
+
+ALL_CHECKS = [
+    check_worked_example,
+    check_constant_rows,
+    check_two_element_rows,
+    check_scale_law,
+    check_eps_dominated,
+    check_rms_of_output,
+    check_against_torch_rms_norm,
+    check_layer_norm_identity,
+    check_exact_small,
+    check_row_and_column_permutations,
+    check_then_add_against_torch,
+    check_sandwich_against_torch,
+    check_sandwich_epsilon_routing,
+    check_sandwich_closed_form,
+    check_sandwich_degenerate,
+    check_bf16_widen_all_patterns,
+    check_bf16_round_against_torch,
+    check_bf16_sandwich_stream,
+]
