@@ -1,0 +1,512 @@
+"""Benchmark of the dual-epsilon sandwich tail (and decode latency) on GB300.
+
+Default workload (one "step" = one call of the fused tail over one batch):
+  sandwich tail, rows=4096, n=6656, f32, eps_post=1e-8, eps_pre=1e-5; each
+  block_out row has mean square log-uniform over 1e-4..1e2 (seeded synthetic).
+Reported: achieved HBM GB/s of that call (algorithmic bytes: block_out and
+residual read once, out_stream and normed written once, both gammas once =
+(4*rows*n + 2*n)*4 bytes), rows/s, the fraction of the measured copy bandwidth,
+and the decode latency of the same kernel at rows=1 (us/call, plain stream
+launches and inside a CUDA graph).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mrn|reference]
+For N > 1 launch under torchrun; every rank runs its own batch (rows are
+independent, no data exchange) and rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and rows/s at n=6656; decode µs/call"
+UNIT = "GB/s"
+KERNEL_SOURCES = ["dual_epsilon_sandwich_gb300/csrc/mrn_kernels.cuh",
+                  "dual_epsilon_sandwich_gb300/csrc/mrn_ops_sandwich.cu",
+                  "dual_epsilon_sandwich_gb300/csrc/mrn_api.cpp"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ncu_sandwich_f32_rows4096_n6656.md")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", choices=("mrn", "reference"), default="mrn")
+    p.add_argument("--rows", type=int, default=4096)
+    p.add_argument("--n", type=int, default=6656)
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--decode-calls", type=int, default=2000)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# helpers shared by both arms
+# ---------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_rows(total_rows: int, world: int, rank: int):
+    """Contiguous row block of `rank` when `total_rows` are split over `world`."""
+    base, extra = divmod(total_rows, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
+def sandwich_bytes(rows: int, n: int, elem: int = 4) -> int:
+    """Algorithmic bytes of one sandwich call: 2 row reads + 2 row writes + 2 gammas."""
+    return (4 * rows * n + 2 * n) * elem
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel sources as they are now; else None."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    d = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != kernel_source_digest():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, rows split over host threads
+# ---------------------------------------------------------------------------
+class OracleRunner:
+    """The oracle's sandwich tail over row blocks, one block per host thread
+    (ctypes releases the GIL, so the blocks run in parallel)."""
+
+    def __init__(self, arrays64, n):
+        import numpy as np
+
+        import oracle
+        self.np = np
+        self.orc = oracle.default()
+        self.b, self.r, self.gp, self.gq = arrays64
+        self.n = n
+        self.threads = os.cpu_count() or 1
+        self.pool = ThreadPoolExecutor(max_workers=self.threads)
+        self.eps_post = float(np.float32(1e-8))
+        self.eps_pre = float(np.float32(1e-5))
+
+    def one_pass(self, rows: int) -> float:
+        """Process the first `rows` rows once; returns the wall time in seconds."""
+        bounds = self.np.linspace(0, rows, self.threads + 1).astype(int)
+
+        def work(i):
+            lo, hi = int(bounds[i]), int(bounds[i + 1])
+            if hi > lo:
+                self.orc.norm_residual_norm(self.b[lo:hi], self.r[lo:hi], self.gp, self.gq,
+                                            self.eps_post, self.eps_pre)
+
+        t0 = time.perf_counter()
+        list(self.pool.map(work, range(self.threads)))
+        return time.perf_counter() - t0
+
+    def rate(self, rows: int, target_seconds: float):
+        """Repeat passes over `rows` rows for about target_seconds; GB/s, rows/s, passes, s."""
+        passes, elapsed = 0, 0.0
+        while passes == 0 or (elapsed < target_seconds and passes < 1000):
+            elapsed += self.one_pass(rows)
+            passes += 1
+        return (sandwich_bytes(rows, self.n) * passes / elapsed / 1e9, rows * passes / elapsed,
+                passes, elapsed)
+
+
+def run_reference(args):
+    """The oracle, timed on the host cores, on the same workload's rows: each
+    step processes a bounded sample of rows, sized so that the whole
+    --warmup + --steps run takes about two minutes."""
+    import numpy as np
+
+    from dual_epsilon_sandwich_gb300 import workloads as wl
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = wl.sandwich_prefill(rows=args.rows, n=args.n)
+    a = w.arrays
+    runner = OracleRunner([a[k].astype(np.float64) for k in ("block_out", "residual",
+                                                             "gamma_post", "gamma_pre")], args.n)
+    calib_rows = min(args.rows, 256)
+    runner.one_pass(calib_rows)
+    rows_per_s = calib_rows / runner.one_pass(calib_rows)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    sample_rows = int(min(args.rows, max(8, rows_per_s * per_step)))
+    for _ in range(args.warmup):
+        runner.one_pass(sample_rows)
+    times = [runner.one_pass(sample_rows) for _ in range(args.steps)]
+    total = sum(times)
+    value = sandwich_bytes(sample_rows, args.n) * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "rows": args.rows, "n": args.n, "eps_post": 1e-8,
+                   "eps_pre": 1e-5, "sample_rows_per_step": sample_rows},
+        "rows_per_s": sample_rows * args.steps / total,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": runner.threads, "kind": "oracle",
+                         "sample": f"first {sample_rows} of the {args.rows} rows per step, "
+                                   f"split over {runner.threads} host threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the CUDA arm
+# ---------------------------------------------------------------------------
+def run_mrn(args):
+    import numpy as np
+    import torch
+
+    from dual_epsilon_sandwich_gb300 import _build, mrn
+    from dual_epsilon_sandwich_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        _build.build()
+    if pg is not None:
+        pg.barrier()
+    mrn.lib()
+
+    rows, n = args.rows, args.n
+    w = wl.sandwich_prefill(rows=rows, n=n)
+    a = w.arrays
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    # two resident buffer sets, used alternately: 2 x 436 MB > L2 between reuse
+    sets = []
+    for _ in range(2):
+        b = torch.from_numpy(a["block_out"]).to(dev)
+        r = torch.from_numpy(a["residual"]).to(dev)
+        gp = torch.from_numpy(a["gamma_post"]).to(dev)
+        gq = torch.from_numpy(a["gamma_pre"]).to(dev)
+        sets.append((b, r, gp, gq, torch.empty_like(b), torch.empty_like(b)))
+
+    def call(sset, nrows=rows):
+        b, r, gp, gq, s, o = sset
+        st = mrn.mrn_norm_residual_norm(b.data_ptr(), r.data_ptr(), gp.data_ptr(),
+                                        gq.data_ptr(), s.data_ptr(), o.data_ptr(), nrows, n,
+                                        1e-8, 1e-5, mrn.MRN_F32, sh)
+        if st != 0:
+            raise mrn.MrnError(st, "mrn_norm_residual_norm")
+
+    geometry = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, rows, n, mrn.MRN_F32, True)
+
+    for i in range(args.warmup):
+        call(sets[i % 2])
+    torch.cuda.synchronize()
+
+    # -- device-resident timed region -------------------------------------
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    sampler.start()
+    time.sleep(0.3)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    launches0 = mrn.mrn_launch_count()
+    t_begin.record(stream)
+    for i in range(K):
+        starts[i].record(stream)
+        call(sets[i % 2])
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if pg is not None:
+        pg.barrier()
+    clocks = sampler.stop()
+    launches = mrn.mrn_launch_count() - launches0
+    total_ms = t_begin.elapsed_time(t_end)
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    avg_kernel_ms = sum(kernel_ms) / K
+    if pg is not None:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    step_bytes = sandwich_bytes(rows, n)
+    value = world * step_bytes * K / (total_ms * 1e-3) / 1e9
+    achieved = step_bytes / (avg_kernel_ms * 1e-3) / 1e9
+
+    # -- end to end through the C ABI with host buffers --------------------
+    pin = {k: torch.from_numpy(a[k]).pin_memory() for k in ("block_out", "residual",
+                                                             "gamma_post", "gamma_pre")}
+    host_s = torch.empty((rows, n), dtype=torch.float32).pin_memory()
+    host_o = torch.empty((rows, n), dtype=torch.float32).pin_memory()
+    b, r, gp, gq, s, o = sets[0]
+    h2d = sum(t.numel() * 4 for t in pin.values())
+    d2h = 2 * rows * n * 4
+
+    def e2e_step():
+        b.copy_(pin["block_out"], non_blocking=True)
+        r.copy_(pin["residual"], non_blocking=True)
+        gp.copy_(pin["gamma_post"], non_blocking=True)
+        gq.copy_(pin["gamma_pre"], non_blocking=True)
+        call(sets[0])
+        host_s.copy_(s, non_blocking=True)
+        host_o.copy_(o, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    if pg is not None:
+        pg.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / args.e2e_steps
+    if pg is not None:
+        t = torch.tensor([e2e_s], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * step_bytes / e2e_s / 1e9
+
+    # -- decode latency: rows=1, n=6656 ---------------------------------------
+    decode = decode_latency(args, dev, stream)
+
+    peak, peak_kind = measured_peaks()
+    traffic = profiled_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "rows": rows, "n": n, "eps_post": 1e-8, "eps_pre": 1e-5,
+                   "global_batch": rows * world, "parallelism": f"rows x{world}, no exchange",
+                   "l2": "inputs larger than L2: two resident buffer sets of 436 MB used "
+                         "alternately", "geometry": geometry},
+        "rows_per_s": world * rows * K / (total_ms * 1e-3),
+        "pct_of_peak": 100.0 * value / (world * peak),
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": step_bytes,
+                     "avg_launch_ms": avg_kernel_ms},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "note": "pinned host buffers, H2D + kernel + D2H "
+                "of both outputs, per step"},
+        "decode": decode,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        runner = OracleRunner([a[k].astype(np.float64) for k in ("block_out", "residual",
+                                                                 "gamma_post", "gamma_pre")], n)
+        gbs, rps, passes, elapsed = runner.rate(rows, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": runner.threads,
+                                "kind": "oracle",
+                                "sample": f"all {rows} rows x {passes} passes ({elapsed:.1f} s), "
+                                          f"rows split over {runner.threads} host threads",
+                                "rows_per_s": rps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def decode_latency(args, dev, stream):
+    """us per call of the sandwich tail at rows=1, n=6656: back-to-back stream
+    launches and a CUDA graph, each over 1024 rotating buffer sets (160 MB > L2)."""
+    import torch
+
+    from dual_epsilon_sandwich_gb300 import mrn
+    from dual_epsilon_sandwich_gb300 import workloads as wl
+    w = wl.sandwich_decode()
+    a = w.arrays
+    nsets = 1024
+    n = w.n
+    big = {k: torch.from_numpy(a[k]).to(dev).repeat(nsets, 1).contiguous()
+           for k in ("block_out", "residual")}
+    gp = torch.from_numpy(a["gamma_post"]).to(dev)
+    gq = torch.from_numpy(a["gamma_pre"]).to(dev)
+    s = torch.empty((nsets, n), device=dev)
+    o = torch.empty((nsets, n), device=dev)
+    sh = stream.cuda_stream
+    ptrs = [(big["block_out"][i].data_ptr(), big["residual"][i].data_ptr(), s[i].data_ptr(),
+             o[i].data_ptr()) for i in range(nsets)]
+
+    def call(i, handle):
+        b, r, ss, oo = ptrs[i % nsets]
+        st = mrn.mrn_norm_residual_norm(b, r, gp.data_ptr(), gq.data_ptr(), ss, oo, 1, n,
+                                        1e-8, 1e-5, mrn.MRN_F32, handle)
+        if st != 0:
+            raise mrn.MrnError(st, "decode")
+
+    calls = args.decode_calls
+    for i in range(64):
+        call(i, sh)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(calls):
+        call(i, sh)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    stream_us = e0.elapsed_time(e1) * 1e3 / calls
+
+    # graph of `per_graph` calls on rotating sets, replayed
+    per_graph = nsets
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for i in range(per_graph):
+                call(i, side.cuda_stream)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, calls // per_graph)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    graph_us = e0.elapsed_time(e1) * 1e3 / (reps * per_graph)
+    # the same call on one buffer set (L2-resident, as right after the producer)
+    g_hot = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_hot, stream=side):
+            for _ in range(per_graph):
+                call(0, side.cuda_stream)
+    stream.wait_stream(side)
+    g_hot.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        g_hot.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    hot_us = e0.elapsed_time(e1) * 1e3 / (reps * per_graph)
+    geometry = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, 1, n, mrn.MRN_F32, True)
+    return {"workload": w.name, "us_per_call_stream": stream_us,
+            "us_per_call_graph": graph_us, "us_per_call_graph_l2_hot": hot_us,
+            "bytes_per_call": sandwich_bytes(1, n), "rotating_sets": nsets,
+            "geometry": geometry}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_mrn(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

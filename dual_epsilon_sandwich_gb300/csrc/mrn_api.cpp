@@ -1,0 +1,383 @@
+// mrn_api.cpp -- the C ABI declared in include/mrn.h: argument validation,
+// geometry choice and the launch of one kernel on the caller's stream.
+//
+// Operations: RMSNorm ("Chapter 12 -- RMSNorm and the dual-epsilon
+// sandwich", section 12.1), post norm then residual add (Hesper "RMSNorm
+// Layer", rmsNormThenAddKernel) and the dual-epsilon sandwich tail (section
+// 12.4.3).  This layer holds no arithmetic of the method; it checks
+// arguments, picks a register geometry from (n, rows, dtype, alignment) and
+// hands the call to the launcher of the operation.
+#include "mrn.h"
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "mrn_internal.h"
+
+namespace {
+
+using mrn::Geometry;
+using mrn::KernelArgs;
+
+std::atomic<uint64_t> g_launch_count{0};
+thread_local int t_last_cuda_error = 0;
+thread_local bool t_forced = false;
+thread_local Geometry t_forced_geometry = {};
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+constexpr int kDefaultSmCount = 152;   // GB300
+
+int elem_bytes(mrn_dtype dt) { return dt == MRN_F32 ? 4 : 2; }
+
+int sm_count_of_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return kDefaultSmCount;
+    }
+    if (dev >= 0 && dev < kMaxDevices) {
+        const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (cached > 0) return cached;
+    }
+    int count = 0;
+    if (cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        count <= 0) {
+        (void)cudaGetLastError();
+        return kDefaultSmCount;
+    }
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(count, std::memory_order_relaxed);
+    return count;
+}
+
+int64_t pow2_ceil(int64_t v) {
+    int64_t p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+int64_t pow2_floor(int64_t v) {
+    int64_t p = 1;
+    while (p * 2 <= v) p <<= 1;
+    return p;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int natural_vec(mrn_dtype dt) { return 16 / elem_bytes(dt); }
+
+// Automatic geometry.  Loads per row: nvec = ceil(n / vec).
+//  * nvec <= 256: several rows per warp (lanes = next power of two of nvec up
+//    to 32, k = ceil(nvec / 32)); no shared memory, no barrier.
+//  * nvec <= 16 * 2048: the row in registers of one CTA or of a cluster of up
+//    to 16 CTAs (2048 loads per CTA at most).  Few rows (decode) are spread
+//    over up to 8 CTAs of a cluster so that more SMs pull the row in.
+//  * wider: the looped fallback.
+Geometry choose_geometry(int64_t rows, int64_t n, mrn_dtype dt, bool aligned16, int sms) {
+    Geometry g = {};
+    g.vec = aligned16 ? natural_vec(dt) : 1;
+    g.cluster = 1;
+    const int64_t nvec = ceil_div(n, g.vec);
+    if (nvec <= 32 * mrn::kMaxK) {
+        g.kind = mrn::kRowsPerWarp;
+        g.threads = mrn::kWarpKernelThreads;
+        g.lanes = nvec <= 32 ? static_cast<int>(pow2_ceil(nvec)) : 32;
+        g.k = static_cast<int>(ceil_div(nvec, 32));
+        g.rows_per_cta = g.threads / g.lanes;
+        return g;
+    }
+    constexpr int64_t kCtaLoads = 2048;
+    int64_t cl = ceil_div(nvec, kCtaLoads);
+    if (cl > mrn::kMaxCluster) {
+        g.kind = mrn::kStream;
+        g.threads = mrn::kStreamMaxThreads;
+        g.k = 1;
+        g.lanes = 0;
+        g.rows_per_cta = 1;
+        return g;
+    }
+    if (rows * 4 <= sms) {
+        const int64_t spread = std::min<int64_t>(8, pow2_floor(std::max<int64_t>(1, nvec / 256)));
+        cl = std::max(cl, spread);
+    }
+    const int64_t per = ceil_div(nvec, cl);
+    double best = 1e30;
+    for (int k = 1; k <= mrn::kMaxK; ++k) {
+        const int64_t t = ceil_div(ceil_div(per, k), 32) * 32;
+        if (t > mrn::cta_max_threads(k)) continue;
+        const double waste = static_cast<double>(t * k - per) / static_cast<double>(per);
+        const double shape = 0.02 * std::fabs(std::log2(static_cast<double>(t) / 256.0));
+        const double score = waste + shape;
+        if (score < best) {
+            best = score;
+            g.k = k;
+            g.threads = static_cast<int>(t);
+        }
+    }
+    g.kind = mrn::kCta;
+    g.cluster = static_cast<int>(cl);
+    g.lanes = 0;
+    g.rows_per_cta = 1;
+    return g;
+}
+
+bool geometry_is_consistent(const Geometry &g) {
+    if (g.kind == mrn::kRowsPerWarp) {
+        const bool pow2 = g.lanes >= 1 && g.lanes <= 32 && (g.lanes & (g.lanes - 1)) == 0;
+        return pow2 && g.k >= 1 && g.k <= mrn::kMaxK && g.threads == mrn::kWarpKernelThreads;
+    }
+    if (g.kind == mrn::kCta) {
+        return g.k >= 1 && g.k <= mrn::kMaxK && g.threads >= 32 && g.threads % 32 == 0 &&
+               g.threads <= mrn::cta_max_threads(g.k) && g.cluster >= 1 &&
+               g.cluster <= mrn::kMaxCluster;
+    }
+    if (g.kind == mrn::kStream) {
+        return g.threads >= 32 && g.threads % 32 == 0 && g.threads <= mrn::kStreamMaxThreads;
+    }
+    return false;
+}
+
+// Resolve the thread's forced geometry for one call; false if it cannot
+// cover the row or asks for vectors the pointers do not allow.
+bool resolve_forced(Geometry g, int64_t n, mrn_dtype dt, bool aligned16, Geometry *out) {
+    if (g.vec == 0) g.vec = aligned16 ? natural_vec(dt) : 1;
+    if (g.vec != 1 && !(g.vec == natural_vec(dt) && aligned16)) return false;
+    const int64_t nvec = ceil_div(n, g.vec);
+    if (g.kind == mrn::kRowsPerWarp) {
+        if (static_cast<int64_t>(g.lanes) * g.k < nvec) return false;
+        g.cluster = 1;
+        g.rows_per_cta = g.threads / g.lanes;
+    } else if (g.kind == mrn::kCta) {
+        if (static_cast<int64_t>(g.cluster) * g.threads * g.k < nvec) return false;
+        g.lanes = 0;
+        g.rows_per_cta = 1;
+    } else {
+        g.k = 1;
+        g.cluster = 1;
+        g.lanes = 0;
+        g.rows_per_cta = 1;
+    }
+    *out = g;
+    return true;
+}
+
+struct Span {
+    uintptr_t lo;
+    uintptr_t hi;
+};
+
+Span span_of(const void *p, int64_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Span{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+bool overlaps(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// An output may coincide exactly with a row input or be disjoint from it.
+bool output_vs_row_input_ok(Span out, Span in) { return !overlaps(out, in) || out.lo == in.lo; }
+
+mrn_status check_common(int64_t rows, int64_t n, mrn_dtype dt, float eps1, float eps2) {
+    if (dt != MRN_F32 && dt != MRN_BF16) return MRN_ERR_UNSUPPORTED_DTYPE;
+    if (n < 1 || rows < 0) return MRN_ERR_INVALID_SIZE;
+    const int64_t e = elem_bytes(dt);
+    if (n > INT64_MAX / e) return MRN_ERR_INVALID_SIZE;
+    if (rows > 0 && rows > INT64_MAX / (n * e)) return MRN_ERR_INVALID_SIZE;
+    if (!(eps1 > 0.0f) || !std::isfinite(eps1)) return MRN_ERR_INVALID_EPS;
+    if (!(eps2 > 0.0f) || !std::isfinite(eps2)) return MRN_ERR_INVALID_EPS;
+    return MRN_OK;
+}
+
+bool aligned_to(const void *p, int64_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+struct Call {
+    mrn::Op op;
+    mrn_dtype dt;
+    int64_t rows;
+    int64_t n;
+    KernelArgs args;
+};
+
+mrn_status launch(const Call &c, bool aligned16, cudaStream_t stream) {
+    Geometry g;
+    if (t_forced) {
+        if (!resolve_forced(t_forced_geometry, c.n, c.dt, aligned16, &g))
+            return MRN_ERR_INVALID_GEOMETRY;
+    } else {
+        g = choose_geometry(c.rows, c.n, c.dt, aligned16, sm_count_of_current_device());
+    }
+    KernelArgs a = c.args;
+    a.n = c.n;
+    a.nvec = ceil_div(c.n, g.vec);
+    const bool bf16 = c.dt == MRN_BF16;
+    uint64_t launched = 0;
+    cudaError_t err;
+    switch (c.op) {
+    case mrn::kRmsnorm: err = mrn::launch_rmsnorm(bf16, g, a, c.rows, stream, &launched); break;
+    case mrn::kThenAdd: err = mrn::launch_then_add(bf16, g, a, c.rows, stream, &launched); break;
+    default: err = mrn::launch_sandwich(bf16, g, a, c.rows, stream, &launched); break;
+    }
+    g_launch_count.fetch_add(launched, std::memory_order_relaxed);
+    if (err != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(err);
+        (void)cudaGetLastError();   // clear the non-sticky launch error
+        return MRN_ERR_CUDA;
+    }
+    return MRN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mrn_status mrn_rmsnorm(const void *x, const void *gamma, void *y, int64_t rows, int64_t n,
+                       float eps, mrn_dtype dtype, cudaStream_t stream) {
+    mrn_status st = check_common(rows, n, dtype, eps, eps);
+    if (st != MRN_OK || rows == 0) return st;
+    if (!x || !gamma || !y) return MRN_ERR_NULL_POINTER;
+    const int64_t e = elem_bytes(dtype);
+    if (!aligned_to(x, e) || !aligned_to(gamma, e) || !aligned_to(y, e))
+        return MRN_ERR_MISALIGNED;
+    const int64_t row_bytes = rows * n * e;
+    const Span sx = span_of(x, row_bytes), sg = span_of(gamma, n * e), sy = span_of(y, row_bytes);
+    if (!output_vs_row_input_ok(sy, sx) || overlaps(sy, sg)) return MRN_ERR_ALIASING;
+    const bool a16 = (n * e) % 16 == 0 && aligned_to(x, 16) && aligned_to(gamma, 16) &&
+                     aligned_to(y, 16);
+    Call c{mrn::kRmsnorm, dtype, rows, n, KernelArgs{}};
+    c.args.x = x;
+    c.args.g1 = gamma;
+    c.args.y = y;
+    c.args.eps1 = eps;
+    c.args.eps2 = eps;
+    return launch(c, a16, stream);
+}
+
+mrn_status mrn_rmsnorm_then_add(const void *x, const void *gamma, const void *residual, void *out,
+                                int64_t rows, int64_t n, float eps, mrn_dtype dtype,
+                                cudaStream_t stream) {
+    mrn_status st = check_common(rows, n, dtype, eps, eps);
+    if (st != MRN_OK || rows == 0) return st;
+    if (!x || !gamma || !residual || !out) return MRN_ERR_NULL_POINTER;
+    const int64_t e = elem_bytes(dtype);
+    if (!aligned_to(x, e) || !aligned_to(gamma, e) || !aligned_to(residual, e) ||
+        !aligned_to(out, e))
+        return MRN_ERR_MISALIGNED;
+    const int64_t row_bytes = rows * n * e;
+    const Span sx = span_of(x, row_bytes), sr = span_of(residual, row_bytes);
+    const Span sg = span_of(gamma, n * e), so = span_of(out, row_bytes);
+    if (!output_vs_row_input_ok(so, sx) || !output_vs_row_input_ok(so, sr) || overlaps(so, sg))
+        return MRN_ERR_ALIASING;
+    const bool a16 = (n * e) % 16 == 0 && aligned_to(x, 16) && aligned_to(gamma, 16) &&
+                     aligned_to(residual, 16) && aligned_to(out, 16);
+    Call c{mrn::kThenAdd, dtype, rows, n, KernelArgs{}};
+    c.args.x = x;
+    c.args.res = residual;
+    c.args.g1 = gamma;
+    c.args.y = out;
+    c.args.eps1 = eps;
+    c.args.eps2 = eps;
+    return launch(c, a16, stream);
+}
+
+mrn_status mrn_norm_residual_norm(const void *block_out, const void *residual,
+                                  const void *gamma_post, const void *gamma_pre,
+                                  void *out_stream, void *normed, int64_t rows, int64_t n,
+                                  float eps_post, float eps_pre, mrn_dtype dtype,
+                                  cudaStream_t stream) {
+    mrn_status st = check_common(rows, n, dtype, eps_post, eps_pre);
+    if (st != MRN_OK || rows == 0) return st;
+    if (!block_out || !residual || !gamma_post || !gamma_pre || !out_stream || !normed)
+        return MRN_ERR_NULL_POINTER;
+    const int64_t e = elem_bytes(dtype);
+    if (!aligned_to(block_out, e) || !aligned_to(residual, e) || !aligned_to(gamma_post, e) ||
+        !aligned_to(gamma_pre, e) || !aligned_to(out_stream, e) || !aligned_to(normed, e))
+        return MRN_ERR_MISALIGNED;
+    const int64_t row_bytes = rows * n * e;
+    const Span sb = span_of(block_out, row_bytes), sr = span_of(residual, row_bytes);
+    const Span sgp = span_of(gamma_post, n * e), sgq = span_of(gamma_pre, n * e);
+    const Span ss = span_of(out_stream, row_bytes), sn = span_of(normed, row_bytes);
+    if (!output_vs_row_input_ok(ss, sb) || !output_vs_row_input_ok(ss, sr) ||
+        !output_vs_row_input_ok(sn, sb) || !output_vs_row_input_ok(sn, sr) || overlaps(ss, sn) ||
+        overlaps(ss, sgp) || overlaps(ss, sgq) || overlaps(sn, sgp) || overlaps(sn, sgq))
+        return MRN_ERR_ALIASING;
+    const bool a16 = (n * e) % 16 == 0 && aligned_to(block_out, 16) && aligned_to(residual, 16) &&
+                     aligned_to(gamma_post, 16) && aligned_to(gamma_pre, 16) &&
+                     aligned_to(out_stream, 16) && aligned_to(normed, 16);
+    Call c{mrn::kSandwich, dtype, rows, n, KernelArgs{}};
+    c.args.x = block_out;
+    c.args.res = residual;
+    c.args.g1 = gamma_post;
+    c.args.g2 = gamma_pre;
+    c.args.y = out_stream;
+    c.args.y2 = normed;
+    c.args.eps1 = eps_post;
+    c.args.eps2 = eps_pre;
+    return launch(c, a16, stream);
+}
+
+const char *mrn_status_string(mrn_status status) {
+    switch (status) {
+    case MRN_OK: return "ok";
+    case MRN_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case MRN_ERR_INVALID_SIZE: return "invalid size (n < 1, rows < 0 or byte size overflow)";
+    case MRN_ERR_INVALID_EPS: return "eps must be finite and > 0";
+    case MRN_ERR_UNSUPPORTED_DTYPE: return "unsupported dtype";
+    case MRN_ERR_ALIASING: return "forbidden overlap between buffers";
+    case MRN_ERR_MISALIGNED: return "pointer not aligned to its element size";
+    case MRN_ERR_CUDA: return "CUDA launch failed (see mrn_last_cuda_error)";
+    case MRN_ERR_INVALID_GEOMETRY: return "forced geometry cannot cover this call";
+    }
+    return "unknown status";
+}
+
+int mrn_last_cuda_error(void) { return t_last_cuda_error; }
+
+mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtype,
+                              int32_t aligned16, int32_t sm_count, mrn_geometry *out) {
+    if (!out) return MRN_ERR_NULL_POINTER;
+    if (op != MRN_OP_RMSNORM && op != MRN_OP_THEN_ADD && op != MRN_OP_SANDWICH)
+        return MRN_ERR_INVALID_GEOMETRY;
+    mrn_status st = check_common(rows, n, dtype, 1.0f, 1.0f);
+    if (st != MRN_OK) return st;
+    const bool a16 = aligned16 != 0 && (n * elem_bytes(dtype)) % 16 == 0;
+    Geometry g;
+    if (t_forced) {
+        if (!resolve_forced(t_forced_geometry, n, dtype, a16, &g)) return MRN_ERR_INVALID_GEOMETRY;
+    } else {
+        g = choose_geometry(rows, n, dtype, a16, sm_count > 0 ? sm_count : sm_count_of_current_device());
+    }
+    out->kind = g.kind;
+    out->vec = g.vec;
+    out->k = g.k;
+    out->threads = g.threads;
+    out->cluster = g.cluster;
+    out->lanes_per_row = g.lanes;
+    out->rows_per_cta = g.rows_per_cta;
+    return MRN_OK;
+}
+
+mrn_status mrn_force_geometry(const mrn_geometry *geometry) {
+    if (!geometry || geometry->kind == MRN_GEOM_AUTO) {
+        t_forced = false;
+        return MRN_OK;
+    }
+    Geometry g = {};
+    g.kind = geometry->kind;
+    g.vec = geometry->vec;
+    g.k = geometry->k;
+    g.threads = geometry->threads;
+    g.cluster = geometry->cluster;
+    g.lanes = geometry->lanes_per_row;
+    if (g.kind == mrn::kRowsPerWarp && g.threads == 0) g.threads = mrn::kWarpKernelThreads;
+    if (g.kind == mrn::kStream) g.k = 1;
+    if (g.kind != mrn::kCta) g.cluster = 1;
+    if (!geometry_is_consistent(g) || g.vec < 0) return MRN_ERR_INVALID_GEOMETRY;
+    t_forced_geometry = g;
+    t_forced = true;
+    return MRN_OK;
+}
+
+uint64_t mrn_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
+
+}  // extern "C"

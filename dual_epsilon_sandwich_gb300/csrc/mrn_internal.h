@@ -1,0 +1,57 @@
+// mrn_internal.h -- host-side interface between the C ABI layer (mrn_api.cpp)
+// and the kernel launchers (mrn_ops_*.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace mrn {
+
+enum Op : int { kRmsnorm = 0, kThenAdd = 1, kSandwich = 2 };
+enum Kind : int { kAuto = 0, kRowsPerWarp = 1, kCta = 2, kStream = 3 };
+
+// Launch-time view of one call.  Pointers are device pointers; row operands
+// are [rows x n] row-major.  For the sandwich, x = block_out, res = residual,
+// g1 = gamma_post, g2 = gamma_pre, y = out_stream, y2 = normed.
+struct KernelArgs {
+    const void *x;
+    const void *res;
+    const void *g1;
+    const void *g2;
+    void *y;
+    void *y2;
+    int64_t n;         // elements per row
+    int64_t nvec;      // loads per row = ceil(n / vec)
+    int64_t row0;      // first row of this launch
+    int64_t rows_end;  // one past the last row of this launch
+    float eps1;        // eps (rmsnorm, then-add) or eps_post (sandwich)
+    float eps2;        // eps_pre (sandwich)
+};
+
+struct Geometry {
+    int kind;          // Kind
+    int vec;           // elements per load
+    int k;             // loads per operand per thread
+    int threads;       // threads per CTA
+    int cluster;       // CTAs per row (kCta)
+    int lanes;         // threads per row (kRowsPerWarp)
+    int rows_per_cta;
+};
+
+// Register-slot limits per thread count: the kernels are compiled with these
+// launch bounds so that every (k, threads <= max) pair can launch.
+constexpr int kMaxK = 8;
+constexpr int kWarpKernelThreads = 256;
+constexpr int kStreamMaxThreads = 512;
+constexpr int kMaxCluster = 16;
+constexpr int cta_max_threads(int k) { return k <= 2 ? 1024 : (k <= 4 ? 512 : 256); }
+
+// One launcher per operation; each returns the CUDA error of the launch(es).
+cudaError_t launch_rmsnorm(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
+                           cudaStream_t stream, uint64_t *launches);
+cudaError_t launch_then_add(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
+                            cudaStream_t stream, uint64_t *launches);
+cudaError_t launch_sandwich(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
+                            cudaStream_t stream, uint64_t *launches);
+
+}  // namespace mrn

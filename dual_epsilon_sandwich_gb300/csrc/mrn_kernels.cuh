@@ -1,0 +1,547 @@
+// mrn_kernels.cuh -- sm_103a kernels for RMSNorm, post-norm-then-add and the
+// dual-epsilon sandwich tail.
+//
+// The computation ("Chapter 12 -- RMSNorm and the dual-epsilon sandwich",
+// sections 12.1 and 12.4.3; Hesper "RMSNorm Layer", rmsNormThenAddKernel):
+//   inv = 1 / sqrt(sum_j v_j^2 / n + eps)            (f32, IEEE sqrt and divide)
+//   rmsnorm   y = (x * inv) * gamma
+//   then-add  out = fma(x * inv, gamma, residual)
+//   sandwich  s = fma(b * inv(b; eps_post), gamma_post, residual)   -> stored
+//             normed = (s * inv(s; eps_pre)) * gamma_pre           (s as stored)
+//
+// Design for a bandwidth-bound row reduction on GB300:
+//  * every operand element is read from HBM once and every output written
+//    once: the row (and the residual) stay in registers between the
+//    reduction and the output pass;
+//  * 16-byte vector loads/stores (4 x f32 or 8 x bf16), consecutive lanes on
+//    consecutive vectors, so a warp moves 512 contiguous bytes per access;
+//    streaming operands bypass L1 (L1::no_allocate) and ask L2 for 256-byte
+//    prefetch; gamma goes through the read-only path and stays cached;
+//  * reductions: butterfly shuffles (every lane ends with the same bits),
+//    then one shared-memory slot per warp, then -- for rows split over a
+//    thread-block cluster -- one DSMEM slot per CTA written into every peer
+//    and a release/acquire cluster barrier.  Every CTA sums the same partials
+//    in the same order, so all CTAs of a row use bit-identical inv;
+//  * three geometries: several rows per warp (small n), one row per CTA or
+//    per cluster (register resident, mid to large n), and a looped
+//    fallback for rows too wide for registers.
+// No kernel waits on a flag, a peer or an mbarrier; the only inter-CTA
+// synchronisation is the hardware cluster barrier, which every thread of
+// every CTA of the cluster reaches unconditionally.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "mrn_internal.h"
+
+namespace mrn {
+
+struct F32 { static constexpr int kBytes = 4; };
+struct BF16 { static constexpr int kBytes = 2; };
+
+// ---------------------------------------------------------------------------
+// Register fragments: VEC elements of one operand, kept as raw bits.
+// ---------------------------------------------------------------------------
+template <class T, int VEC> struct Frag;
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);   // round to nearest even
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <> struct Frag<F32, 4> {
+    uint32_t w[4];
+    __device__ __forceinline__ void zero() { w[0] = w[1] = w[2] = w[3] = 0u; }
+    __device__ __forceinline__ float get(int i) const { return __uint_as_float(w[i]); }
+    __device__ __forceinline__ void put(const float (&f)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = __float_as_uint(f[i]);
+    }
+};
+
+template <> struct Frag<BF16, 8> {
+    uint32_t w[4];
+    __device__ __forceinline__ void zero() { w[0] = w[1] = w[2] = w[3] = 0u; }
+    __device__ __forceinline__ float get(int i) const {
+        const uint32_t u = w[i >> 1];
+        return (i & 1) ? __uint_as_float(u & 0xFFFF0000u) : __uint_as_float(u << 16);
+    }
+    __device__ __forceinline__ void put(const float (&f)[8]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+    }
+};
+
+template <> struct Frag<F32, 1> {
+    uint32_t w;
+    __device__ __forceinline__ void zero() { w = 0u; }
+    __device__ __forceinline__ float get(int) const { return __uint_as_float(w); }
+    __device__ __forceinline__ void put(const float (&f)[1]) { w = __float_as_uint(f[0]); }
+};
+
+template <> struct Frag<BF16, 1> {
+    unsigned short h;
+    __device__ __forceinline__ void zero() { h = 0; }
+    __device__ __forceinline__ float get(int) const {
+        return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    }
+    __device__ __forceinline__ void put(const float (&f)[1]) {
+        h = __bfloat16_as_ushort(__float2bfloat16_rn(f[0]));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Global memory access.  `stream` = operand read once (bypass L1, 256-byte L2
+// prefetch); `ro` = read-only, cached (gamma); `st` = plain store; `ld` =
+// plain coherent load (re-reading data this thread stored earlier).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ld_stream(Frag<F32, 4> &f, const void *p) {
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(Frag<BF16, 8> &f, const void *p) {
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(Frag<F32, 1> &f, const void *p) {
+    asm volatile("ld.global.L1::no_allocate.u32 %0, [%1];" : "=r"(f.w) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(Frag<BF16, 1> &f, const void *p) {
+    asm volatile("ld.global.L1::no_allocate.u16 %0, [%1];" : "=h"(f.h) : "l"(p));
+}
+
+__device__ __forceinline__ void ld_ro(Frag<F32, 4> &f, const void *p) {
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p));
+}
+__device__ __forceinline__ void ld_ro(Frag<BF16, 8> &f, const void *p) {
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p));
+}
+__device__ __forceinline__ void ld_ro(Frag<F32, 1> &f, const void *p) {
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(f.w) : "l"(p));
+}
+__device__ __forceinline__ void ld_ro(Frag<BF16, 1> &f, const void *p) {
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(f.h) : "l"(p));
+}
+
+__device__ __forceinline__ void ld_plain(Frag<F32, 4> &f, const void *p) {
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void ld_plain(Frag<BF16, 8> &f, const void *p) {
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void ld_plain(Frag<F32, 1> &f, const void *p) {
+    asm volatile("ld.global.u32 %0, [%1];" : "=r"(f.w) : "l"(p) : "memory");
+}
+__device__ __forceinline__ void ld_plain(Frag<BF16, 1> &f, const void *p) {
+    asm volatile("ld.global.u16 %0, [%1];" : "=h"(f.h) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ void st_global(void *p, const Frag<F32, 4> &f) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(f.w[0]), "r"(f.w[1]), "r"(f.w[2]), "r"(f.w[3]) : "memory");
+}
+__device__ __forceinline__ void st_global(void *p, const Frag<BF16, 8> &f) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(f.w[0]), "r"(f.w[1]), "r"(f.w[2]), "r"(f.w[3]) : "memory");
+}
+__device__ __forceinline__ void st_global(void *p, const Frag<F32, 1> &f) {
+    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(f.w) : "memory");
+}
+__device__ __forceinline__ void st_global(void *p, const Frag<BF16, 1> &f) {
+    asm volatile("st.global.u16 [%0], %1;" :: "l"(p), "h"(f.h) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Reductions
+// ---------------------------------------------------------------------------
+// Butterfly sum over `width` lanes (a power of two <= 32).  Both operands of
+// every addition are the same on the two partner lanes and f32 addition is
+// commutative, so all lanes of a group end with bit-identical sums.
+__device__ __forceinline__ float group_allsum(float v, int width) {
+    for (int o = width >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_allsum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ unsigned cluster_nctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_index_x() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Store v into the shared-memory word `local` of CTA `rank` of this cluster.
+__device__ __forceinline__ void st_cluster_f32(float *local, unsigned rank, float v) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(local));
+    unsigned remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(remote), "f"(v) : "memory");
+}
+
+struct ReduceSlots {
+    float warp[32];
+    float cta[kMaxCluster];
+};
+
+// Sum of v over all threads of the CTA and, when cl > 1, over all CTAs of
+// the cluster.  Every thread of every CTA must call it (it contains
+// __syncthreads and cluster barriers).  `first` marks the first cluster
+// reduction of the kernel: it completes the arrive issued at kernel start,
+// which guarantees every peer CTA is running before its shared memory is
+// written.
+__device__ __forceinline__ float cta_allsum(float v, ReduceSlots &s, unsigned cl, unsigned crank,
+                                            bool first) {
+    v = warp_allsum(v);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    if (lane == 0) s.warp[warp] = v;
+    __syncthreads();
+    float t = warp_allsum(lane < nwarps ? s.warp[lane] : 0.0f);
+    if (cl > 1) {
+        if (first) cluster_wait_acquire();
+        if (threadIdx.x < cl) st_cluster_f32(&s.cta[crank], threadIdx.x, t);
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        t = warp_allsum(lane < static_cast<int>(cl) ? s.cta[lane] : 0.0f);
+    }
+    return t;
+}
+
+__device__ __forceinline__ float inv_rms(float sum_sq, int64_t n, float eps) {
+    return 1.0f / sqrtf(sum_sq / static_cast<float>(n) + eps);
+}
+
+template <class T, int VEC>
+__device__ __forceinline__ float frag_sum_sq(const Frag<T, VEC> &f) {
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) s = fmaf(f.get(i), f.get(i), s);
+    return s;
+}
+
+template <class T> __device__ __forceinline__ const char *elem_ptr(const void *base, int64_t e) {
+    return static_cast<const char *>(base) + e * T::kBytes;
+}
+template <class T> __device__ __forceinline__ char *elem_ptr(void *base, int64_t e) {
+    return static_cast<char *>(base) + e * T::kBytes;
+}
+
+// y = (x * inv) * g
+template <class T, int VEC>
+__device__ __forceinline__ Frag<T, VEC> apply_norm(const Frag<T, VEC> &x, float inv,
+                                                    const Frag<T, VEC> &g) {
+    float o[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) o[i] = (x.get(i) * inv) * g.get(i);
+    Frag<T, VEC> r;
+    r.put(o);
+    return r;
+}
+
+// out = fma(x * inv, g, r)
+template <class T, int VEC>
+__device__ __forceinline__ Frag<T, VEC> apply_norm_add(const Frag<T, VEC> &x, float inv,
+                                                        const Frag<T, VEC> &g,
+                                                        const Frag<T, VEC> &r) {
+    float o[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) o[i] = fmaf(x.get(i) * inv, g.get(i), r.get(i));
+    Frag<T, VEC> out;
+    out.put(o);
+    return out;
+}
+
+// ---------------------------------------------------------------------------
+// Row body shared by the register-resident kernels.  A "slot" k of this
+// thread holds load index v = first + k * stride of the row (masked when
+// v >= nvec).  `Reduce` sums a float over all threads of the row.
+// ---------------------------------------------------------------------------
+template <int OP, class T, int VEC, int K, class Reduce1, class Reduce2>
+__device__ __forceinline__ void row_body(const KernelArgs &a, int64_t row, bool row_ok,
+                                         int64_t first, int64_t stride, Reduce1 reduce1,
+                                         Reduce2 reduce2) {
+    using Fr = Frag<T, VEC>;
+    const int64_t row_elem = row * a.n;
+    Fr xv[K];
+    Fr rv[K];
+    Fr gv[K];
+    bool ok[K];
+    // All loads of the row are issued before the first reduction: the row, the
+    // residual and the first gamma are in flight together.
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int64_t v = first + k * stride;
+        ok[k] = row_ok && v < a.nvec;
+        const int64_t e = row_elem + v * VEC;
+        if (ok[k]) {
+            ld_stream(xv[k], elem_ptr<T>(a.x, e));
+            if (OP != kRmsnorm) ld_stream(rv[k], elem_ptr<T>(a.res, e));
+        } else {
+            xv[k].zero();
+            rv[k].zero();
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (ok[k]) ld_ro(gv[k], elem_ptr<T>(a.g1, (first + k * stride) * VEC));
+    }
+
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) ss += frag_sum_sq(xv[k]);
+    const float inv1 = inv_rms(reduce1(ss), a.n, a.eps1);
+
+    if (OP == kRmsnorm || OP == kThenAdd) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (!ok[k]) continue;
+            const int64_t v = first + k * stride;
+            const Fr o = (OP == kRmsnorm) ? apply_norm(xv[k], inv1, gv[k])
+                                          : apply_norm_add(xv[k], inv1, gv[k], rv[k]);
+            st_global(elem_ptr<T>(a.y, row_elem + v * VEC), o);
+        }
+        return;
+    }
+
+    // Sandwich: stream = fma(b * inv_post, gamma_post, residual), stored, and its
+    // stored (rounded) value feeds the second reduction and the pre norm.
+    float ss2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (!ok[k]) continue;
+        const int64_t v = first + k * stride;
+        rv[k] = apply_norm_add(xv[k], inv1, gv[k], rv[k]);
+        st_global(elem_ptr<T>(a.y, row_elem + v * VEC), rv[k]);
+        ss2 += frag_sum_sq(rv[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (ok[k]) ld_ro(gv[k], elem_ptr<T>(a.g2, (first + k * stride) * VEC));
+    }
+    const float inv2 = inv_rms(reduce2(ss2), a.n, a.eps2);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (!ok[k]) continue;
+        const int64_t v = first + k * stride;
+        st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(rv[k], inv2, gv[k]));
+    }
+}
+
+// Several rows per warp: `lanes` (power of two <= 32) threads per row, K
+// register slots each; 256 threads per CTA.
+template <int OP, class T, int VEC, int K>
+__global__ void __launch_bounds__(kWarpKernelThreads)
+mrn_rows_per_warp_kernel(const KernelArgs a, const int lanes) {
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t row = a.row0 + gtid / lanes;
+    const int lane_in_row = threadIdx.x & (lanes - 1);
+    auto reduce = [lanes](float v) { return group_allsum(v, lanes); };
+    row_body<OP, T, VEC, K>(a, row, row < a.rows_end, lane_in_row, lanes, reduce, reduce);
+}
+
+// One row per CTA, or per cluster of cl CTAs (launched with a cluster
+// dimension); CTA `rank` covers loads [rank*threads*K, (rank+1)*threads*K).
+template <int OP, class T, int VEC, int K>
+__global__ void __launch_bounds__(cta_max_threads(K))
+mrn_cta_kernel(const KernelArgs a) {
+    __shared__ ReduceSlots slots1;
+    __shared__ ReduceSlots slots2;
+    const unsigned cl = cluster_nctarank();
+    const unsigned crank = cluster_ctarank();
+    if (cl > 1) cluster_arrive_relaxed();
+    const int64_t row = a.row0 + cluster_index_x();
+    const int64_t first = static_cast<int64_t>(crank) * blockDim.x * K + threadIdx.x;
+    auto reduce1 = [&](float v) { return cta_allsum(v, slots1, cl, crank, true); };
+    auto reduce2 = [&](float v) { return cta_allsum(v, slots2, cl, crank, false); };
+    row_body<OP, T, VEC, K>(a, row, true, first, blockDim.x, reduce1, reduce2);
+}
+
+// Looped fallback for rows wider than the register-resident geometries
+// hold: one row per CTA, the row is read once for the sum and once more for
+// the output (the second read is usually served by L2).  The sandwich's pre
+// norm re-reads the stream values this same thread stored.  Each iteration
+// handles kStreamUnroll loads per operand so that several are in flight.
+constexpr int kStreamUnroll = 4;
+
+template <int OP, class T, int VEC>
+__global__ void __launch_bounds__(kStreamMaxThreads)
+mrn_stream_kernel(const KernelArgs a) {
+    using Fr = Frag<T, VEC>;
+    constexpr int U = kStreamUnroll;
+    __shared__ ReduceSlots slots1;
+    __shared__ ReduceSlots slots2;
+    const int64_t row = a.row0 + blockIdx.x;
+    const int64_t row_elem = row * a.n;
+    const int64_t nt = blockDim.x;
+
+    float ss = 0.0f;
+    for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
+        Fr x[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * nt;
+            if (v < a.nvec) ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
+            else x[u].zero();
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) ss += frag_sum_sq(x[u]);
+    }
+    const float inv1 = inv_rms(cta_allsum(ss, slots1, 1, 0, false), a.n, a.eps1);
+
+    float ss2 = 0.0f;
+    for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
+        Fr x[U], g[U], r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * nt;
+            if (v < a.nvec) {
+                ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
+                ld_ro(g[u], elem_ptr<T>(a.g1, v * VEC));
+                if (OP != kRmsnorm) ld_stream(r[u], elem_ptr<T>(a.res, row_elem + v * VEC));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * nt;
+            if (v >= a.nvec) continue;
+            const int64_t e = row_elem + v * VEC;
+            if (OP == kRmsnorm) {
+                st_global(elem_ptr<T>(a.y, e), apply_norm(x[u], inv1, g[u]));
+            } else {
+                const Fr o = apply_norm_add(x[u], inv1, g[u], r[u]);
+                st_global(elem_ptr<T>(a.y, e), o);
+                if (OP == kSandwich) ss2 += frag_sum_sq(o);
+            }
+        }
+    }
+    if (OP != kSandwich) return;
+
+    const float inv2 = inv_rms(cta_allsum(ss2, slots2, 1, 0, false), a.n, a.eps2);
+    for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
+        Fr s[U], g[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * nt;
+            if (v < a.nvec) {
+                ld_plain(s[u], elem_ptr<T>(a.y, row_elem + v * VEC));
+                ld_ro(g[u], elem_ptr<T>(a.g2, v * VEC));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * nt;
+            if (v < a.nvec)
+                st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(s[u], inv2, g[u]));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launch of one operation (instantiated once per .cu file).
+// ---------------------------------------------------------------------------
+using WarpKernelFn = void (*)(KernelArgs, int);
+using CtaKernelFn = void (*)(KernelArgs);
+
+template <int OP, class T, int VEC> struct KernelTable {
+    static constexpr WarpKernelFn warp[kMaxK] = {
+        mrn_rows_per_warp_kernel<OP, T, VEC, 1>, mrn_rows_per_warp_kernel<OP, T, VEC, 2>,
+        mrn_rows_per_warp_kernel<OP, T, VEC, 3>, mrn_rows_per_warp_kernel<OP, T, VEC, 4>,
+        mrn_rows_per_warp_kernel<OP, T, VEC, 5>, mrn_rows_per_warp_kernel<OP, T, VEC, 6>,
+        mrn_rows_per_warp_kernel<OP, T, VEC, 7>, mrn_rows_per_warp_kernel<OP, T, VEC, 8>};
+    static constexpr CtaKernelFn cta[kMaxK] = {
+        mrn_cta_kernel<OP, T, VEC, 1>, mrn_cta_kernel<OP, T, VEC, 2>,
+        mrn_cta_kernel<OP, T, VEC, 3>, mrn_cta_kernel<OP, T, VEC, 4>,
+        mrn_cta_kernel<OP, T, VEC, 5>, mrn_cta_kernel<OP, T, VEC, 6>,
+        mrn_cta_kernel<OP, T, VEC, 7>, mrn_cta_kernel<OP, T, VEC, 8>};
+    static constexpr CtaKernelFn stream = mrn_stream_kernel<OP, T, VEC>;
+};
+
+// Rows per launch, so that grid.x stays far below 2^31 - 1 for any cluster.
+constexpr int64_t kRowsPerLaunch = int64_t(1) << 26;
+
+template <int OP, class T, int VEC>
+cudaError_t launch_typed(const Geometry &g, KernelArgs a, int64_t rows, cudaStream_t stream,
+                         uint64_t *launches) {
+    using Tab = KernelTable<OP, T, VEC>;
+    for (int64_t r0 = 0; r0 < rows; r0 += kRowsPerLaunch) {
+        const int64_t nrows = rows - r0 < kRowsPerLaunch ? rows - r0 : kRowsPerLaunch;
+        a.row0 = r0;
+        a.rows_end = r0 + nrows;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        cfg.blockDim = dim3(g.threads, 1, 1);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaError_t err;
+        if (g.kind == kRowsPerWarp) {
+            const int64_t rpc = g.threads / g.lanes;
+            cfg.gridDim = dim3(static_cast<unsigned>((nrows + rpc - 1) / rpc), 1, 1);
+            err = cudaLaunchKernelEx(&cfg, Tab::warp[g.k - 1], a, g.lanes);
+        } else if (g.kind == kCta) {
+            const CtaKernelFn fn = Tab::cta[g.k - 1];
+            cfg.gridDim = dim3(static_cast<unsigned>(nrows * g.cluster), 1, 1);
+            if (g.cluster > 1) {
+                if (g.cluster > 8) {
+                    err = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                    if (err != cudaSuccess) return err;
+                }
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = static_cast<unsigned>(g.cluster);
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+            }
+            err = cudaLaunchKernelEx(&cfg, fn, a);
+        } else {
+            cfg.gridDim = dim3(static_cast<unsigned>(nrows), 1, 1);
+            err = cudaLaunchKernelEx(&cfg, Tab::stream, a);
+        }
+        if (err != cudaSuccess) return err;
+        ++*launches;
+    }
+    return cudaSuccess;
+}
+
+template <int OP>
+cudaError_t launch_op(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
+                      cudaStream_t stream, uint64_t *launches) {
+    if (bf16) {
+        return g.vec == 1 ? launch_typed<OP, BF16, 1>(g, a, rows, stream, launches)
+                          : launch_typed<OP, BF16, 8>(g, a, rows, stream, launches);
+    }
+    return g.vec == 1 ? launch_typed<OP, F32, 1>(g, a, rows, stream, launches)
+                      : launch_typed<OP, F32, 4>(g, a, rows, stream, launches);
+}
+
+}  // namespace mrn

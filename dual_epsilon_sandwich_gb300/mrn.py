@@ -1,0 +1,247 @@
+"""Python binding of libmrn (``include/mrn.h``): argument marshalling only.
+
+The functions named ``mrn_*`` mirror the C ABI one to one: pointers are plain
+integers (device addresses), sizes are ints, the stream is a ``cudaStream_t``
+handle as an int (0 = legacy default stream), and each returns the
+``mrn_status`` code.  ``rmsnorm``, ``rmsnorm_then_add`` and
+``norm_residual_norm`` are conveniences for torch CUDA tensors: they read
+pointers, sizes, dtype and the current stream off the tensors, call the C ABI
+and raise ``MrnError`` on a non-zero status.  Every step of the computation
+runs in the library's CUDA kernels; there is no other code path.  If
+``libmrn.so`` has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(PKG, "libmrn.so")
+
+MRN_F32 = 0
+MRN_BF16 = 1
+
+MRN_OP_RMSNORM = 0
+MRN_OP_THEN_ADD = 1
+MRN_OP_SANDWICH = 2
+
+MRN_GEOM_AUTO = 0
+MRN_GEOM_ROWS_PER_WARP = 1
+MRN_GEOM_CTA = 2
+MRN_GEOM_STREAM = 3
+
+STATUS = {
+    0: "MRN_OK",
+    1: "MRN_ERR_NULL_POINTER",
+    2: "MRN_ERR_INVALID_SIZE",
+    3: "MRN_ERR_INVALID_EPS",
+    4: "MRN_ERR_UNSUPPORTED_DTYPE",
+    5: "MRN_ERR_ALIASING",
+    6: "MRN_ERR_MISALIGNED",
+    7: "MRN_ERR_CUDA",
+    8: "MRN_ERR_INVALID_GEOMETRY",
+}
+for _code, _name in STATUS.items():
+    globals()[_name] = _code
+
+EXPORTS = ("mrn_rmsnorm", "mrn_rmsnorm_then_add", "mrn_norm_residual_norm",
+           "mrn_status_string", "mrn_last_cuda_error", "mrn_query_geometry",
+           "mrn_force_geometry", "mrn_launch_count")
+
+
+class MrnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        name = STATUS.get(status, str(status))
+        detail = mrn_status_string(status)
+        if status == 7:
+            detail += f" (cudaError {mrn_last_cuda_error()})"
+        super().__init__(f"{what}: {name}: {detail}" if what else f"{name}: {detail}")
+
+
+class MrnGeometry(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("vec", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("threads", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("lanes_per_row", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_f = ctypes.c_float
+_i = ctypes.c_int
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmrn.so.  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIBRARY):
+                raise RuntimeError(
+                    f"{LIBRARY} is not built; run dual_epsilon_sandwich_gb300._build.build() "
+                    "(or __graft_entry__.build()) first")
+            L = ctypes.CDLL(LIBRARY)
+            L.mrn_rmsnorm.argtypes = [_vp, _vp, _vp, _i64, _i64, _f, _i, _vp]
+            L.mrn_rmsnorm_then_add.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _f, _i, _vp]
+            L.mrn_norm_residual_norm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                                                 _f, _f, _i, _vp]
+            for fn in (L.mrn_rmsnorm, L.mrn_rmsnorm_then_add, L.mrn_norm_residual_norm):
+                fn.restype = _i
+            L.mrn_status_string.argtypes = [_i]
+            L.mrn_status_string.restype = ctypes.c_char_p
+            L.mrn_last_cuda_error.argtypes = []
+            L.mrn_last_cuda_error.restype = _i
+            L.mrn_query_geometry.argtypes = [_i, _i64, _i64, _i, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.POINTER(MrnGeometry)]
+            L.mrn_query_geometry.restype = _i
+            L.mrn_force_geometry.argtypes = [ctypes.POINTER(MrnGeometry)]
+            L.mrn_force_geometry.restype = _i
+            L.mrn_launch_count.argtypes = []
+            L.mrn_launch_count.restype = ctypes.c_uint64
+            _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------------------
+# The C ABI, one to one
+# ---------------------------------------------------------------------------
+def mrn_rmsnorm(x, gamma, y, rows, n, eps, dtype, stream=0) -> int:
+    return lib().mrn_rmsnorm(x, gamma, y, rows, n, eps, dtype, stream)
+
+
+def mrn_rmsnorm_then_add(x, gamma, residual, out, rows, n, eps, dtype, stream=0) -> int:
+    return lib().mrn_rmsnorm_then_add(x, gamma, residual, out, rows, n, eps, dtype, stream)
+
+
+def mrn_norm_residual_norm(block_out, residual, gamma_post, gamma_pre, out_stream, normed,
+                           rows, n, eps_post, eps_pre, dtype, stream=0) -> int:
+    return lib().mrn_norm_residual_norm(block_out, residual, gamma_post, gamma_pre, out_stream,
+                                        normed, rows, n, eps_post, eps_pre, dtype, stream)
+
+
+def mrn_status_string(status: int) -> str:
+    return lib().mrn_status_string(status).decode()
+
+
+def mrn_last_cuda_error() -> int:
+    return lib().mrn_last_cuda_error()
+
+
+def mrn_query_geometry(op, rows, n, dtype, aligned16=True, sm_count=0) -> dict:
+    g = MrnGeometry()
+    st = lib().mrn_query_geometry(op, rows, n, dtype, 1 if aligned16 else 0, sm_count,
+                                  ctypes.byref(g))
+    if st != 0:
+        raise MrnError(st, "mrn_query_geometry")
+    return g.as_dict()
+
+
+def mrn_force_geometry(geometry: dict | None) -> int:
+    """Force the calling thread's geometry (None restores the automatic choice)."""
+    if geometry is None:
+        return lib().mrn_force_geometry(None)
+    g = MrnGeometry(**{k: int(v) for k, v in geometry.items() if k != "rows_per_cta"})
+    return lib().mrn_force_geometry(ctypes.byref(g))
+
+
+def mrn_launch_count() -> int:
+    return lib().mrn_launch_count()
+
+
+# ---------------------------------------------------------------------------
+# torch tensor conveniences (marshalling only)
+# ---------------------------------------------------------------------------
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return MRN_F32
+    if t.dtype == torch.bfloat16:
+        return MRN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float32 or bfloat16")
+
+
+def _check(t, name, dtype, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _rows_n(x):
+    n = x.shape[-1]
+    rows = x.numel() // n if n else 0
+    return rows, n
+
+
+def _stream(t):
+    import torch
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def rmsnorm(x, gamma, eps: float, out=None):
+    """y = RMSNorm(x) * gamma over the last dimension; out may be x."""
+    import torch
+    dt = _dtype_code(x)
+    _check(x, "x", x.dtype)
+    rows, n = _rows_n(x)
+    _check(gamma, "gamma", x.dtype, (n,))
+    out = torch.empty_like(x) if out is None else out
+    _check(out, "out", x.dtype, x.shape)
+    st = mrn_rmsnorm(x.data_ptr(), gamma.data_ptr(), out.data_ptr(), rows, n, eps, dt,
+                     _stream(x))
+    if st != 0:
+        raise MrnError(st, "mrn_rmsnorm")
+    return out
+
+
+def rmsnorm_then_add(x, gamma, residual, eps: float, out=None):
+    """out = RMSNorm(x) * gamma + residual; out may be x or residual."""
+    import torch
+    dt = _dtype_code(x)
+    _check(x, "x", x.dtype)
+    rows, n = _rows_n(x)
+    _check(gamma, "gamma", x.dtype, (n,))
+    _check(residual, "residual", x.dtype, x.shape)
+    out = torch.empty_like(x) if out is None else out
+    _check(out, "out", x.dtype, x.shape)
+    st = mrn_rmsnorm_then_add(x.data_ptr(), gamma.data_ptr(), residual.data_ptr(),
+                              out.data_ptr(), rows, n, eps, dt, _stream(x))
+    if st != 0:
+        raise MrnError(st, "mrn_rmsnorm_then_add")
+    return out
+
+
+def norm_residual_norm(block_out, residual, gamma_post, gamma_pre, eps_post: float = 1e-8,
+                       eps_pre: float = 1e-5, out_stream=None, normed=None):
+    """(out_stream, normed) of the dual-epsilon sandwich tail; out_stream may be
+    residual (in-place update)."""
+    import torch
+    dt = _dtype_code(block_out)
+    _check(block_out, "block_out", block_out.dtype)
+    rows, n = _rows_n(block_out)
+    _check(residual, "residual", block_out.dtype, block_out.shape)
+    _check(gamma_post, "gamma_post", block_out.dtype, (n,))
+    _check(gamma_pre, "gamma_pre", block_out.dtype, (n,))
+    out_stream = torch.empty_like(block_out) if out_stream is None else out_stream
+    normed = torch.empty_like(block_out) if normed is None else normed
+    _check(out_stream, "out_stream", block_out.dtype, block_out.shape)
+    _check(normed, "normed", block_out.dtype, block_out.shape)
+    st = mrn_norm_residual_norm(block_out.data_ptr(), residual.data_ptr(), gamma_post.data_ptr(),
+                                gamma_pre.data_ptr(), out_stream.data_ptr(), normed.data_ptr(),
+                                rows, n, eps_post, eps_pre, dt, _stream(block_out))
+    if st != 0:
+        raise MrnError(st, "mrn_norm_residual_norm")
+    return out_stream, normed

@@ -1,0 +1,191 @@
+/*
+ * mrn.h -- C ABI of libmrn: RMSNorm, post-norm-then-add and the dual-epsilon
+ * sandwich tail on NVIDIA GB300 (sm_103a), hand-written CUDA kernels.
+ *
+ * Operations (row r of a contiguous row-major [rows x n] matrix, j = 0..n-1):
+ *
+ *   mrn_rmsnorm             y[r,j]   = x[r,j] * inv(x[r,:]; eps) * gamma[j]
+ *   mrn_rmsnorm_then_add    out[r,j] = x[r,j] * inv(x[r,:]; eps) * gamma[j] + residual[r,j]
+ *   mrn_norm_residual_norm  out_stream[r,j] = block_out[r,j] * inv(block_out[r,:]; eps_post)
+ *                                             * gamma_post[j] + residual[r,j]
+ *                           normed[r,j]     = out_stream[r,j] * inv(out_stream[r,:]; eps_pre)
+ *                                             * gamma_pre[j]
+ *   with inv(v; eps) = 1 / sqrt((1/n) sum_j v_j^2 + eps).
+ *
+ * Sources: "Chapter 12 -- RMSNorm and the dual-epsilon sandwich" section 12.1
+ * (definition), 12.2 (two epsilons: 1e-8 for the post norms, 1e-5 for the pre
+ * norms), 12.4.3 (the fused tail: hidden += rms_norm(src, eps1) * w1, then
+ * output = rms_norm(hidden, eps2) * w2, in one dispatch); the Hesper "RMSNorm
+ * Layer" page, rmsNormThenAddKernel / rmsNormThenAddBatchKernel (post norm then
+ * residual add, row-major batch) and rmsNormThenAddBatchInPlaceKernel (in-place
+ * residual update).
+ *
+ * Common conventions for the three operations
+ * -------------------------------------------
+ * Pointers   All data pointers are CUDA device pointers (or managed memory)
+ *            owned by the caller.  The library allocates no memory, keeps no
+ *            per-call state and never frees anything.
+ * Layout     Row operands are contiguous row-major [rows x n]: element (r, j)
+ *            at base + r*n + j.  gamma vectors are [n] and shared by all rows.
+ * dtype      MRN_F32: every operand is float.  MRN_BF16: every operand (row
+ *            data and gamma) is bfloat16; arithmetic is f32 and each output is
+ *            rounded once to bf16 (to nearest, ties to even).  In the bf16
+ *            sandwich, normed is computed from the rounded out_stream that is
+ *            stored (the split route's publication boundary, section 12.4.4).
+ * eps        float, finite and > 0; used as given (the f32 value).
+ * Sizes      n >= 1; rows >= 0.  rows == 0 is a no-op that returns MRN_OK
+ *            without reading any pointer.  rows * n * element size must fit
+ *            in int64.
+ * Alignment  Each pointer must be aligned to its element size.  When every
+ *            pointer is 16-byte aligned and n * element size is a multiple
+ *            of 16, rows are moved in 16-byte vectors; otherwise element-wise.
+ * Aliasing   An output may be the very same buffer as a row input (same base
+ *            pointer): y == x, out == x or out == residual, out_stream ==
+ *            residual (the in-place residual update) or out_stream ==
+ *            block_out, normed == block_out or normed == residual.  Any
+ *            other overlap -- partial overlaps, two outputs overlapping, an
+ *            output overlapping a gamma -- is rejected with MRN_ERR_ALIASING.
+ * Stream     Work is enqueued on `stream` (0 = the legacy default stream) and
+ *            runs asynchronously; the call returns once it is enqueued.
+ * Errors     Argument errors are detected before anything is enqueued; nothing
+ *            is written.  MRN_ERR_CUDA means the launch itself failed (see
+ *            mrn_last_cuda_error).  Faults during execution surface at the
+ *            caller's next synchronisation, as for any CUDA kernel.
+ * Threads    All entry points are thread-safe.
+ */
+#ifndef MRN_H
+#define MRN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mrn_dtype {
+    MRN_F32 = 0,
+    MRN_BF16 = 1
+} mrn_dtype;
+
+typedef enum mrn_status {
+    MRN_OK = 0,
+    MRN_ERR_NULL_POINTER = 1,      /* a required pointer is NULL (rows > 0) */
+    MRN_ERR_INVALID_SIZE = 2,      /* n < 1, rows < 0, or rows*n*size overflows */
+    MRN_ERR_INVALID_EPS = 3,       /* eps not finite or not > 0 */
+    MRN_ERR_UNSUPPORTED_DTYPE = 4, /* dtype not MRN_F32 / MRN_BF16 */
+    MRN_ERR_ALIASING = 5,          /* a forbidden overlap between buffers */
+    MRN_ERR_MISALIGNED = 6,        /* a pointer not aligned to its element size */
+    MRN_ERR_CUDA = 7,              /* the CUDA runtime refused the launch */
+    MRN_ERR_INVALID_GEOMETRY = 8   /* a forced geometry cannot cover the row */
+} mrn_status;
+
+/*
+ * RMSNorm of every row ("Chapter 12", section 12.1; the ferrite-lineage
+ * rms_norm_batch of section 12.4.1 computes the same thing):
+ *   x      [rows x n]  input rows
+ *   gamma  [n]         per-channel gain
+ *   y      [rows x n]  output; may be x itself
+ */
+mrn_status mrn_rmsnorm(const void *x, const void *gamma, void *y,
+                       int64_t rows, int64_t n, float eps,
+                       mrn_dtype dtype, cudaStream_t stream);
+
+/*
+ * Post norm then residual add (Hesper "RMSNorm Layer", rmsNormThenAddKernel and
+ * its row-major batch form rmsNormAddBatchRowsKernel):
+ *   x         [rows x n]  the block output that is normalised
+ *   gamma     [n]
+ *   residual  [rows x n]  added after the norm
+ *   out       [rows x n]  may be x or residual itself (in-place residual update,
+ *                         rmsNormThenAddBatchInPlaceKernel)
+ */
+mrn_status mrn_rmsnorm_then_add(const void *x, const void *gamma,
+                                const void *residual, void *out,
+                                int64_t rows, int64_t n, float eps,
+                                mrn_dtype dtype, cudaStream_t stream);
+
+/*
+ * Dual-epsilon sandwich tail in one kernel ("Chapter 12", section 12.4.3,
+ * muser_fused_norm_residual_rms_norm_32sg; roles: src = block_out,
+ * hidden = residual / out_stream, weight1 = gamma_post, weight2 = gamma_pre,
+ * eps1 = eps_post (1e-8 on the pages' model), eps2 = eps_pre (1e-5)):
+ *   block_out   [rows x n]  sub-block output (attention o_proj or FFN down)
+ *   residual    [rows x n]  residual stream before the update
+ *   gamma_post  [n]         the post norm's gain
+ *   gamma_pre   [n]         the next pre norm's gain
+ *   out_stream  [rows x n]  updated stream; may be residual (in place) or block_out
+ *   normed      [rows x n]  next sub-block's input; may be block_out or residual,
+ *                           never overlapping out_stream
+ */
+mrn_status mrn_norm_residual_norm(const void *block_out, const void *residual,
+                                  const void *gamma_post, const void *gamma_pre,
+                                  void *out_stream, void *normed,
+                                  int64_t rows, int64_t n,
+                                  float eps_post, float eps_pre,
+                                  mrn_dtype dtype, cudaStream_t stream);
+
+/* Static, human-readable name of a status code; never NULL. */
+const char *mrn_status_string(mrn_status status);
+
+/* cudaError_t of the most recent MRN_ERR_CUDA returned on the calling thread
+ * (0 if none). */
+int mrn_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------ */
+/* Introspection and test hooks.  These are not on the pages: they expose the
+ * kernel geometry the library picks so that tests can drive every variant
+ * and benchmarks can report it.                                              */
+
+typedef enum mrn_op {
+    MRN_OP_RMSNORM = 0,
+    MRN_OP_THEN_ADD = 1,
+    MRN_OP_SANDWICH = 2
+} mrn_op;
+
+typedef enum mrn_geometry_kind {
+    MRN_GEOM_AUTO = 0,          /* (for mrn_force_geometry) let the library choose */
+    MRN_GEOM_ROWS_PER_WARP = 1, /* lanes_per_row (1..32) lanes per row, several rows
+                                   per CTA, shuffle-only reduction */
+    MRN_GEOM_CTA = 2,           /* one row per CTA, or per thread-block cluster of
+                                   `cluster` CTAs with a DSMEM reduction; row held
+                                   in registers */
+    MRN_GEOM_STREAM = 3         /* one row per CTA, looped over the row: any n */
+} mrn_geometry_kind;
+
+typedef struct mrn_geometry {
+    int32_t kind;          /* mrn_geometry_kind */
+    int32_t vec;           /* elements per load: 16 / element size, or 1 */
+    int32_t k;             /* loads per operand per thread (register slots) */
+    int32_t threads;       /* threads per CTA */
+    int32_t cluster;       /* CTAs per row (1 unless MRN_GEOM_CTA is split) */
+    int32_t lanes_per_row; /* threads per row for MRN_GEOM_ROWS_PER_WARP */
+    int32_t rows_per_cta;  /* rows one CTA handles */
+} mrn_geometry;
+
+/*
+ * The geometry an operation would launch with.  aligned16 != 0 states that all
+ * pointers would be 16-byte aligned.  sm_count 0 means: ask the current
+ * device; a positive value is used as given (lets host-only tests query).
+ * The thread's forced geometry, if any, is reported instead.
+ */
+mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtype,
+                              int32_t aligned16, int32_t sm_count, mrn_geometry *out);
+
+/*
+ * Force the geometry of the calling thread's later calls (NULL or kind
+ * MRN_GEOM_AUTO restores the automatic choice).  Fields 0 mean "automatic"
+ * for vec.  A forced geometry that cannot cover a call's row makes that call
+ * return MRN_ERR_INVALID_GEOMETRY.  The geometry is checked for internal
+ * consistency here (MRN_ERR_INVALID_GEOMETRY if not).
+ */
+mrn_status mrn_force_geometry(const mrn_geometry *geometry);
+
+/* Number of kernels this library has launched in the process (all threads). */
+uint64_t mrn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MRN_H */

@@ -1,0 +1,278 @@
+"""Helpers for the GPU parity tests: device buffers with guard bands, the
+tolerance rules, and calls through the C ABI.
+
+Tolerances (the contract the tests enforce):
+* f32 outputs that are plain norms (rmsnorm y, sandwich normed):
+  |gpu - oracle| <= 1e-5 * |oracle|, and an exact 0 where the oracle is 0.
+* f32 outputs that are sums (then-add out, sandwich out_stream): the relative
+  bound is taken against the size of the summands,
+  |gpu - oracle| <= 1e-5 * (|x * inv * gamma| + |residual|), because a sum
+  that cancels has no meaningful relative error.
+* bf16 outputs: at most 1 unit in the last place from the round-to-nearest-even
+  bf16 of the f64 oracle value, or |gpu - oracle| <= ulp(oracle) + 1e-5 *
+  summands: the f32 accumulation tolerance plus one bf16 rounding.  The
+  second clause only differs from the first under cancellation, where the
+  result is small against its summands and the f32 error of the summands is
+  no longer small against one bf16 ulp of the result.
+* normed is checked against the oracle's norm of the stream the GPU stored
+  (the value the kernel actually reads), and its end-to-end error against
+  the oracle's own sandwich is checked with the propagated bound.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from dual_epsilon_sandwich_gb300 import mrn
+
+F32_TOL = 1e-5
+GUARD_BYTES = 64
+SENTINEL = {"f32": 0x7FBADBAD, "bf16": 0x7FBD}   # NaN patterns no kernel produces
+
+
+def elem_bytes(dtype):
+    return 4 if dtype == "f32" else 2
+
+
+def code(dtype):
+    return mrn.MRN_F32 if dtype == "f32" else mrn.MRN_BF16
+
+
+def to_device(a, dtype) -> torch.Tensor:
+    """numpy f32 array or uint16 bf16 bit patterns -> CUDA tensor."""
+    if dtype == "f32":
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+    bits = np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)
+    return torch.from_numpy(bits).cuda().view(torch.bfloat16)
+
+
+def widen(a, dtype) -> np.ndarray:
+    """Host array (f32 or bf16 bits) -> exact float64."""
+    if dtype == "f32":
+        return np.asarray(a, dtype=np.float32).astype(np.float64)
+    return oracle.double_from_bf16(a)
+
+
+def to_host(t: torch.Tensor, dtype) -> np.ndarray:
+    """CUDA tensor -> f32 array or uint16 bit patterns."""
+    t = t.detach().cpu().contiguous()
+    if dtype == "f32":
+        return t.numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+class Guarded:
+    """An output buffer [rows x n] inside a larger allocation whose guard bands
+    (64 bytes before and after) and body are prefilled with a sentinel NaN."""
+
+    def __init__(self, rows, n, dtype, offset_elems=0):
+        self.dtype = dtype
+        e = elem_bytes(dtype)
+        self.guard = GUARD_BYTES // e
+        self.off = self.guard + offset_elems
+        self.count = rows * n
+        total = self.off + self.count + self.guard
+        itype = torch.int32 if dtype == "f32" else torch.int16
+        sent = SENTINEL[dtype]
+        if dtype == "bf16":
+            sent = np.int16(np.uint16(sent))
+        else:
+            sent = np.int32(np.uint32(sent))
+        self.raw = torch.full((total,), int(sent), dtype=itype, device="cuda")
+        self.sentinel = int(sent)
+        ftype = torch.float32 if dtype == "f32" else torch.bfloat16
+        self.tensor = self.raw[self.off:self.off + self.count].view(ftype).view(rows, n)
+
+    def ptr(self):
+        return self.tensor.data_ptr()
+
+    def check(self, what=""):
+        raw = self.raw
+        head = raw[:self.off]
+        tail = raw[self.off + self.count:]
+        assert bool((head == self.sentinel).all()), f"{what}: write before the output"
+        assert bool((tail == self.sentinel).all()), f"{what}: write after the output"
+        body = raw[self.off:self.off + self.count]
+        unwritten = int((body == self.sentinel).sum())
+        assert unwritten == 0, f"{what}: {unwritten} outputs never written"
+
+    def host(self):
+        return to_host(self.tensor, self.dtype)
+
+
+# ---------------------------------------------------------------------------
+# tolerance checks (return the worst error seen, for reporting)
+# ---------------------------------------------------------------------------
+def check_f32_norm(got, want, what):
+    got = np.asarray(got, dtype=np.float64)
+    zero = want == 0
+    assert np.all(got[zero] == 0), f"{what}: nonzero output where the oracle is 0"
+    err = np.abs(got - want)
+    bad = err > F32_TOL * np.abs(want)
+    if np.any(bad):
+        i = np.flatnonzero(bad.ravel())[:5]
+        raise AssertionError(f"{what}: {bad.sum()} elements over 1e-5 relative; e.g. "
+                             f"got {got.ravel()[i]} want {want.ravel()[i]}")
+    nz = ~zero
+    return float(np.max(err[nz] / np.abs(want[nz]))) if np.any(nz) else 0.0
+
+
+def check_f32_sum(got, want, scale, what):
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - want)
+    bad = err > F32_TOL * scale
+    if np.any(bad):
+        i = np.flatnonzero(bad.ravel())[:5]
+        raise AssertionError(f"{what}: {bad.sum()} elements over 1e-5 of the summands; e.g. "
+                             f"got {got.ravel()[i]} want {want.ravel()[i]} "
+                             f"scale {scale.ravel()[i]}")
+    pos = scale > 0
+    return float(np.max(err[pos] / scale[pos])) if np.any(pos) else 0.0
+
+
+def _ordered(bits):
+    b = bits.astype(np.int64)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+
+
+def bf16_ulp(v):
+    a = np.maximum(np.abs(v), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def check_bf16(got_bits, want, scale, what):
+    """got_bits: uint16; want: f64 oracle; scale: size of the summands (or |want|).
+
+    Pass: at most 1 ulp from the bf16 rounding of the oracle value, or -- where
+    the f32 tolerance on the summands is not small against one bf16 ulp of the
+    result, i.e. under cancellation -- within one ulp plus that f32 tolerance.
+    Returns (max ulp distance, number of elements that needed the second clause)."""
+    exp_bits = oracle.bf16_from_double(want)
+    dist = np.abs(_ordered(got_bits) - _ordered(exp_bits))
+    got = oracle.double_from_bf16(got_bits)
+    within_ulp = dist <= 1
+    cancel = np.abs(got - want) <= bf16_ulp(want) + F32_TOL * scale
+    ok = within_ulp | cancel
+    if not np.all(ok):
+        i = np.flatnonzero(~ok.ravel())[:5]
+        raise AssertionError(f"{what}: {np.sum(~ok)} elements beyond 1 bf16 ulp; e.g. got "
+                             f"{got.ravel()[i]} want {want.ravel()[i]} ulps {dist.ravel()[i]}")
+    return int(dist.max()), int(np.sum(~within_ulp))
+
+
+# ---------------------------------------------------------------------------
+# C-ABI calls on torch buffers (pointers and sizes only)
+# ---------------------------------------------------------------------------
+def stream_handle():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def call_rmsnorm(x, g, y, rows, n, eps, dtype):
+    return mrn.mrn_rmsnorm(x.data_ptr(), g.data_ptr(), _p(y), rows, n, eps, code(dtype),
+                           stream_handle())
+
+
+def call_then_add(x, g, r, out, rows, n, eps, dtype):
+    return mrn.mrn_rmsnorm_then_add(x.data_ptr(), g.data_ptr(), r.data_ptr(), _p(out), rows, n,
+                                    eps, code(dtype), stream_handle())
+
+
+def call_sandwich(b, r, gp, gq, s, o, rows, n, eps_post, eps_pre, dtype):
+    return mrn.mrn_norm_residual_norm(b.data_ptr(), r.data_ptr(), gp.data_ptr(), gq.data_ptr(),
+                                      _p(s), _p(o), rows, n, eps_post, eps_pre, code(dtype),
+                                      stream_handle())
+
+
+def _p(t):
+    return t.ptr() if isinstance(t, Guarded) else t.data_ptr()
+
+
+# ---------------------------------------------------------------------------
+# whole-operation parity: run on the GPU, compare with the oracle
+# ---------------------------------------------------------------------------
+def parity_rmsnorm(x, gamma, eps, dtype, rows_sample=None, what="rmsnorm"):
+    rows, n = x.shape
+    dx, dg = to_device(x, dtype), to_device(gamma, dtype)
+    y = Guarded(rows, n, dtype)
+    st = call_rmsnorm(dx, dg, y, rows, n, eps, dtype)
+    assert st == 0, f"{what}: status {mrn.STATUS.get(st)}"
+    torch.cuda.synchronize()
+    y.check(what)
+    got = y.host()
+    sel = slice(None) if rows_sample is None else rows_sample
+    xs, gs = widen(x[sel], dtype), widen(gamma, dtype)
+    want = oracle.rmsnorm(xs, gs, float(np.float32(eps)))
+    if dtype == "f32":
+        return check_f32_norm(got[sel], want, what)
+    return check_bf16(got[sel], want, np.abs(want), what)
+
+
+def parity_then_add(x, gamma, res, eps, dtype, rows_sample=None, what="then_add"):
+    rows, n = x.shape
+    dx, dg, dr = to_device(x, dtype), to_device(gamma, dtype), to_device(res, dtype)
+    out = Guarded(rows, n, dtype)
+    st = call_then_add(dx, dg, dr, out, rows, n, eps, dtype)
+    assert st == 0, f"{what}: status {mrn.STATUS.get(st)}"
+    torch.cuda.synchronize()
+    out.check(what)
+    got = out.host()
+    sel = slice(None) if rows_sample is None else rows_sample
+    xs, gs, rs = widen(x[sel], dtype), widen(gamma, dtype), widen(res[sel], dtype)
+    e = float(np.float32(eps))
+    want = oracle.rmsnorm_then_add(xs, gs, rs, e)
+    scale = np.abs(oracle.rmsnorm(xs, gs, e)) + np.abs(rs)
+    if dtype == "f32":
+        return check_f32_sum(got[sel], want, scale, what)
+    return check_bf16(got[sel], want, scale, what)
+
+
+def parity_sandwich(b, res, gp, gq, eps_post, eps_pre, dtype, rows_sample=None,
+                    what="sandwich", inplace=None):
+    """inplace: None, "residual" (out_stream == residual) or "block_out"."""
+    rows, n = b.shape
+    db, dr = to_device(b, dtype), to_device(res, dtype)
+    dgp, dgq = to_device(gp, dtype), to_device(gq, dtype)
+    o = Guarded(rows, n, dtype)
+    if inplace == "residual":
+        s_t = dr
+    elif inplace == "block_out":
+        s_t = db
+    else:
+        s_t = Guarded(rows, n, dtype)
+    st = call_sandwich(db, dr, dgp, dgq, s_t, o, rows, n, eps_post, eps_pre, dtype)
+    assert st == 0, f"{what}: status {mrn.STATUS.get(st)}"
+    torch.cuda.synchronize()
+    o.check(what + " normed")
+    if isinstance(s_t, Guarded):
+        s_t.check(what + " out_stream")
+        got_s = s_t.host()
+    else:
+        got_s = to_host(s_t, dtype)
+    got_o = o.host()
+    sel = slice(None) if rows_sample is None else rows_sample
+    bs, rs = widen(b[sel], dtype), widen(res[sel], dtype)
+    gps, gqs = widen(gp, dtype), widen(gq, dtype)
+    e1, e2 = float(np.float32(eps_post)), float(np.float32(eps_pre))
+    want_s, want_o = oracle.norm_residual_norm(bs, rs, gps, gqs, e1, e2)
+    scale_s = np.abs(oracle.rmsnorm(bs, gps, e1)) + np.abs(rs)
+    gs_sel = widen(got_s[sel], dtype)
+    cond_o = oracle.rmsnorm(gs_sel, gqs, e2)          # norm of the stream the GPU stored
+    if dtype == "f32":
+        es = check_f32_sum(got_s[sel], want_s, scale_s, what + " out_stream")
+        eo = check_f32_norm(got_o[sel], cond_o, what + " normed")
+        inv2 = 1.0 / np.sqrt(np.mean(want_s * want_s, axis=1, keepdims=True) + e2)
+        e2e = check_f32_sum(got_o[sel], want_o, np.abs(want_o) + 2 * scale_s * inv2 * np.abs(gqs),
+                            what + " normed end to end")
+        return es, eo, e2e
+    es = check_bf16(got_s[sel], want_s, scale_s, what + " out_stream")
+    eo = check_bf16(got_o[sel], cond_o, np.abs(cond_o), what + " normed")
+    return es, eo
+
+
+def sample_rows(rows, count, seed, must=()):
+    g = np.random.Generator(np.random.PCG64(seed))
+    pick = set(int(v) for v in g.choice(rows, size=min(rows, count), replace=False))
+    pick.update(int(v) for v in must)
+    pick.update({0, rows - 1})
+    return np.array(sorted(pick))

@@ -1,0 +1,177 @@
+"""Host-only checks of the C ABI (no GPU, no kernel launch).
+
+Every call here fails validation before anything is enqueued, so the pointers
+are fake addresses that are never dereferenced.
+"""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+from dual_epsilon_sandwich_gb300 import _build, mrn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mrn.h")
+
+A = 0x7F0000000000        # fake, 256-byte aligned device addresses
+B = 0x7F0100000000
+G = 0x7F0200000000
+H = 0x7F0300000000
+Y = 0x7F0400000000
+Z = 0x7F0500000000
+
+
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    _build.build()
+    return mrn.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mrn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(library):
+    names = declared_functions()
+    assert set(names) == set(mrn.EXPORTS), names
+    for name in names:
+        assert hasattr(library, name), f"libmrn.so does not export {name}"
+    nm = subprocess.run(["nm", "-D", "--defined-only", mrn.LIBRARY], capture_output=True,
+                        text=True, check=True).stdout
+    for name in names:
+        assert re.search(rf"\bT {name}$", nm, flags=re.M), name
+
+
+def test_status_strings():
+    for code in range(9):
+        assert mrn.mrn_status_string(code)
+    assert "unknown" in mrn.mrn_status_string(99)
+    assert mrn.mrn_last_cuda_error() == 0
+
+
+def rms(x=A, g=G, y=Y, rows=4, n=64, eps=1e-5, dt=mrn.MRN_F32):
+    return mrn.mrn_rmsnorm(x, g, y, rows, n, eps, dt, 0)
+
+
+def tadd(x=A, g=G, r=B, o=Y, rows=4, n=64, eps=1e-5, dt=mrn.MRN_F32):
+    return mrn.mrn_rmsnorm_then_add(x, g, r, o, rows, n, eps, dt, 0)
+
+
+def sand(b=A, r=B, gp=G, gq=H, s=Y, o=Z, rows=4, n=64, e1=1e-8, e2=1e-5, dt=mrn.MRN_F32):
+    return mrn.mrn_norm_residual_norm(b, r, gp, gq, s, o, rows, n, e1, e2, dt, 0)
+
+
+def test_size_validation():
+    assert rms(n=0) == mrn.MRN_ERR_INVALID_SIZE
+    assert rms(n=-3) == mrn.MRN_ERR_INVALID_SIZE
+    assert rms(rows=-1) == mrn.MRN_ERR_INVALID_SIZE
+    assert tadd(rows=2 ** 40, n=2 ** 30) == mrn.MRN_ERR_INVALID_SIZE     # bytes overflow int64
+    assert sand(n=2 ** 62) == mrn.MRN_ERR_INVALID_SIZE
+
+
+def test_rows_zero_is_a_no_op_without_pointers():
+    assert rms(x=None, g=None, y=None, rows=0) == mrn.MRN_OK
+    assert tadd(x=None, g=None, r=None, o=None, rows=0) == mrn.MRN_OK
+    assert sand(b=None, r=None, gp=None, gq=None, s=None, o=None, rows=0) == mrn.MRN_OK
+    assert mrn.mrn_launch_count() == 0
+
+
+@pytest.mark.parametrize("eps", [0.0, -1e-5, float("nan"), float("inf"), -0.0])
+def test_eps_validation(eps):
+    assert rms(eps=eps) == mrn.MRN_ERR_INVALID_EPS
+    assert tadd(eps=eps) == mrn.MRN_ERR_INVALID_EPS
+    assert sand(e1=eps) == mrn.MRN_ERR_INVALID_EPS
+    assert sand(e2=eps) == mrn.MRN_ERR_INVALID_EPS
+
+
+def test_dtype_validation():
+    assert rms(dt=2) == mrn.MRN_ERR_UNSUPPORTED_DTYPE
+    assert tadd(dt=-1) == mrn.MRN_ERR_UNSUPPORTED_DTYPE
+    assert sand(dt=7) == mrn.MRN_ERR_UNSUPPORTED_DTYPE
+
+
+def test_null_pointers():
+    assert rms(x=None) == mrn.MRN_ERR_NULL_POINTER
+    assert rms(g=None) == mrn.MRN_ERR_NULL_POINTER
+    assert tadd(r=None) == mrn.MRN_ERR_NULL_POINTER
+    for kw in ("b", "r", "gp", "gq", "s", "o"):
+        assert sand(**{kw: None}) == mrn.MRN_ERR_NULL_POINTER, kw
+
+
+def test_misaligned_pointers():
+    assert rms(x=A + 2) == mrn.MRN_ERR_MISALIGNED                 # f32 needs 4 bytes
+    assert rms(x=A + 1, dt=mrn.MRN_BF16) == mrn.MRN_ERR_MISALIGNED
+    assert tadd(r=B + 1) == mrn.MRN_ERR_MISALIGNED
+    assert sand(gq=H + 3) == mrn.MRN_ERR_MISALIGNED
+
+
+def test_forbidden_aliasing():
+    rb = 4 * 64 * 4
+    assert rms(y=A + 4) == mrn.MRN_ERR_ALIASING                    # partial overlap
+    assert rms(y=G - 8) == mrn.MRN_ERR_ALIASING                    # output over gamma
+    assert tadd(o=B + rb - 4) == mrn.MRN_ERR_ALIASING              # tail overlaps residual
+    assert sand(o=Y) == mrn.MRN_ERR_ALIASING                       # normed == out_stream
+    assert sand(o=Y + 64) == mrn.MRN_ERR_ALIASING                  # outputs overlap
+    assert sand(s=G) == mrn.MRN_ERR_ALIASING                       # stream over gamma_post
+    assert sand(o=H - 16) == mrn.MRN_ERR_ALIASING                  # normed over gamma_pre
+    assert sand(s=A + 256) == mrn.MRN_ERR_ALIASING                 # partial over block_out
+    assert mrn.mrn_launch_count() == 0
+
+
+def test_geometry_covers_every_row_width():
+    for dt, e in ((mrn.MRN_F32, 4), (mrn.MRN_BF16, 2)):
+        for n in [1, 2, 3, 7, 8, 31, 33, 100, 127, 128, 129, 255, 256, 257, 768, 1000, 2048,
+                  4096, 5120, 6656, 6657, 8192, 16384, 32768, 65536, 131072, 262144, 1 << 20]:
+            for rows in (1, 4, 64, 4096, 65536):
+                for a16 in (True, False):
+                    for op in (0, 1, 2):
+                        g = mrn.mrn_query_geometry(op, rows, n, dt, a16, 152)
+                        vec = g["vec"]
+                        assert vec == (16 // e if a16 and (n * e) % 16 == 0 else 1)
+                        nvec = -(-n // vec)
+                        if g["kind"] == mrn.MRN_GEOM_ROWS_PER_WARP:
+                            assert g["lanes_per_row"] * g["k"] >= nvec
+                            assert g["threads"] == 256 and 32 % g["lanes_per_row"] == 0
+                        elif g["kind"] == mrn.MRN_GEOM_CTA:
+                            assert g["cluster"] * g["threads"] * g["k"] >= nvec
+                            assert g["threads"] % 32 == 0 and 1 <= g["cluster"] <= 16
+                            cap = 1024 if g["k"] <= 2 else (512 if g["k"] <= 4 else 256)
+                            assert g["threads"] <= cap
+                        else:
+                            assert g["kind"] == mrn.MRN_GEOM_STREAM
+                            assert nvec > 16 * 2048
+
+
+def test_force_geometry_validation():
+    bad = [
+        {"kind": 1, "lanes_per_row": 3, "k": 1},
+        {"kind": 1, "lanes_per_row": 64, "k": 1},
+        {"kind": 2, "k": 9, "threads": 128, "cluster": 1},
+        {"kind": 2, "k": 8, "threads": 512, "cluster": 1},     # above the k=8 launch bound
+        {"kind": 2, "k": 1, "threads": 100, "cluster": 1},
+        {"kind": 2, "k": 1, "threads": 128, "cluster": 17},
+        {"kind": 3, "threads": 1024},
+        {"kind": 9},
+    ]
+    for g in bad:
+        assert mrn.mrn_force_geometry(g) == mrn.MRN_ERR_INVALID_GEOMETRY, g
+    assert mrn.mrn_force_geometry({"kind": 2, "k": 2, "threads": 64, "cluster": 2}) == 0
+    got = mrn.mrn_query_geometry(0, 8, 1024, mrn.MRN_F32, True, 152)
+    assert (got["kind"], got["k"], got["threads"], got["cluster"]) == (2, 2, 64, 2)
+    with pytest.raises(mrn.MrnError):          # 2*64*2 = 256 loads cannot cover n = 4096
+        mrn.mrn_query_geometry(0, 8, 4096, mrn.MRN_F32, True, 152)
+    assert mrn.mrn_force_geometry(None) == 0
+    assert mrn.mrn_query_geometry(0, 8, 4096, mrn.MRN_F32, True, 152)["kind"] == 2
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    code = ("import dual_epsilon_sandwich_gb300.mrn as m; m.LIBRARY = '/nonexistent/libmrn.so'\n"
+            "try:\n    m.mrn_status_string(0)\nexcept RuntimeError as e:\n"
+            "    print('raised', e)\nelse:\n    raise SystemExit('no error')\n")
+    res = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
+    assert res.returncode == 0 and "raised" in res.stdout, res.stderr

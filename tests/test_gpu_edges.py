@@ -1,0 +1,277 @@
+"""GPU parity on edge cases: tiny and ragged rows (the d=2 silent-wrong-answer
+class the dormouse page reports), misaligned rows, in-place aliasing, every
+geometry variant forced on the same inputs, cluster sizes 1..16, the looped
+fallback for very wide rows, epsilon routing, determinism and streams."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as gu
+import oracle
+from dual_epsilon_sandwich_gb300 import mrn
+from dual_epsilon_sandwich_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ("f32", "bf16")
+
+
+@pytest.fixture(autouse=True)
+def _lib(gpu_lib):
+    mrn.mrn_force_geometry(None)
+    yield
+    mrn.mrn_force_geometry(None)
+
+
+def rows_data(seed, rows, n, dtype, scale=1.0):
+    return wl.random_rows(seed, rows, n, dtype, scale)
+
+
+def all_ops(d, dtype, what, sample=None):
+    x, r, g, g2 = d["x"], d["residual"], d["gamma"], d["gamma2"]
+    gu.parity_rmsnorm(x, g, 1e-5, dtype, sample, what=f"{what} rmsnorm")
+    gu.parity_then_add(x, g, r, 1e-6, dtype, sample, what=f"{what} then_add")
+    gu.parity_sandwich(x, r, g, g2, 1e-8, 1e-5, dtype, sample, what=f"{what} sandwich")
+
+
+SMALL_N = [1, 2, 3, 4, 5, 7, 8, 9, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256,
+           257, 260, 1000, 2049]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("n", SMALL_N)
+def test_small_and_ragged_rows_every_output_written(n, dtype):
+    for rows in (1, 2, 3, 4, 5, 33):
+        all_ops(rows_data(1000 * n + rows, rows, n, dtype), dtype, f"{rows}x{n}")
+
+
+def test_two_element_rows_by_hand():
+    """x = [3, 4] -> [3, 4] / sqrt(12.5 + eps); x = [1, -1] -> +-1/sqrt(1 + eps), at rows 1..4."""
+    x = np.array([[3, 4], [1, -1], [0, 0], [-4, 3]], dtype=np.float32)
+    for rows in (1, 2, 3, 4):
+        dx = gu.to_device(x[:rows], "f32")
+        dg = gu.to_device(np.ones(2, np.float32), "f32")
+        y = gu.Guarded(rows, 2, "f32")
+        assert gu.call_rmsnorm(dx, dg, y, rows, 2, 1e-5, "f32") == 0
+        torch.cuda.synchronize()
+        y.check(f"n=2 rows={rows}")
+        e = float(np.float32(1e-5))
+        want = np.array([[3, 4] / np.sqrt(12.5 + e), [1, -1] / np.sqrt(1 + e), [0, 0],
+                         [-4, 3] / np.sqrt(12.5 + e)])[:rows]
+        gu.check_f32_norm(y.host(), want, f"n=2 rows={rows}")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_rows_not_16_byte_aligned(dtype):
+    """Pointers offset by one element: rows move element-wise, same results."""
+    rows, n = 5, 6656
+    d = rows_data(7, rows, n, dtype)
+    e = gu.elem_bytes(dtype)
+
+    def shifted(a):
+        t = gu.to_device(np.concatenate([np.zeros(1, a.dtype), a.ravel()]), dtype)
+        return t[1:].view(a.shape) if a.ndim == 2 else t[1:]
+
+    x, r, g, g2 = (shifted(d[k]) for k in ("x", "residual", "gamma", "gamma2"))
+    assert x.data_ptr() % 16 != 0
+    y = gu.Guarded(rows, n, dtype, offset_elems=1)
+    assert gu.call_rmsnorm(x, g, y, rows, n, 1e-5, dtype) == 0
+    torch.cuda.synchronize()
+    y.check("misaligned rmsnorm")
+    want = oracle.rmsnorm(gu.widen(d["x"], dtype), gu.widen(d["gamma"], dtype),
+                          float(np.float32(1e-5)))
+    if dtype == "f32":
+        gu.check_f32_norm(y.host(), want, "misaligned rmsnorm")
+    else:
+        gu.check_bf16(y.host(), want, np.abs(want), "misaligned rmsnorm")
+    s = gu.Guarded(rows, n, dtype, offset_elems=1)
+    o = gu.Guarded(rows, n, dtype, offset_elems=1)
+    assert gu.call_sandwich(x, r, g, g2, s, o, rows, n, 1e-8, 1e-5, dtype) == 0
+    torch.cuda.synchronize()
+    s.check("misaligned stream")
+    o.check("misaligned normed")
+    assert e in (2, 4)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_in_place_aliasing(dtype):
+    rows, n = 7, 2048
+    d = rows_data(8, rows, n, dtype)
+    x, r, g, g2 = (gu.to_device(d[k], dtype) for k in ("x", "residual", "gamma", "gamma2"))
+
+    ref_y = torch.empty_like(x)
+    assert gu.call_rmsnorm(x, g, ref_y, rows, n, 1e-5, dtype) == 0
+    xi = x.clone()
+    assert gu.call_rmsnorm(xi, g, xi, rows, n, 1e-5, dtype) == 0            # y == x
+    ref_o = torch.empty_like(x)
+    assert gu.call_then_add(x, g, r, ref_o, rows, n, 1e-5, dtype) == 0
+    ri = r.clone()
+    assert gu.call_then_add(x, g, ri, ri, rows, n, 1e-5, dtype) == 0        # out == residual
+    xo = x.clone()
+    assert gu.call_then_add(xo, g, r, xo, rows, n, 1e-5, dtype) == 0        # out == x
+    ref_s, ref_n = torch.empty_like(x), torch.empty_like(x)
+    assert gu.call_sandwich(x, r, g, g2, ref_s, ref_n, rows, n, 1e-8, 1e-5, dtype) == 0
+    r1, n1 = r.clone(), torch.empty_like(x)
+    assert gu.call_sandwich(x, r1, g, g2, r1, n1, rows, n, 1e-8, 1e-5, dtype) == 0   # stream == residual
+    b2, n2 = x.clone(), torch.empty_like(x)
+    assert gu.call_sandwich(b2, r, g, g2, b2, n2, rows, n, 1e-8, 1e-5, dtype) == 0   # stream == block_out
+    b3, s3 = x.clone(), torch.empty_like(x)
+    assert gu.call_sandwich(b3, r, g, g2, s3, b3, rows, n, 1e-8, 1e-5, dtype) == 0   # normed == block_out
+    r4, s4 = r.clone(), torch.empty_like(x)
+    assert gu.call_sandwich(x, r4, g, g2, s4, r4, rows, n, 1e-8, 1e-5, dtype) == 0   # normed == residual
+    torch.cuda.synchronize()
+
+    def same(a, b, what):
+        assert torch.equal(a.view(torch.int16 if dtype == "bf16" else torch.int32),
+                           b.view(torch.int16 if dtype == "bf16" else torch.int32)), what
+
+    same(xi, ref_y, "y == x")
+    same(ri, ref_o, "out == residual")
+    same(xo, ref_o, "out == x")
+    same(r1, ref_s, "stream == residual (stream)")
+    same(n1, ref_n, "stream == residual (normed)")
+    same(b2, ref_s, "stream == block_out (stream)")
+    same(n2, ref_n, "stream == block_out (normed)")
+    same(s3, ref_s, "normed == block_out (stream)")
+    same(b3, ref_n, "normed == block_out (normed)")
+    same(s4, ref_s, "normed == residual (stream)")
+    same(r4, ref_n, "normed == residual (normed)")
+    gu.parity_then_add(d["x"], d["gamma"], d["residual"], 1e-5, dtype)
+
+
+# Every geometry variant on shapes it can cover, including ragged coverage.
+FORCED = [
+    ({"kind": 1, "lanes_per_row": 32, "k": 8}, 250),
+    ({"kind": 1, "lanes_per_row": 32, "k": 3}, 90),
+    ({"kind": 1, "lanes_per_row": 16, "k": 5}, 77),
+    ({"kind": 1, "lanes_per_row": 4, "k": 7}, 25),
+    ({"kind": 1, "lanes_per_row": 1, "k": 2}, 2),
+    ({"kind": 2, "k": 1, "threads": 1024, "cluster": 1}, 1000),
+    ({"kind": 2, "k": 2, "threads": 96, "cluster": 5}, 950),
+    ({"kind": 2, "k": 3, "threads": 64, "cluster": 2}, 380),
+    ({"kind": 2, "k": 4, "threads": 512, "cluster": 1}, 2048),
+    ({"kind": 2, "k": 5, "threads": 256, "cluster": 3}, 3800),
+    ({"kind": 2, "k": 6, "threads": 32, "cluster": 7}, 1300),
+    ({"kind": 2, "k": 7, "threads": 224, "cluster": 1}, 1500),
+    ({"kind": 2, "k": 8, "threads": 256, "cluster": 16}, 32768),
+    ({"kind": 3, "threads": 32}, 1999),
+    ({"kind": 3, "threads": 512}, 7000),
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("geom,nvec", FORCED, ids=[str(i) for i in range(len(FORCED))])
+def test_forced_geometry(geom, nvec, dtype):
+    vec = 4 if dtype == "f32" else 8
+    for n, g in ((nvec * vec, geom), (nvec, dict(geom, vec=1))):
+        assert mrn.mrn_force_geometry(g) == 0
+        rows = 3 if n * 3 < (1 << 22) else 2
+        all_ops(rows_data(n + rows, rows, n, dtype), dtype, f"forced {g} n={n}")
+        mrn.mrn_force_geometry(None)
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 3, 4, 5, 6, 7, 8, 12, 16])
+def test_cluster_split_decode_row(cluster):
+    """One n=6656 row split over `cluster` CTAs with a DSMEM reduction."""
+    per = -(-1664 // cluster)
+    k = 1 if per <= 1024 else 2
+    threads = -(-per // (32 * k)) * 32
+    assert mrn.mrn_force_geometry({"kind": 2, "k": k, "threads": threads,
+                                   "cluster": cluster}) == 0
+    w = wl.sandwich_decode()
+    a = w.arrays
+    gu.parity_sandwich(a["block_out"], a["residual"], a["gamma_post"], a["gamma_pre"], w.eps,
+                       w.eps_pre, "f32", what=f"cluster {cluster}")
+    d = rows_data(9, 3, 6656, "bf16")
+    gu.parity_sandwich(d["x"], d["residual"], d["gamma"], d["gamma2"], 1e-8, 1e-5, "bf16",
+                       what=f"bf16 cluster {cluster}")
+
+
+@pytest.mark.parametrize("dtype,n", [("f32", 200000), ("f32", 140001), ("bf16", 300000),
+                                     ("bf16", 270001)])
+def test_wide_rows_use_the_looped_fallback(dtype, n):
+    g = mrn.mrn_query_geometry(0, 3, n, gu.code(dtype), True)
+    assert g["kind"] == mrn.MRN_GEOM_STREAM
+    all_ops(rows_data(n, 3, n, dtype), dtype, f"wide n={n}")
+
+
+def test_epsilon_routing_is_visible():
+    """Block output of mean square 1e-8 and a stream of mean square ~1e-6:
+    eps_post = 1e-8 and eps_pre = 1e-5 both move the outputs, and an oracle with
+    the two swapped is far outside the tolerance the GPU meets."""
+    g = np.random.Generator(np.random.PCG64(77))
+    rows, n = 8, 4096
+    b = (1e-4 * np.where(g.random((rows, n)) < 0.5, -1.0, 1.0)).astype(np.float32)
+    r = (1e-3 * g.standard_normal((rows, n))).astype(np.float32)
+    gp = (1e-3 * (1.0 + 0.1 * g.standard_normal(n))).astype(np.float32)
+    gq = (1.0 + 0.1 * g.standard_normal(n)).astype(np.float32)
+    gu.parity_sandwich(b, r, gp, gq, 1e-8, 1e-5, "f32", what="routing")
+    db, dr, dgp, dgq = (gu.to_device(a, "f32") for a in (b, r, gp, gq))
+    s, o = torch.empty_like(db), torch.empty_like(db)
+    assert gu.call_sandwich(db, dr, dgp, dgq, s, o, rows, n, 1e-8, 1e-5, "f32") == 0
+    torch.cuda.synchronize()
+    ws, wo = oracle.norm_residual_norm(b, r, gp, gq, float(np.float32(1e-5)),
+                                       float(np.float32(1e-8)))
+    with pytest.raises(AssertionError):
+        gu.check_f32_norm(gu.to_host(o, "f32"), wo, "swapped eps must be detectable")
+
+
+@pytest.mark.parametrize("scale", [1e-20, 1e-9, 1e-3, 1e3, 1e15])
+def test_row_magnitudes(scale):
+    """From epsilon-dominated rows (mean square << eps) to large ones."""
+    for dtype in DTYPES:
+        all_ops(rows_data(5, 6, 6656, dtype, scale=scale), dtype, f"scale {scale}")
+
+
+def test_all_ones_gamma_entry_norm():
+    """The entry norm binds an all-ones gamma (Chapter 12, section 12.3)."""
+    d = rows_data(10, 4, 6656, "f32")
+    gu.parity_rmsnorm(d["x"], np.ones(6656, np.float32), 1e-5, "f32")
+
+
+def test_deterministic_bits():
+    d = rows_data(11, 64, 6656, "f32")
+    x, r, g, g2 = (gu.to_device(d[k], "f32") for k in ("x", "residual", "gamma", "gamma2"))
+    outs = []
+    for _ in range(2):
+        s, o = torch.empty_like(x), torch.empty_like(x)
+        assert gu.call_sandwich(x, r, g, g2, s, o, 64, 6656, 1e-8, 1e-5, "f32") == 0
+        outs.append((s, o))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_non_default_stream_and_launch_count():
+    d = rows_data(12, 16, 4096, "bf16")
+    x, g = gu.to_device(d["x"], "bf16"), gu.to_device(d["gamma"], "bf16")
+    side = torch.cuda.Stream()
+    before = mrn.mrn_launch_count()
+    with torch.cuda.stream(side):
+        y = torch.empty_like(x)
+        assert gu.call_rmsnorm(x, g, y, 16, 4096, 1e-6, "bf16") == 0
+    side.synchronize()
+    assert mrn.mrn_launch_count() == before + 1
+    want = oracle.rmsnorm(gu.widen(d["x"], "bf16"), gu.widen(d["gamma"], "bf16"),
+                          float(np.float32(1e-6)))
+    gu.check_bf16(gu.to_host(y, "bf16"), want, np.abs(want), "side stream")
+    assert mrn.mrn_rmsnorm(0, 0, 0, 0, 4096, 1e-6, mrn.MRN_BF16, 0) == 0
+    assert mrn.mrn_launch_count() == before + 1
+
+
+def test_tensor_convenience_api():
+    d = rows_data(13, 5, 768, "f32")
+    x, r, g, g2 = (gu.to_device(d[k], "f32") for k in ("x", "residual", "gamma", "gamma2"))
+    y = mrn.rmsnorm(x, g, 1e-5)
+    s, o = mrn.norm_residual_norm(x, r, g, g2)
+    torch.cuda.synchronize()
+    want = oracle.rmsnorm(d["x"].astype(np.float64), d["gamma"].astype(np.float64),
+                          float(np.float32(1e-5)))
+    gu.check_f32_norm(y.cpu().numpy(), want, "tensor api")
+    with pytest.raises(mrn.MrnError):
+        mrn.rmsnorm(x, g, 0.0)
+    base = torch.empty(5 * 768 + 1, device="cuda")
+    x2 = base[:5 * 768].view(5, 768)
+    x2.copy_(x)
+    with pytest.raises(mrn.MrnError) as exc:          # output overlaps x by all but one element
+        mrn.rmsnorm_then_add(x2, g, r, 1e-5, out=base[1:].view(5, 768))
+    assert exc.value.status == mrn.MRN_ERR_ALIASING
