@@ -53,6 +53,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-launches", type=int, default=0,
+                   help="only run --warmup + this many launches of the timed call (for ncu)")
     return p.parse_args(argv)
 
 
@@ -305,6 +307,12 @@ def run_mrn(args):
     for i in range(args.warmup):
         call(sets[i % 2])
     torch.cuda.synchronize()
+    if args.profile_launches:
+        for i in range(args.profile_launches):
+            call(sets[i % 2])
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_launches": args.profile_launches, "geometry": geometry}))
+        return 0
 
     # -- device-resident timed region -------------------------------------
     K = args.steps

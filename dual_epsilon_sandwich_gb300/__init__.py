@@ -8,4 +8,4 @@ synthetic inputs used by the tests and the benchmark.
 from .mrn import (  # noqa: F401
     MRN_BF16, MRN_F32, MrnError, mrn_force_geometry, mrn_last_cuda_error, mrn_launch_count,
     mrn_norm_residual_norm, mrn_query_geometry, mrn_rmsnorm, mrn_rmsnorm_then_add,
-    mrn_status_string, norm_residual_norm, rmsnorm, rmsnorm_then_add)
+    mrn_status_string, mrn_wait_timeouts, norm_residual_norm, rmsnorm, rmsnorm_then_add)

@@ -68,14 +68,44 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int natural_vec(mrn_dtype dt) { return 16 / elem_bytes(dt); }
 
+// Register slots k and threads t for `per` loads of a row in one CTA (or one
+// warp group): the least waste (t*k - per), then t nearest `target`.
+void pick_threads(int64_t per, int *k_out, int *t_out, int (*max_threads)(int) = nullptr,
+                  double target = 256.0) {
+    double best = 1e30;
+    for (int k = 1; k <= mrn::kMaxK; ++k) {
+        const int64_t t = ceil_div(ceil_div(per, k), 32) * 32;
+        const int cap = max_threads ? max_threads(k) : mrn::cta_max_threads(k);
+        if (t > cap) continue;
+        const double waste = static_cast<double>(t * k - per) / static_cast<double>(per);
+        const double shape = 0.02 * std::fabs(std::log2(static_cast<double>(t) / target));
+        const double score = waste + shape;
+        if (score < best) {
+            best = score;
+            *k_out = k;
+            *t_out = static_cast<int>(t);
+        }
+    }
+}
+
+int tma_group_cap(int k) { return mrn::tma_group_max_threads(k); }
+
+// Dynamic shared memory the staged kernel may use (the rest of the 227 KB
+// holds its static reduction slots and barriers).
+constexpr int64_t kTmaSharedBudget = mrn::kSharedBytesPerCta - 1024;
+
 // Automatic geometry.  Loads per row: nvec = ceil(n / vec).
 //  * nvec <= 256: several rows per warp (lanes = next power of two of nvec up
 //    to 32, k = ceil(nvec / 32)); no shared memory, no barrier.
+//  * at least one row per SM, 16-byte aligned rows, nvec <= 2048, and two
+//    rows' operands fit in shared memory: the persistent TMA-staged kernel,
+//    two warp groups, one stage each;
 //  * nvec <= 16 * 2048: the row in registers of one CTA or of a cluster of up
 //    to 16 CTAs (2048 loads per CTA at most).  Few rows (decode) are spread
 //    over up to 8 CTAs of a cluster so that more SMs pull the row in.
 //  * wider: the looped fallback.
-Geometry choose_geometry(int64_t rows, int64_t n, mrn_dtype dt, bool aligned16, int sms) {
+Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool aligned16,
+                         int sms) {
     Geometry g = {};
     g.vec = aligned16 ? natural_vec(dt) : 1;
     g.cluster = 1;
@@ -88,6 +118,28 @@ Geometry choose_geometry(int64_t rows, int64_t n, mrn_dtype dt, bool aligned16, 
         g.rows_per_cta = g.threads / g.lanes;
         return g;
     }
+    // Many rows of aligned data whose staged copies fit in shared memory: the
+    // persistent TMA-staged kernel with two warp groups (two rows reduced at a
+    // time) and one stage per group; the occupancy calculator then puts as many
+    // CTAs on an SM as fit.  (Measured on GB300: more rows in flight per SM beat
+    // deeper per-CTA prefetch; groups of about 128 threads with more register
+    // slots each beat wider groups.)
+    const int64_t row_bytes = n * elem_bytes(dt);
+    if (aligned16 && rows >= sms && nvec <= 2 * 1024) {
+        const int stages = 2;
+        if (mrn::tma_shared_bytes(op, row_bytes, stages) <= kTmaSharedBudget) {
+            g.kind = mrn::kTma;
+            g.stages = stages;
+            g.ctas = 0;
+            g.groups = 2;
+            int per_group = 0;
+            pick_threads(nvec, &g.k, &per_group, tma_group_cap, 128.0);
+            g.threads = 2 * per_group;
+            g.lanes = 0;
+            g.rows_per_cta = 2;
+            return g;
+        }
+    }
     constexpr int64_t kCtaLoads = 2048;
     int64_t cl = ceil_div(nvec, kCtaLoads);
     if (cl > mrn::kMaxCluster) {
@@ -98,24 +150,14 @@ Geometry choose_geometry(int64_t rows, int64_t n, mrn_dtype dt, bool aligned16, 
         g.rows_per_cta = 1;
         return g;
     }
-    if (rows * 4 <= sms) {
-        const int64_t spread = std::min<int64_t>(8, pow2_floor(std::max<int64_t>(1, nvec / 256)));
-        cl = std::max(cl, spread);
+    if (rows * 2 <= sms) {
+        // Few rows (decode): spread each row over up to 8 CTAs of a cluster,
+        // keeping at least ~192 loads per CTA, so that more SMs pull it in.
+        const int64_t by_rows = pow2_floor(std::max<int64_t>(1, sms / rows));
+        const int64_t by_width = pow2_floor(std::max<int64_t>(1, nvec / 192));
+        cl = std::max(cl, std::min<int64_t>(8, std::min(by_rows, by_width)));
     }
-    const int64_t per = ceil_div(nvec, cl);
-    double best = 1e30;
-    for (int k = 1; k <= mrn::kMaxK; ++k) {
-        const int64_t t = ceil_div(ceil_div(per, k), 32) * 32;
-        if (t > mrn::cta_max_threads(k)) continue;
-        const double waste = static_cast<double>(t * k - per) / static_cast<double>(per);
-        const double shape = 0.02 * std::fabs(std::log2(static_cast<double>(t) / 256.0));
-        const double score = waste + shape;
-        if (score < best) {
-            best = score;
-            g.k = k;
-            g.threads = static_cast<int>(t);
-        }
-    }
+    pick_threads(ceil_div(nvec, cl), &g.k, &g.threads);
     g.kind = mrn::kCta;
     g.cluster = static_cast<int>(cl);
     g.lanes = 0;
@@ -136,16 +178,33 @@ bool geometry_is_consistent(const Geometry &g) {
     if (g.kind == mrn::kStream) {
         return g.threads >= 32 && g.threads % 32 == 0 && g.threads <= mrn::kStreamMaxThreads;
     }
+    if (g.kind == mrn::kTma) {
+        if (g.groups < 1 || g.groups > mrn::kTmaMaxGroups) return false;
+        const int per_group = g.threads / g.groups;
+        return g.k >= 1 && g.k <= mrn::kMaxK && g.threads % (32 * g.groups) == 0 &&
+               per_group >= 32 && g.threads <= mrn::tma_max_threads(g.k, g.groups) &&
+               g.stages >= g.groups && g.stages % g.groups == 0 &&
+               g.stages <= mrn::kTmaMaxStages && g.ctas >= 0;
+    }
     return false;
 }
 
 // Resolve the thread's forced geometry for one call; false if it cannot
 // cover the row or asks for vectors the pointers do not allow.
-bool resolve_forced(Geometry g, int64_t n, mrn_dtype dt, bool aligned16, Geometry *out) {
+bool resolve_forced(Geometry g, mrn::Op op, int64_t n, mrn_dtype dt, bool aligned16,
+                    Geometry *out) {
     if (g.vec == 0) g.vec = aligned16 ? natural_vec(dt) : 1;
     if (g.vec != 1 && !(g.vec == natural_vec(dt) && aligned16)) return false;
     const int64_t nvec = ceil_div(n, g.vec);
-    if (g.kind == mrn::kRowsPerWarp) {
+    if (g.kind == mrn::kTma) {
+        if (!aligned16 || g.vec != natural_vec(dt)) return false;
+        if (static_cast<int64_t>(g.threads / g.groups) * g.k < nvec) return false;
+        if (mrn::tma_shared_bytes(op, n * elem_bytes(dt), g.stages) > kTmaSharedBudget)
+            return false;
+        g.cluster = 1;
+        g.lanes = 0;
+        g.rows_per_cta = g.groups;
+    } else if (g.kind == mrn::kRowsPerWarp) {
         if (static_cast<int64_t>(g.lanes) * g.k < nvec) return false;
         g.cluster = 1;
         g.rows_per_cta = g.threads / g.lanes;
@@ -202,10 +261,10 @@ struct Call {
 mrn_status launch(const Call &c, bool aligned16, cudaStream_t stream) {
     Geometry g;
     if (t_forced) {
-        if (!resolve_forced(t_forced_geometry, c.n, c.dt, aligned16, &g))
+        if (!resolve_forced(t_forced_geometry, c.op, c.n, c.dt, aligned16, &g))
             return MRN_ERR_INVALID_GEOMETRY;
     } else {
-        g = choose_geometry(c.rows, c.n, c.dt, aligned16, sm_count_of_current_device());
+        g = choose_geometry(c.op, c.rows, c.n, c.dt, aligned16, sm_count_of_current_device());
     }
     KernelArgs a = c.args;
     a.n = c.n;
@@ -327,6 +386,7 @@ const char *mrn_status_string(mrn_status status) {
     case MRN_ERR_MISALIGNED: return "pointer not aligned to its element size";
     case MRN_ERR_CUDA: return "CUDA launch failed (see mrn_last_cuda_error)";
     case MRN_ERR_INVALID_GEOMETRY: return "forced geometry cannot cover this call";
+    case MRN_ERR_WAIT_TIMEOUT: return "a bounded wait in a kernel ran out (mrn_wait_timeouts)";
     }
     return "unknown status";
 }
@@ -343,9 +403,11 @@ mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtyp
     const bool a16 = aligned16 != 0 && (n * elem_bytes(dtype)) % 16 == 0;
     Geometry g;
     if (t_forced) {
-        if (!resolve_forced(t_forced_geometry, n, dtype, a16, &g)) return MRN_ERR_INVALID_GEOMETRY;
+        if (!resolve_forced(t_forced_geometry, static_cast<mrn::Op>(op), n, dtype, a16, &g))
+            return MRN_ERR_INVALID_GEOMETRY;
     } else {
-        g = choose_geometry(rows, n, dtype, a16, sm_count > 0 ? sm_count : sm_count_of_current_device());
+        g = choose_geometry(static_cast<mrn::Op>(op), rows, n, dtype, a16,
+                            sm_count > 0 ? sm_count : sm_count_of_current_device());
     }
     out->kind = g.kind;
     out->vec = g.vec;
@@ -354,6 +416,9 @@ mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtyp
     out->cluster = g.cluster;
     out->lanes_per_row = g.lanes;
     out->rows_per_cta = g.rows_per_cta;
+    out->stages = g.kind == mrn::kTma ? g.stages : 0;
+    out->ctas = g.kind == mrn::kTma ? g.ctas : 0;
+    out->groups = g.kind == mrn::kTma ? g.groups : 0;
     return MRN_OK;
 }
 
@@ -369,6 +434,10 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry) {
     g.threads = geometry->threads;
     g.cluster = geometry->cluster;
     g.lanes = geometry->lanes_per_row;
+    g.stages = geometry->stages;
+    g.ctas = geometry->ctas;
+    g.groups = geometry->groups;
+    if (g.kind == mrn::kTma && g.groups == 0) g.groups = 1;
     if (g.kind == mrn::kRowsPerWarp && g.threads == 0) g.threads = mrn::kWarpKernelThreads;
     if (g.kind == mrn::kStream) g.k = 1;
     if (g.kind != mrn::kCta) g.cluster = 1;
@@ -379,5 +448,16 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry) {
 }
 
 uint64_t mrn_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
+
+int mrn_wait_timeouts(void) {
+    const int a = mrn::take_wait_timeouts_rmsnorm();
+    const int b = mrn::take_wait_timeouts_then_add();
+    const int c = mrn::take_wait_timeouts_sandwich();
+    if (a < 0 || b < 0 || c < 0) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    return a + b + c;
+}
 
 }  // extern "C"

@@ -8,7 +8,7 @@
 namespace mrn {
 
 enum Op : int { kRmsnorm = 0, kThenAdd = 1, kSandwich = 2 };
-enum Kind : int { kAuto = 0, kRowsPerWarp = 1, kCta = 2, kStream = 3 };
+enum Kind : int { kAuto = 0, kRowsPerWarp = 1, kCta = 2, kStream = 3, kTma = 4 };
 
 // Launch-time view of one call.  Pointers are device pointers; row operands
 // are [rows x n] row-major.  For the sandwich, x = block_out, res = residual,
@@ -36,6 +36,9 @@ struct Geometry {
     int cluster;       // CTAs per row (kCta)
     int lanes;         // threads per row (kRowsPerWarp)
     int rows_per_cta;
+    int stages;        // shared-memory row stages (kTma)
+    int ctas;          // CTAs launched (kTma: persistent grid), 0 = from rows
+    int groups;        // warp groups per CTA (kTma), each on its own rows
 };
 
 // Register-slot limits per thread count: the kernels are compiled with these
@@ -44,7 +47,15 @@ constexpr int kMaxK = 8;
 constexpr int kWarpKernelThreads = 256;
 constexpr int kStreamMaxThreads = 512;
 constexpr int kMaxCluster = 16;
+constexpr int kTmaMaxStages = 4;
+constexpr int kSharedBytesPerCta = 232448;    // 227 KB opt-in limit on sm_100 / sm_103
 constexpr int cta_max_threads(int k) { return k <= 2 ? 1024 : (k <= 4 ? 512 : 256); }
+// Staged kernel: threads per warp group, and per CTA for 1 or 2 groups.
+constexpr int kTmaMaxGroups = 2;
+constexpr int tma_group_max_threads(int k) { return k <= 2 ? 512 : (k <= 4 ? 416 : 256); }
+constexpr int tma_max_threads(int k, int groups) {
+    return groups == 1 ? cta_max_threads(k) : groups * tma_group_max_threads(k);
+}
 
 // One launcher per operation; each returns the CUDA error of the launch(es).
 cudaError_t launch_rmsnorm(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
@@ -53,5 +64,15 @@ cudaError_t launch_then_add(bool bf16, const Geometry &g, const KernelArgs &a, i
                             cudaStream_t stream, uint64_t *launches);
 cudaError_t launch_sandwich(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
                             cudaStream_t stream, uint64_t *launches);
+
+// Dynamic shared memory of the staged (kTma) kernel for one operation.
+constexpr int64_t tma_shared_bytes(int op, int64_t row_bytes, int stages) {
+    return row_bytes * ((op == kSandwich ? 2 : 1) + stages * (op == kRmsnorm ? 1 : 2));
+}
+
+// Number of bounded waits that ran out since the last call (and reset them).
+int take_wait_timeouts_rmsnorm();
+int take_wait_timeouts_then_add();
+int take_wait_timeouts_sandwich();
 
 }  // namespace mrn

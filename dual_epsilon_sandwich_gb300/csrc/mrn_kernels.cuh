@@ -30,11 +30,27 @@
 // every CTA of the cluster reaches unconditionally.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "mrn_internal.h"
+
+// Compile-time cache-policy switches (defaults are the measured best):
+//   MRN_STORE_STREAMING  1: outputs stored with .cs (evict-first in L2)
+//   MRN_BULK_EVICT_FIRST 1: staged row copies carry an L2 evict-first policy
+#ifndef MRN_STORE_STREAMING
+#define MRN_STORE_STREAMING 0
+#endif
+#ifndef MRN_BULK_EVICT_FIRST
+#define MRN_BULK_EVICT_FIRST 1
+#endif
+#if MRN_STORE_STREAMING
+#define MRN_ST_OP "st.global.cs"
+#else
+#define MRN_ST_OP "st.global"
+#endif
 
 namespace mrn {
 
@@ -143,18 +159,18 @@ __device__ __forceinline__ void ld_plain(Frag<BF16, 1> &f, const void *p) {
 }
 
 __device__ __forceinline__ void st_global(void *p, const Frag<F32, 4> &f) {
-    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+    asm volatile(MRN_ST_OP ".v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(f.w[0]), "r"(f.w[1]), "r"(f.w[2]), "r"(f.w[3]) : "memory");
 }
 __device__ __forceinline__ void st_global(void *p, const Frag<BF16, 8> &f) {
-    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+    asm volatile(MRN_ST_OP ".v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(f.w[0]), "r"(f.w[1]), "r"(f.w[2]), "r"(f.w[3]) : "memory");
 }
 __device__ __forceinline__ void st_global(void *p, const Frag<F32, 1> &f) {
-    asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(f.w) : "memory");
+    asm volatile(MRN_ST_OP ".u32 [%0], %1;" :: "l"(p), "r"(f.w) : "memory");
 }
 __device__ __forceinline__ void st_global(void *p, const Frag<BF16, 1> &f) {
-    asm volatile("st.global.u16 [%0], %1;" :: "l"(p), "h"(f.h) : "memory");
+    asm volatile(MRN_ST_OP ".u16 [%0], %1;" :: "l"(p), "h"(f.h) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -466,8 +482,300 @@ mrn_stream_kernel(const KernelArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// Persistent, TMA-staged kernel.  Each CTA owns rows blockIdx.x, +gridDim.x,
+// ...  and keeps `stages` of them in flight in shared memory: the row (and
+// the residual) of a future row arrive by cp.async.bulk while the current
+// row is reduced and written, so HBM reads never wait for the reductions.
+// The gammas are copied into shared memory once per CTA.  A stage is
+// refilled right after the first reduction of the row it held: that
+// reduction's barrier is the point after which every thread has moved the
+// stage into registers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_to_shared(void *dst, const void *src, uint32_t bytes,
+                                               uint64_t *bar) {
+#if MRN_BULK_EVICT_FIRST
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+                 "[%0], [%1], %2, [%3], %4;"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+                 : "memory");
+#else
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+                 "[%0], [%1], %2, [%3];"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+#endif
+}
+
+// Every wait on an mbarrier is bounded: about one second of wall time (and
+// an iteration cap) after which the wait reports failure.  A failed wait is
+// counted in g_wait_timeouts, the CTA agrees on it at its next barrier,
+// drains the copies it has in flight (again bounded) and returns without
+// writing the row.  With the copies issued here a wait never runs out.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+static __device__ unsigned int g_wait_timeouts;   // one per translation unit
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1; i < (1u << 28); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
+    return false;
+}
+
+// Shared-memory loads of staged rows; the memory clobber keeps them ahead of
+// the barrier after which the stage is refilled.
+__device__ __forceinline__ void ld_shared(Frag<F32, 4> &f, const void *p) {
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "r"(smem_addr(p))
+                 : "memory");
+}
+__device__ __forceinline__ void ld_shared(Frag<BF16, 8> &f, const void *p) {
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "r"(smem_addr(p))
+                 : "memory");
+}
+
+// Copy one row of x (and of the residual when NS == 2) into a stage.
+template <int NS>
+__device__ __forceinline__ void stage_row(unsigned char *dst, const char *x, const char *res,
+                                          int64_t offset, uint32_t rb, uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, NS * rb);
+    bulk_to_shared(dst, x + offset, rb, bar);
+    if (NS == 2) bulk_to_shared(dst + rb, res + offset, rb, bar);
+}
+
+// Named barrier `id` over `count` threads (a multiple of 32).
+__device__ __forceinline__ void group_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+// Named barrier that also returns the OR of `flag` over the participants.
+__device__ __forceinline__ int group_sync_or(int id, int count, int flag) {
+    int any;
+    asm volatile("{\n\t.reg .pred q, p;\n\t"
+                 "setp.ne.s32 q, %1, 0;\n\t"
+                 "bar.red.or.pred p, %2, %3, q;\n\t"
+                 "selp.s32 %0, 1, 0, p;\n\t}"
+                 : "=r"(any) : "r"(flag), "r"(id), "r"(count) : "memory");
+    return any;
+}
+
+// Sum of v over the `count` threads of one warp group (named barrier `id`),
+// optionally ORing a failure flag across the group in the same barrier.
+template <bool VOTE>
+__device__ __forceinline__ float wg_allsum(float v, ReduceSlots &s, int id, int count,
+                                              int gtid, int flag, int *any) {
+    v = warp_allsum(v);
+    const int lane = gtid & 31;
+    const int warp = gtid >> 5;
+    if (lane == 0) s.warp[warp] = v;
+    if (VOTE) {
+        *any = group_sync_or(id, count, flag);
+    } else {
+        group_sync(id, count);
+    }
+    return warp_allsum(lane < (count >> 5) ? s.warp[lane] : 0.0f);
+}
+
+// G warp groups share the stage ring and the gammas; group g handles the
+// CTA's rows it = g, g+G, ...  so that G rows are reduced and written at the
+// same time while the other stages are being filled.  Each group reduces
+// over its own named barrier (ids 1..G).  `stages` must be a multiple of G:
+// stage s then only ever holds rows of group s % G, so every wait on a stage
+// barrier comes after the previous use of that stage has completed (a parity
+// wait cannot tell a phase from the one two steps earlier), and every refill
+// follows the consumption of the row it replaces.  If any wait runs out, the group
+// that sees it raises `abort`; every group stops at its next vote, all meet
+// at a CTA barrier, and thread 0 drains (bounded) every stage copy still in
+// flight before the CTA exits.
+template <int OP, class T, int K, int G>
+__global__ void __launch_bounds__(tma_max_threads(K, G), 1)
+mrn_tma_kernel(const KernelArgs a, const int stages) {
+    constexpr int VEC = 16 / T::kBytes;
+    using Fr = Frag<T, VEC>;
+    constexpr int NS = (OP == kRmsnorm) ? 1 : 2;   // row operands staged per row
+    constexpr int NG = (OP == kSandwich) ? 2 : 1;  // gammas kept in shared memory
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ ReduceSlots slots1[G];
+    __shared__ ReduceSlots slots2[G];
+    __shared__ __align__(8) uint64_t bars[kTmaMaxStages + 1];   // [stages] = the gammas
+    __shared__ int issued[kTmaMaxStages];
+    __shared__ int consumed[kTmaMaxStages];
+    __shared__ volatile int abort_flag;
+
+    const uint32_t rb = static_cast<uint32_t>(a.n * T::kBytes);
+    unsigned char *const gsm = smem;
+    unsigned char *const stage0 = smem + NG * rb;
+    const int tid = threadIdx.x;
+    const int gsize = blockDim.x / G;
+    const int grp = tid / gsize;
+    const int gtid = tid - grp * gsize;
+    const int bar_id = 1 + grp;
+    const int64_t first = a.row0 + blockIdx.x;
+    const int64_t step = gridDim.x;
+    const int64_t my_rows = first < a.rows_end ? (a.rows_end - first + step - 1) / step : 0;
+    const int64_t row_bytes = a.n * T::kBytes;
+    const char *const xg = static_cast<const char *>(a.x);
+    const char *const rg = static_cast<const char *>(a.res);
+    if (stages < G || stages > kTmaMaxStages || stages % G != 0) {
+        // The host never launches this; refuse rather than start any copy.
+        if (tid == 0) atomicAdd(&g_wait_timeouts, 1u);
+        return;
+    }
+
+    if (tid == 0) {
+        for (int s = 0; s <= stages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < kTmaMaxStages; ++s) issued[s] = consumed[s] = 0;
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0 && my_rows > 0) {
+        mbar_arrive_expect_tx(&bars[stages], NG * rb);
+        bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
+        if (NG == 2) bulk_to_shared(gsm + rb, a.g2, rb, &bars[stages]);
+        for (int s = 0; s < stages && s < my_rows; ++s) {
+            stage_row<NS>(stage0 + s * NS * rb, xg, rg, (first + s * step) * row_bytes, rb,
+                          &bars[s]);
+            issued[s] = 1;
+        }
+    }
+    int failed = (my_rows > 0 && !mbar_wait_bounded(&bars[stages], 0)) ? 1 : 0;
+
+    for (int64_t it = grp; it < my_rows; it += G) {
+        const int s = static_cast<int>(it % stages);
+        const uint32_t parity = static_cast<uint32_t>((it / stages) & 1);
+        const int64_t row = first + it * step;
+        if (!failed && !mbar_wait_bounded(&bars[s], parity)) failed = 1;
+
+        Fr xv[K];
+        Fr rv[K];
+        const unsigned char *sp = stage0 + s * NS * rb;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+            if (v < a.nvec) {
+                ld_shared(xv[k], sp + v * 16);
+                if (NS == 2) ld_shared(rv[k], sp + rb + v * 16);
+            } else {
+                xv[k].zero();
+                rv[k].zero();
+            }
+        }
+        float ss = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) ss += frag_sum_sq(xv[k]);
+        int any_failed;
+        const float tot = wg_allsum<true>(ss, slots1[grp], bar_id, gsize, gtid,
+                                             failed | abort_flag, &any_failed);
+        if (any_failed) {
+            if (gtid == 0) abort_flag = 1;
+            break;
+        }
+        // Every thread of the group holds its part of the stage now: refill it.
+        if (gtid == 0) {
+            consumed[s] += 1;
+            if (it + stages < my_rows) {
+                fence_proxy_async_smem();
+                stage_row<NS>(stage0 + s * NS * rb, xg, rg,
+                              (first + (it + stages) * step) * row_bytes, rb, &bars[s]);
+                issued[s] += 1;
+            }
+        }
+        const float inv1 = inv_rms(tot, a.n, a.eps1);
+        const int64_t row_elem = row * a.n;
+
+        if (OP == kRmsnorm || OP == kThenAdd) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+                if (v >= a.nvec) continue;
+                Fr g;
+                ld_shared(g, gsm + v * 16);
+                const Fr o = (OP == kRmsnorm) ? apply_norm(xv[k], inv1, g)
+                                              : apply_norm_add(xv[k], inv1, g, rv[k]);
+                st_global(elem_ptr<T>(a.y, row_elem + v * VEC), o);
+            }
+            continue;
+        }
+        float ss2 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+            if (v >= a.nvec) continue;
+            Fr g;
+            ld_shared(g, gsm + v * 16);
+            rv[k] = apply_norm_add(xv[k], inv1, g, rv[k]);
+            st_global(elem_ptr<T>(a.y, row_elem + v * VEC), rv[k]);
+            ss2 += frag_sum_sq(rv[k]);
+        }
+        const float inv2 = inv_rms(wg_allsum<false>(ss2, slots2[grp], bar_id, gsize, gtid, 0,
+                                                       nullptr),
+                                   a.n, a.eps2);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+            if (v >= a.nvec) continue;
+            Fr g;
+            ld_shared(g, gsm + rb + v * 16);
+            st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(rv[k], inv2, g));
+        }
+    }
+
+    // Exit: with no failure every issued copy was consumed.  After a failure,
+    // wait (bounded) for the copies still in flight so that none lands after
+    // the CTA has left its shared memory.
+    __syncthreads();
+    if (tid == 0 && my_rows > 0 && abort_flag) {
+        atomicAdd(&g_wait_timeouts, 1u);
+        (void)mbar_wait_bounded(&bars[stages], 0);
+        for (int s = 0; s < stages; ++s) {
+            if (issued[s] > consumed[s])
+                (void)mbar_wait_bounded(&bars[s], static_cast<uint32_t>(consumed[s] & 1));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Host-side launch of one operation (instantiated once per .cu file).
 // ---------------------------------------------------------------------------
+// Rows per launch, so that grid.x stays far below 2^31 - 1 for any cluster.
+constexpr int64_t kRowsPerLaunch = int64_t(1) << 26;
+
 using WarpKernelFn = void (*)(KernelArgs, int);
 using CtaKernelFn = void (*)(KernelArgs);
 
@@ -485,8 +793,102 @@ template <int OP, class T, int VEC> struct KernelTable {
     static constexpr CtaKernelFn stream = mrn_stream_kernel<OP, T, VEC>;
 };
 
-// Rows per launch, so that grid.x stays far below 2^31 - 1 for any cluster.
-constexpr int64_t kRowsPerLaunch = int64_t(1) << 26;
+template <int OP, class T> struct TmaTable {
+    static constexpr WarpKernelFn fn[2][kMaxK] = {
+        {mrn_tma_kernel<OP, T, 1, 1>, mrn_tma_kernel<OP, T, 2, 1>, mrn_tma_kernel<OP, T, 3, 1>,
+         mrn_tma_kernel<OP, T, 4, 1>, mrn_tma_kernel<OP, T, 5, 1>, mrn_tma_kernel<OP, T, 6, 1>,
+         mrn_tma_kernel<OP, T, 7, 1>, mrn_tma_kernel<OP, T, 8, 1>},
+        {mrn_tma_kernel<OP, T, 1, 2>, mrn_tma_kernel<OP, T, 2, 2>, mrn_tma_kernel<OP, T, 3, 2>,
+         mrn_tma_kernel<OP, T, 4, 2>, mrn_tma_kernel<OP, T, 5, 2>, mrn_tma_kernel<OP, T, 6, 2>,
+         mrn_tma_kernel<OP, T, 7, 2>, mrn_tma_kernel<OP, T, 8, 2>}};
+};
+
+// Persistent grid of the staged kernel: as many CTAs as fit on the device
+// (SM count x CTAs per SM), at most one per row.  Occupancy answers are
+// cached per (kernel, threads, shared bytes); the SM count per device.
+inline int device_sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    int count = 0;
+    if (cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (dev >= 0 && dev < 64) cached[dev] = count;
+    return count;
+}
+
+// Per-kernel, per-device launch facts of the staged kernel, cached after the
+// first launch: the dynamic shared memory it was opened up to, and the CTAs
+// per SM at the last (threads, shared bytes) asked for.  Races between
+// threads only repeat an idempotent runtime call.
+constexpr int kMaxCachedDevices = 64;
+struct TmaLaunchCache {
+    std::atomic<int64_t> shared_opened{0};
+    std::atomic<int64_t> occ_key{-1};
+    std::atomic<int> occ_per_sm{0};
+};
+
+template <int OP, class T>
+cudaError_t launch_tma(const Geometry &g, KernelArgs a, int64_t rows, cudaStream_t stream,
+                       uint64_t *launches) {
+    static TmaLaunchCache cache[kMaxCachedDevices][2][kMaxK];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    TmaLaunchCache uncached;
+    const int gi = g.groups - 1;
+    TmaLaunchCache &c =
+        (dev >= 0 && dev < kMaxCachedDevices) ? cache[dev][gi][g.k - 1] : uncached;
+    const WarpKernelFn fn = TmaTable<OP, T>::fn[gi][g.k - 1];
+    const int64_t shared = tma_shared_bytes(OP, a.n * T::kBytes, g.stages);
+    cudaError_t err;
+    if (c.shared_opened.load(std::memory_order_relaxed) < shared) {
+        err = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(shared));
+        if (err != cudaSuccess) return err;
+        c.shared_opened.store(shared, std::memory_order_relaxed);
+    }
+    int64_t ctas = g.ctas;
+    if (ctas <= 0) {
+        const int64_t key = shared * 2048 + g.threads;
+        int per_sm = c.occ_key.load(std::memory_order_relaxed) == key
+                         ? c.occ_per_sm.load(std::memory_order_relaxed) : 0;
+        if (per_sm == 0) {
+            err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, g.threads,
+                                                                static_cast<size_t>(shared));
+            if (err != cudaSuccess) return err;
+            if (per_sm < 1) return cudaErrorInvalidConfiguration;
+            c.occ_per_sm.store(per_sm, std::memory_order_relaxed);
+            c.occ_key.store(key, std::memory_order_relaxed);
+        }
+        ctas = static_cast<int64_t>(device_sm_count()) * per_sm;
+        if (ctas < 1) return cudaErrorInvalidDevice;
+    }
+    for (int64_t r0 = 0; r0 < rows; r0 += kRowsPerLaunch) {
+        const int64_t nrows = rows - r0 < kRowsPerLaunch ? rows - r0 : kRowsPerLaunch;
+        a.row0 = r0;
+        a.rows_end = r0 + nrows;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(ctas < nrows ? ctas : nrows), 1, 1);
+        cfg.blockDim = dim3(g.threads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(shared);
+        cfg.stream = stream;
+        err = cudaLaunchKernelEx(&cfg, fn, a, g.stages);
+        if (err != cudaSuccess) return err;
+        ++*launches;
+    }
+    return cudaSuccess;
+}
+
+template <int OP> int take_wait_timeouts() {
+    unsigned int count = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&count, g_wait_timeouts, sizeof(count)) != cudaSuccess) return -1;
+    if (count != 0 && cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero)) != cudaSuccess)
+        return -1;
+    return static_cast<int>(count);
+}
+
 
 template <int OP, class T, int VEC>
 cudaError_t launch_typed(const Geometry &g, KernelArgs a, int64_t rows, cudaStream_t stream,
@@ -536,6 +938,10 @@ cudaError_t launch_typed(const Geometry &g, KernelArgs a, int64_t rows, cudaStre
 template <int OP>
 cudaError_t launch_op(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
                       cudaStream_t stream, uint64_t *launches) {
+    if (g.kind == kTma) {
+        return bf16 ? launch_tma<OP, BF16>(g, a, rows, stream, launches)
+                    : launch_tma<OP, F32>(g, a, rows, stream, launches);
+    }
     if (bf16) {
         return g.vec == 1 ? launch_typed<OP, BF16, 1>(g, a, rows, stream, launches)
                           : launch_typed<OP, BF16, 8>(g, a, rows, stream, launches);

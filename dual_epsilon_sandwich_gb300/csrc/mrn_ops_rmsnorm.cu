@@ -9,4 +9,6 @@ cudaError_t launch_rmsnorm(bool bf16, const Geometry &g, const KernelArgs &a, in
     return launch_op<kRmsnorm>(bf16, g, a, rows, stream, launches);
 }
 
+int take_wait_timeouts_rmsnorm() { return take_wait_timeouts<kRmsnorm>(); }
+
 }  // namespace mrn

@@ -9,4 +9,6 @@ cudaError_t launch_sandwich(bool bf16, const Geometry &g, const KernelArgs &a, i
     return launch_op<kSandwich>(bf16, g, a, rows, stream, launches);
 }
 
+int take_wait_timeouts_sandwich() { return take_wait_timeouts<kSandwich>(); }
+
 }  // namespace mrn

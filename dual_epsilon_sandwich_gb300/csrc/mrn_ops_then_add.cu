@@ -9,4 +9,6 @@ cudaError_t launch_then_add(bool bf16, const Geometry &g, const KernelArgs &a, i
     return launch_op<kThenAdd>(bf16, g, a, rows, stream, launches);
 }
 
+int take_wait_timeouts_then_add() { return take_wait_timeouts<kThenAdd>(); }
+
 }  // namespace mrn

@@ -30,6 +30,7 @@ MRN_GEOM_AUTO = 0
 MRN_GEOM_ROWS_PER_WARP = 1
 MRN_GEOM_CTA = 2
 MRN_GEOM_STREAM = 3
+MRN_GEOM_TMA = 4
 
 STATUS = {
     0: "MRN_OK",
@@ -41,13 +42,14 @@ STATUS = {
     6: "MRN_ERR_MISALIGNED",
     7: "MRN_ERR_CUDA",
     8: "MRN_ERR_INVALID_GEOMETRY",
+    9: "MRN_ERR_WAIT_TIMEOUT",
 }
 for _code, _name in STATUS.items():
     globals()[_name] = _code
 
 EXPORTS = ("mrn_rmsnorm", "mrn_rmsnorm_then_add", "mrn_norm_residual_norm",
            "mrn_status_string", "mrn_last_cuda_error", "mrn_query_geometry",
-           "mrn_force_geometry", "mrn_launch_count")
+           "mrn_force_geometry", "mrn_launch_count", "mrn_wait_timeouts")
 
 
 class MrnError(RuntimeError):
@@ -63,7 +65,9 @@ class MrnError(RuntimeError):
 class MrnGeometry(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("vec", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("cluster", ctypes.c_int32),
-                ("lanes_per_row", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32)]
+                ("lanes_per_row", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("ctas", ctypes.c_int32),
+                ("groups", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -107,6 +111,8 @@ def lib() -> ctypes.CDLL:
             L.mrn_force_geometry.restype = _i
             L.mrn_launch_count.argtypes = []
             L.mrn_launch_count.restype = ctypes.c_uint64
+            L.mrn_wait_timeouts.argtypes = []
+            L.mrn_wait_timeouts.restype = _i
             _lib = L
     return _lib
 
@@ -155,6 +161,11 @@ def mrn_force_geometry(geometry: dict | None) -> int:
 
 def mrn_launch_count() -> int:
     return lib().mrn_launch_count()
+
+
+def mrn_wait_timeouts() -> int:
+    """Bounded waits that ran out since the last call (synchronises the device)."""
+    return lib().mrn_wait_timeouts()
 
 
 # ---------------------------------------------------------------------------

@@ -77,7 +77,10 @@ typedef enum mrn_status {
     MRN_ERR_ALIASING = 5,          /* a forbidden overlap between buffers */
     MRN_ERR_MISALIGNED = 6,        /* a pointer not aligned to its element size */
     MRN_ERR_CUDA = 7,              /* the CUDA runtime refused the launch */
-    MRN_ERR_INVALID_GEOMETRY = 8   /* a forced geometry cannot cover the row */
+    MRN_ERR_INVALID_GEOMETRY = 8,  /* a forced geometry cannot cover the row */
+    MRN_ERR_WAIT_TIMEOUT = 9       /* a kernel's bounded wait ran out (see
+                                      mrn_wait_timeouts); outputs of the affected
+                                      rows were not written */
 } mrn_status;
 
 /*
@@ -150,7 +153,11 @@ typedef enum mrn_geometry_kind {
     MRN_GEOM_CTA = 2,           /* one row per CTA, or per thread-block cluster of
                                    `cluster` CTAs with a DSMEM reduction; row held
                                    in registers */
-    MRN_GEOM_STREAM = 3         /* one row per CTA, looped over the row: any n */
+    MRN_GEOM_STREAM = 3,        /* one row per CTA, looped over the row: any n */
+    MRN_GEOM_TMA = 4            /* persistent CTAs; `stages` future rows are copied
+                                   into shared memory by cp.async.bulk while the
+                                   current one is reduced; gammas kept in shared
+                                   memory; needs 16-byte aligned rows */
 } mrn_geometry_kind;
 
 typedef struct mrn_geometry {
@@ -160,7 +167,11 @@ typedef struct mrn_geometry {
     int32_t threads;       /* threads per CTA */
     int32_t cluster;       /* CTAs per row (1 unless MRN_GEOM_CTA is split) */
     int32_t lanes_per_row; /* threads per row for MRN_GEOM_ROWS_PER_WARP */
-    int32_t rows_per_cta;  /* rows one CTA handles */
+    int32_t rows_per_cta;  /* rows one CTA handles at a time */
+    int32_t stages;        /* MRN_GEOM_TMA: rows staged in shared memory (1..4) */
+    int32_t ctas;          /* MRN_GEOM_TMA: persistent CTAs (0 = fill the device) */
+    int32_t groups;        /* MRN_GEOM_TMA: warp groups per CTA (1 or 2), each
+                              reducing its own rows; threads is the CTA total */
 } mrn_geometry;
 
 /*
@@ -183,6 +194,16 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry);
 
 /* Number of kernels this library has launched in the process (all threads). */
 uint64_t mrn_launch_count(void);
+
+/*
+ * Number of bounded waits (on the shared-memory copy barriers of the
+ * MRN_GEOM_TMA kernels) that ran out on the current device since the previous
+ * call, which resets the count; -1 if the count could not be read.  Every
+ * wait gives up after about one second; the CTA then drains its copies and
+ * returns without writing its remaining rows, so the context stays usable.
+ * Synchronises the device.  Not on the pages: a diagnostic of this library.
+ */
+int mrn_wait_timeouts(void);
 
 #ifdef __cplusplus
 }

@@ -48,7 +48,7 @@ def test_exports_every_declared_symbol(library):
 
 
 def test_status_strings():
-    for code in range(9):
+    for code in range(10):
         assert mrn.mrn_status_string(code)
     assert "unknown" in mrn.mrn_status_string(99)
     assert mrn.mrn_last_cuda_error() == 0
@@ -142,6 +142,15 @@ def test_geometry_covers_every_row_width():
                             assert g["threads"] % 32 == 0 and 1 <= g["cluster"] <= 16
                             cap = 1024 if g["k"] <= 2 else (512 if g["k"] <= 4 else 256)
                             assert g["threads"] <= cap
+                        elif g["kind"] == mrn.MRN_GEOM_TMA:
+                            assert a16 and rows >= 152
+                            per_group = g["threads"] // g["groups"]
+                            assert per_group * g["k"] >= nvec and per_group % 32 == 0
+                            assert 2 <= g["stages"] <= 4 and g["ctas"] == 0
+                            assert g["groups"] in (1, 2) and g["stages"] % g["groups"] == 0
+                            ng = 2 if op == 2 else 1
+                            ns = 1 if op == 0 else 2
+                            assert (ng + g["stages"] * ns) * n * e <= 232448 - 1024
                         else:
                             assert g["kind"] == mrn.MRN_GEOM_STREAM
                             assert nvec > 16 * 2048
@@ -156,6 +165,15 @@ def test_force_geometry_validation():
         {"kind": 2, "k": 1, "threads": 100, "cluster": 1},
         {"kind": 2, "k": 1, "threads": 128, "cluster": 17},
         {"kind": 3, "threads": 1024},
+        {"kind": 4, "k": 4, "threads": 416, "stages": 0},
+        {"kind": 4, "k": 4, "threads": 416, "stages": 5},
+        {"kind": 4, "k": 8, "threads": 512, "stages": 2},
+        {"kind": 4, "k": 2, "threads": 96, "stages": 2, "ctas": -1},
+        {"kind": 4, "k": 4, "threads": 832, "stages": 3, "groups": 3},
+        {"kind": 4, "k": 4, "threads": 832, "stages": 1, "groups": 2},     # a stage per group
+        {"kind": 4, "k": 7, "threads": 512, "stages": 3, "groups": 2},     # stages % groups
+        {"kind": 4, "k": 4, "threads": 800, "stages": 2, "groups": 2},     # 400 not a warp multiple
+        {"kind": 4, "k": 8, "threads": 1024, "stages": 2, "groups": 2},    # 512 > 256 per group
         {"kind": 9},
     ]
     for g in bad:
@@ -167,6 +185,18 @@ def test_force_geometry_validation():
         mrn.mrn_query_geometry(0, 8, 4096, mrn.MRN_F32, True, 152)
     assert mrn.mrn_force_geometry(None) == 0
     assert mrn.mrn_query_geometry(0, 8, 4096, mrn.MRN_F32, True, 152)["kind"] == 2
+    # staged kernel: needs aligned rows and shared memory for the stages
+    assert mrn.mrn_force_geometry({"kind": 4, "k": 4, "threads": 416, "stages": 3}) == 0
+    got = mrn.mrn_query_geometry(2, 4096, 6656, mrn.MRN_F32, True, 152)
+    assert (got["kind"], got["k"], got["threads"], got["stages"]) == (4, 4, 416, 3)
+    with pytest.raises(mrn.MrnError):          # misaligned rows cannot be bulk-copied
+        mrn.mrn_query_geometry(2, 4096, 6656, mrn.MRN_F32, False, 152)
+    assert mrn.mrn_force_geometry({"kind": 4, "k": 4, "threads": 416, "stages": 4}) == 0
+    with pytest.raises(mrn.MrnError):          # (2 + 4*2) rows of 26 KB exceed 227 KB
+        mrn.mrn_query_geometry(2, 4096, 6656, mrn.MRN_F32, True, 152)
+    assert mrn.mrn_force_geometry(None) == 0
+    assert mrn.mrn_query_geometry(2, 4096, 6656, mrn.MRN_F32, True, 152)["kind"] == 4
+    assert mrn.mrn_query_geometry(2, 1, 6656, mrn.MRN_F32, True, 152)["kind"] == 2
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path):

@@ -275,3 +275,44 @@ def test_tensor_convenience_api():
     with pytest.raises(mrn.MrnError) as exc:          # output overlaps x by all but one element
         mrn.rmsnorm_then_add(x2, g, r, 1e-5, out=base[1:].view(5, 768))
     assert exc.value.status == mrn.MRN_ERR_ALIASING
+
+
+# The persistent TMA-staged kernel: stages 1..4, persistent grids from one CTA
+# (every row through one pipeline) to the full device, ragged register coverage.
+FORCED_TMA = [
+    ({"kind": 4, "k": 4, "threads": 416, "stages": 3}, 1664, 1000),
+    ({"kind": 4, "k": 1, "threads": 1024, "stages": 1, "ctas": 7}, 1024, 50),
+    ({"kind": 4, "k": 2, "threads": 96, "stages": 4, "ctas": 5}, 190, 333),
+    ({"kind": 4, "k": 8, "threads": 256, "stages": 2}, 2000, 400),
+    ({"kind": 4, "k": 3, "threads": 64, "stages": 2, "ctas": 1}, 150, 37),
+    ({"kind": 4, "k": 5, "threads": 128, "stages": 3, "ctas": 300}, 600, 7),
+    ({"kind": 4, "k": 7, "threads": 512, "stages": 2, "groups": 2}, 1664, 1000),
+    ({"kind": 4, "k": 4, "threads": 832, "stages": 2, "groups": 2}, 1664, 300),
+    ({"kind": 4, "k": 4, "threads": 256, "stages": 4, "groups": 2, "ctas": 19}, 250, 500),
+    ({"kind": 4, "k": 2, "threads": 192, "stages": 2, "groups": 2, "ctas": 3}, 190, 101),
+    ({"kind": 4, "k": 1, "threads": 64, "stages": 4, "groups": 2, "ctas": 1}, 20, 9),
+]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("geom,nvec,rows", FORCED_TMA, ids=[str(i) for i in range(len(FORCED_TMA))])
+def test_forced_staged_kernel(geom, nvec, rows, dtype):
+    n = nvec * (4 if dtype == "f32" else 8)
+    assert mrn.mrn_force_geometry(geom) == 0
+    g = mrn.mrn_query_geometry(2, rows, n, gu.code(dtype), True)
+    assert g["kind"] == mrn.MRN_GEOM_TMA
+    all_ops(rows_data(n * 7 + rows, rows, n, dtype), dtype, f"staged {geom} {rows}x{n}")
+    mrn.mrn_force_geometry(None)
+    assert mrn.mrn_wait_timeouts() == 0
+
+
+def test_staged_kernel_is_the_automatic_choice_for_batches():
+    for op in (0, 1, 2):
+        assert mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True)["kind"] == \
+            mrn.MRN_GEOM_TMA
+        assert mrn.mrn_query_geometry(op, 16384, 4096, mrn.MRN_BF16, True)["kind"] == \
+            mrn.MRN_GEOM_TMA
+    assert mrn.mrn_query_geometry(2, 1, 6656, mrn.MRN_F32, True)["kind"] == mrn.MRN_GEOM_CTA
+    d = rows_data(14, 2048, 6656, "f32")
+    all_ops(d, "f32", "auto staged 2048x6656")
+    assert mrn.mrn_wait_timeouts() == 0
