@@ -52,7 +52,11 @@ def parse_args(argv=None):
     p.add_argument("--decode-calls", type=int, default=2000)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--reference-seconds", type=float, default=120.0,
+                   help="--impl reference: wall time budget of the whole run")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-secondary", action="store_true",
+                   help="skip the bf16 16384x4096 and f32 4x6656 secondary measurements")
     p.add_argument("--profile-launches", type=int, default=0,
                    help="only run --warmup + this many launches of the timed call (for ncu)")
     return p.parse_args(argv)
@@ -73,6 +77,17 @@ def shard_rows(total_rows: int, world: int, rank: int):
     base, extra = divmod(total_rows, world)
     start = rank * base + min(rank, extra)
     return start, start + base + (1 if rank < extra else 0)
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest `value` over all ranks (one scalar all-reduce; identity
+    without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def sandwich_bytes(rows: int, n: int, elem: int = 4) -> int:
@@ -229,7 +244,7 @@ def run_reference(args):
     calib_rows = min(args.rows, 256)
     runner.one_pass(calib_rows)
     rows_per_s = calib_rows / runner.one_pass(calib_rows)
-    per_step = 120.0 / max(1, args.steps + args.warmup)
+    per_step = args.reference_seconds / max(1, args.steps + args.warmup)
     sample_rows = int(min(args.rows, max(8, rows_per_s * per_step)))
     for _ in range(args.warmup):
         runner.one_pass(sample_rows)
@@ -315,9 +330,10 @@ def run_mrn(args):
         return 0
 
     # -- device-resident timed region -------------------------------------
+    # One launch per step, back to back on one stream, bracketed by a barrier
+    # and a synchronize on both sides; the average launch duration is the
+    # region's time over K (the region holds nothing but these launches).
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev.index if world == 1 else local)
@@ -329,22 +345,16 @@ def run_mrn(args):
     launches0 = mrn.mrn_launch_count()
     t_begin.record(stream)
     for i in range(K):
-        starts[i].record(stream)
         call(sets[i % 2])
-        ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if pg is not None:
         pg.barrier()
     clocks = sampler.stop()
     launches = mrn.mrn_launch_count() - launches0
-    total_ms = t_begin.elapsed_time(t_end)
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    avg_kernel_ms = sum(kernel_ms) / K
-    if pg is not None:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    local_ms = t_begin.elapsed_time(t_end)
+    total_ms = max_over_ranks(local_ms, pg, dev)
+    avg_kernel_ms = local_ms / launches
     step_bytes = sandwich_bytes(rows, n)
     value = world * step_bytes * K / (total_ms * 1e-3) / 1e9
     achieved = step_bytes / (avg_kernel_ms * 1e-3) / 1e9
@@ -376,14 +386,12 @@ def run_mrn(args):
     for _ in range(args.e2e_steps):
         e2e_step()
     e2e_s = (time.perf_counter() - t0) / args.e2e_steps
-    if pg is not None:
-        t = torch.tensor([e2e_s], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, pg, dev)
     e2e_value = world * step_bytes / e2e_s / 1e9
 
     # -- decode latency: rows=1, n=6656 ---------------------------------------
     decode = decode_latency(args, dev, stream)
+    secondary = {} if args.no_secondary else secondary_workloads(dev, stream)
 
     peak, peak_kind = measured_peaks()
     traffic = profiled_traffic()
@@ -409,6 +417,7 @@ def run_mrn(args):
                 "d2h_bytes_per_step": d2h, "note": "pinned host buffers, H2D + kernel + D2H "
                 "of both outputs, per step"},
         "decode": decode,
+        "secondary": secondary,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         runner = OracleRunner([a[k].astype(np.float64) for k in ("block_out", "residual",
@@ -507,6 +516,89 @@ def decode_latency(args, dev, stream):
             "us_per_call_graph": graph_us, "us_per_call_graph_l2_hot": hot_us,
             "bytes_per_call": sandwich_bytes(1, n), "rotating_sets": nsets,
             "geometry": geometry}
+
+
+def secondary_workloads(dev, stream):
+    """The other two measured workloads: Llama-style bf16 plain RMSNorm and
+    then-add at 16384 x 4096 (GB/s, two rotating buffer sets of >= 268 MB), and
+    plain f32 RMSNorm at 4 x 6656 (us/call in a CUDA graph over 512 rotating
+    buffer sets, 122 MB > L2)."""
+    import torch
+
+    from dual_epsilon_sandwich_gb300 import mrn
+    from dual_epsilon_sandwich_gb300 import workloads as wl
+    out = {}
+    sh = stream.cuda_stream
+    w = wl.llama_bf16()
+    a = w.arrays
+
+    def bf16(arr):
+        return torch.from_numpy(arr.view("int16")).to(dev).view(torch.bfloat16)
+
+    sets = [(bf16(a["x"]), bf16(a["gamma"]), bf16(a["residual"])) for _ in range(2)]
+    outs = [torch.empty_like(sets[0][0]) for _ in range(2)]
+    rows, n = w.rows, w.n
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, op, nbytes in (("rmsnorm_bf16_rows16384_n4096", 0, (2 * rows * n + n) * 2),
+                             ("then_add_bf16_rows16384_n4096", 1, (3 * rows * n + n) * 2)):
+        def call(i):
+            x, g, r = sets[i % 2]
+            y = outs[i % 2]
+            if op == 0:
+                st = mrn.mrn_rmsnorm(x.data_ptr(), g.data_ptr(), y.data_ptr(), rows, n, w.eps,
+                                     mrn.MRN_BF16, sh)
+            else:
+                st = mrn.mrn_rmsnorm_then_add(x.data_ptr(), g.data_ptr(), r.data_ptr(),
+                                              y.data_ptr(), rows, n, w.eps, mrn.MRN_BF16, sh)
+            if st != 0:
+                raise mrn.MrnError(st, name)
+        for i in range(20):
+            call(i)
+        torch.cuda.synchronize()
+        iters = 500
+        e0.record(stream)
+        for i in range(iters):
+            call(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / iters
+        out[name] = {"GB_per_s": nbytes / (us * 1e-6) / 1e9, "us_per_call": us,
+                     "rows_per_s": rows / (us * 1e-6), "bytes_per_call": nbytes,
+                     "geometry": mrn.mrn_query_geometry(op, rows, n, mrn.MRN_BF16, True)}
+    del sets, outs
+    torch.cuda.empty_cache()
+
+    w = wl.plain_decode_rows()
+    nsets = 512
+    x = torch.from_numpy(w.arrays["x"]).to(dev).repeat(nsets, 1).view(nsets, w.rows, w.n)
+    g = torch.from_numpy(w.arrays["gamma"]).to(dev)
+    y = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        for i in range(nsets):
+            mrn.mrn_rmsnorm(x[i].data_ptr(), g.data_ptr(), y[i].data_ptr(), w.rows, w.n, w.eps,
+                            mrn.MRN_F32, side.cuda_stream)
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(nsets):
+                st = mrn.mrn_rmsnorm(x[i].data_ptr(), g.data_ptr(), y[i].data_ptr(), w.rows, w.n,
+                                     w.eps, mrn.MRN_F32, side.cuda_stream)
+                if st != 0:
+                    raise mrn.MrnError(st, w.name)
+    stream.wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    reps = 4
+    e0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * nsets)
+    out[w.name] = {"us_per_call_graph": us, "bytes_per_call": (2 * w.rows * w.n + w.n) * 4,
+                   "geometry": mrn.mrn_query_geometry(0, w.rows, w.n, mrn.MRN_F32, True)}
+    return out
 
 
 def main(argv=None):
