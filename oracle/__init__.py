@@ -11,7 +11,8 @@ sums, compiled without fast-math or FMA contraction).  This module compiles it
 with the host C compiler and marshals numpy arrays through ctypes.  Every
 function cites the passage it follows in ``oracle.c`` / ``oracle.h``:
 "Chapter 12 -- RMSNorm and the dual-epsilon sandwich" (sections 12.1, 12.3,
-12.4.3, 12.4.4) and the Hesper "RMSNorm Layer" API page (rmsNormThenAddKernel).
+12.4.3, 12.4.4) and the Hesper "RMSNorm Layer" API page (rmsNormThenAddKernel,
+rmsNormThenAddThenBroadcastScaleKernel, residualAddRmsNormKernel).
 
 ctypes releases the GIL during a foreign call, so callers may run disjoint row
 blocks on several threads (the oracle itself stays single-threaded code).
@@ -84,6 +85,12 @@ class Oracle:
                                                   _i64, _i64, ctypes.c_double,
                                                   ctypes.c_double, ctypes.c_int]
         lib.oracle_norm_residual_norm.restype = None
+        lib.oracle_add_rmsnorm.argtypes = [_f64p, _f64p, _f64p, _f64p, _f64p, _i64, _i64,
+                                           ctypes.c_double, ctypes.c_int]
+        lib.oracle_add_rmsnorm.restype = None
+        lib.oracle_rmsnorm_then_add_scale.argtypes = [_f64p, _f64p, _f64p, ctypes.c_double,
+                                                      _f64p, _i64, _i64, ctypes.c_double]
+        lib.oracle_rmsnorm_then_add_scale.restype = None
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
         lib.oracle_bf16_from_double.restype = ctypes.c_uint16
         lib.oracle_double_from_bf16.argtypes = [ctypes.c_uint16]
@@ -139,6 +146,32 @@ class Oracle:
                                            float(eps_pre), 1 if stream_bf16 else 0)
         return s.reshape(b.shape), o.reshape(b.shape)
 
+    def add_rmsnorm(self, a, b, gamma, eps: float, sum_bf16: bool = False):
+        """(a + b, RMSNorm(a + b) * gamma) per row (Hesper residualAddRmsNormKernel)."""
+        a = _as_f64(a)
+        b = _as_f64(b)
+        g = _as_f64(gamma)
+        rows, n = _shape2(a)
+        assert b.size == a.size and g.shape == (n,)
+        s = np.empty((rows, n), dtype=np.float64)
+        o = np.empty((rows, n), dtype=np.float64)
+        self.lib.oracle_add_rmsnorm(_ptr(a), _ptr(b), _ptr(g), _ptr(s), _ptr(o), rows, n,
+                                    float(eps), 1 if sum_bf16 else 0)
+        return s.reshape(a.shape), o.reshape(a.shape)
+
+    def rmsnorm_then_add_scale(self, x, gamma, residual, out_scale: float, eps: float):
+        """(RMSNorm(x) * gamma + residual) * out_scale per row
+        (Hesper rmsNormThenAddThenBroadcastScaleKernel)."""
+        x = _as_f64(x)
+        g = _as_f64(gamma)
+        r = _as_f64(residual)
+        rows, n = _shape2(x)
+        assert g.shape == (n,) and r.size == x.size
+        out = np.empty((rows, n), dtype=np.float64)
+        self.lib.oracle_rmsnorm_then_add_scale(_ptr(x), _ptr(g), _ptr(r), float(out_scale),
+                                               _ptr(out), rows, n, float(eps))
+        return out.reshape(x.shape)
+
     # -- bf16 conversions -----------------------------------------------------
     def bf16_from_double(self, v) -> np.ndarray:
         """Round to nearest bf16, ties to even; returns uint16 bit patterns."""
@@ -182,6 +215,14 @@ def norm_residual_norm(block_out, residual, gamma_post, gamma_pre, eps_post, eps
                        stream_bf16=False):
     return default().norm_residual_norm(block_out, residual, gamma_post, gamma_pre,
                                         eps_post, eps_pre, stream_bf16)
+
+
+def add_rmsnorm(a, b, gamma, eps, sum_bf16=False):
+    return default().add_rmsnorm(a, b, gamma, eps, sum_bf16)
+
+
+def rmsnorm_then_add_scale(x, gamma, residual, out_scale, eps):
+    return default().rmsnorm_then_add_scale(x, gamma, residual, out_scale, eps)
 
 
 def bf16_from_double(v):

@@ -79,6 +79,43 @@ void oracle_norm_residual_norm(const double *block_out, const double *residual,
     }
 }
 
+void oracle_add_rmsnorm(const double *a, const double *b, const double *gamma,
+                        double *residual_out, double *normed,
+                        int64_t rows, int64_t n, double eps, int sum_bf16)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *ar = a + r * n;
+        const double *br = b + r * n;
+        double *sr = residual_out + r * n;
+        double *nr = normed + r * n;
+
+        /* residual add; the stored sum is what the norm reads */
+        for (int64_t j = 0; j < n; ++j) {
+            double s = ar[j] + br[j];
+            if (sum_bf16)
+                s = oracle_double_from_bf16(oracle_bf16_from_double(s));
+            sr[j] = s;
+        }
+        double inv_rms = row_inv_rms(sr, n, eps);
+        for (int64_t j = 0; j < n; ++j)
+            nr[j] = sr[j] * inv_rms * gamma[j];
+    }
+}
+
+void oracle_rmsnorm_then_add_scale(const double *x, const double *gamma,
+                                   const double *residual, double out_scale, double *out,
+                                   int64_t rows, int64_t n, double eps)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * n;
+        const double *rr = residual + r * n;
+        double *outr = out + r * n;
+        double inv_rms = row_inv_rms(xr, n, eps);
+        for (int64_t j = 0; j < n; ++j)
+            outr[j] = (xr[j] * inv_rms * gamma[j] + rr[j]) * out_scale;
+    }
+}
+
 /*
  * bf16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits.  Normal
  * numbers are (1 + f/128) * 2^(e-127) for e in 1..254; e = 0 holds the

@@ -14,7 +14,10 @@
  *        12.4.4 (the split route's f32 publication boundary between the norms).
  *   [P4] "RMSNorm Layer - Root Mean Square Normalization" (Hesper API docs),
  *        rmsNormThenAddKernel / rmsNormThenAddBatchKernel:
- *        output = RMSNorm(layer_out) * scale + residual.
+ *        output = RMSNorm(layer_out) * scale + residual;
+ *        rmsNormThenAddThenBroadcastScaleKernel: the same times out_scale[0];
+ *        residualAddRmsNormKernel: residualOut = a + b,
+ *        output = RMSNorm(residualOut) * scale.
  *
  * Layout: every row operand is a contiguous row-major [rows x n] array of
  * double, row r at base + r*n; gamma is [n] and shared by all rows.  Inputs
@@ -57,6 +60,25 @@ void oracle_norm_residual_norm(const double *block_out, const double *residual,
                                double *out_stream, double *normed,
                                int64_t rows, int64_t n,
                                double eps_post, double eps_pre, int stream_bf16);
+
+/*
+ * Residual add, then RMSNorm of the sum            [P4 residualAddRmsNormKernel]
+ *   residual_out = a + b
+ *   normed       = RMSNorm(residual_out; eps) * gamma
+ * With sum_bf16 non-zero the sum is rounded to bf16 before it is stored and
+ * normed, as the sandwich's stream is.
+ */
+void oracle_add_rmsnorm(const double *a, const double *b, const double *gamma,
+                        double *residual_out, double *normed,
+                        int64_t rows, int64_t n, double eps, int sum_bf16);
+
+/*
+ * Post norm, residual add, then a broadcast scalar   [P4 rmsNormThenAddThenBroadcastScaleKernel]
+ *   out = (RMSNorm(x; eps) * gamma + residual) * out_scale
+ */
+void oracle_rmsnorm_then_add_scale(const double *x, const double *gamma,
+                                   const double *residual, double out_scale, double *out,
+                                   int64_t rows, int64_t n, double eps);
 
 /* Round a double to the nearest bf16 (ties to even); returns the bit pattern. */
 uint16_t oracle_bf16_from_double(double v);

@@ -338,6 +338,54 @@ def check_sandwich_degenerate(orc):
     _assert_rel(o, _torch_rms(r, gq, 1e-5), 1e-12, "normed of the bare residual")
 
 
+def check_add_rmsnorm(orc):
+    """Residual add then norm (Hesper residualAddRmsNormKernel): against torch in
+    float64, symmetric in its two inputs, b = 0 gives RMSNorm(a), constant rows
+    in closed form, and the bf16 sum is the rounded sum re-normed."""
+    g = _rng(26)
+    rows, n = 5, 1000
+    a = g.standard_normal((rows, n)) * 10.0 ** g.uniform(-2, 2, size=(rows, 1))
+    b = g.standard_normal((rows, n))
+    gamma = 1.0 + 0.1 * g.standard_normal(n)
+    s, o = orc.add_rmsnorm(a, b, gamma, 1e-5)
+    assert np.array_equal(s, a + b), "residual_out is the plain sum"
+    _assert_rel(o, _torch_rms(a + b, gamma, 1e-5), 1e-12, "add+norm vs torch", floor=1e-300)
+    s2, o2 = orc.add_rmsnorm(b, a, gamma, 1e-5)
+    assert np.array_equal(s2, s) and np.array_equal(o2, o), "symmetric in a and b"
+    s3, o3 = orc.add_rmsnorm(a, np.zeros_like(a), gamma, 1e-5)
+    assert np.array_equal(s3, a)
+    _assert_rel(o3, _torch_rms(a, gamma, 1e-5), 1e-12, "b = 0", floor=1e-300)
+    for c, d in ((1.5, -0.25), (1e-4, 2e-4)):
+        sc, oc = orc.add_rmsnorm(np.full((2, 7), c), np.full((2, 7), d), gamma[:7], 1e-8)
+        _assert_rel(oc, np.broadcast_to((c + d) / np.sqrt((c + d) ** 2 + 1e-8) * gamma[:7],
+                                        oc.shape), 1e-13, f"constant rows {c}+{d}")
+    sb, ob = orc.add_rmsnorm(a, b, gamma, 1e-5, sum_bf16=True)
+    tb = _torch_bf16_bits((a + b).astype(np.float32))
+    exact32 = (a + b).astype(np.float32).astype(np.float64) == a + b
+    bits = orc.bf16_from_double(sb)
+    assert np.array_equal(orc.double_from_bf16(bits), sb), "bf16 sum is representable"
+    assert np.array_equal(bits[exact32], tb[exact32]), "bf16 sum is the rounded sum"
+    _assert_rel(ob, _torch_rms(sb, gamma, 1e-5), 1e-12, "bf16 sum re-normed", floor=1e-300)
+
+
+def check_then_add_scale(orc):
+    """(RMSNorm(x) gamma + r) * s (Hesper rmsNormThenAddThenBroadcastScaleKernel):
+    against torch, s = 1 is the then-add, s = 0 gives zeros, a power of two
+    scales exactly."""
+    g = _rng(27)
+    rows, n = 4, 777
+    x = g.standard_normal((rows, n)) * 3.0
+    r = g.standard_normal((rows, n))
+    gamma = 1.0 + 0.1 * g.standard_normal(n)
+    base = orc.rmsnorm_then_add(x, gamma, r, 1e-6)
+    assert np.array_equal(orc.rmsnorm_then_add_scale(x, gamma, r, 1.0, 1e-6), base)
+    assert np.array_equal(orc.rmsnorm_then_add_scale(x, gamma, r, -2.0, 1e-6), -2.0 * base)
+    assert np.all(orc.rmsnorm_then_add_scale(x, gamma, r, 0.0, 1e-6) == 0.0)
+    p = _torch_rms(x, gamma, 1e-6)
+    got = orc.rmsnorm_then_add_scale(x, gamma, r, 0.37, 1e-6)
+    _assert_close(got, (p + r) * 0.37, 1e-12 * 0.37 * (np.abs(p) + np.abs(r)), "vs torch")
+
+
 # ---------------------------------------------------------------------------
 # bf16 conversions
 # ---------------------------------------------------------------------------
@@ -418,6 +466,8 @@ ALL_CHECKS = [
     check_sandwich_epsilon_routing,
     check_sandwich_closed_form,
     check_sandwich_degenerate,
+    check_add_rmsnorm,
+    check_then_add_scale,
     check_bf16_widen_all_patterns,
     check_bf16_round_against_torch,
     check_bf16_sandwich_stream,

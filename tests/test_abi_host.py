@@ -199,6 +199,14 @@ def test_force_geometry_validation():
     assert mrn.mrn_query_geometry(2, 1, 6656, mrn.MRN_F32, True, 152)["kind"] == 2
 
 
+def test_launch_options():
+    assert mrn.mrn_launch_options() == 0
+    assert mrn.mrn_set_launch_options(2) == mrn.MRN_ERR_INVALID_GEOMETRY
+    assert mrn.mrn_set_launch_options(mrn.MRN_LAUNCH_PDL) == 0
+    assert mrn.mrn_launch_options() == mrn.MRN_LAUNCH_PDL
+    assert mrn.mrn_set_launch_options(0) == 0 and mrn.mrn_launch_options() == 0
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path):
     code = ("import dual_epsilon_sandwich_gb300.mrn as m; m.LIBRARY = '/nonexistent/libmrn.so'\n"
             "try:\n    m.mrn_status_string(0)\nexcept RuntimeError as e:\n"

@@ -316,3 +316,29 @@ def test_staged_kernel_is_the_automatic_choice_for_batches():
     d = rows_data(14, 2048, 6656, "f32")
     all_ops(d, "f32", "auto staged 2048x6656")
     assert mrn.mrn_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("rows,n", [(1, 6656), (4, 6656), (2048, 6656), (300, 768), (64, 200000)])
+def test_programmatic_launch_chain_matches(rows, n):
+    """A chain of dependent sandwich calls (each call's normed is the next
+    call's block_out, its stream the next residual, updated in place) gives the
+    same bits with programmatic dependent launch as without."""
+    d = rows_data(15 + n, rows, n, "f32")
+    g1, g2 = gu.to_device(d["gamma"], "f32"), gu.to_device(d["gamma2"], "f32")
+
+    def chain(options):
+        assert mrn.mrn_set_launch_options(options) == 0
+        b = gu.to_device(d["x"], "f32")
+        r = gu.to_device(d["residual"], "f32")
+        o = torch.empty_like(b)
+        for _ in range(6):
+            assert gu.call_sandwich(b, r, g1, g2, r, o, rows, n, 1e-8, 1e-5, "f32") == 0
+            b, o = o, b
+        torch.cuda.synchronize()
+        assert mrn.mrn_set_launch_options(0) == 0
+        return b, r
+
+    b0, r0 = chain(0)
+    b1, r1 = chain(mrn.MRN_LAUNCH_PDL)
+    assert torch.equal(b0, b1) and torch.equal(r0, r1)
+    assert mrn.mrn_wait_timeouts() == 0

@@ -44,6 +44,15 @@ MUTANTS = [
     ("sandwich residual row offset lost", "const double *rr = residual + r * n;\n        double *sr",
      "const double *rr = residual;\n        double *sr"),
     ("bf16 stream rounding skipped", "if (stream_bf16)", "if (0)"),
+    ("add-norm: b dropped", "double s = ar[j] + br[j];", "double s = ar[j];"),
+    ("add-norm: b subtracted", "double s = ar[j] + br[j];", "double s = ar[j] - br[j];"),
+    ("add-norm: norm of a, not the sum", "double inv_rms = row_inv_rms(sr, n, eps);\n        for (int64_t j = 0; j < n; ++j)\n            nr[j]",
+     "double inv_rms = row_inv_rms(ar, n, eps);\n        for (int64_t j = 0; j < n; ++j)\n            nr[j]"),
+    ("add-norm: bf16 sum rounding skipped", "if (sum_bf16)", "if (0)"),
+    ("add-norm: normed from a", "nr[j] = sr[j] * inv_rms * gamma[j];", "nr[j] = ar[j] * inv_rms * gamma[j];"),
+    ("then-add-scale: scale dropped", "+ rr[j]) * out_scale;", "+ rr[j]);"),
+    ("then-add-scale: scale on the norm only", "outr[j] = (xr[j] * inv_rms * gamma[j] + rr[j]) * out_scale;",
+     "outr[j] = xr[j] * inv_rms * gamma[j] * out_scale + rr[j];"),
     ("bf16 ties away from zero", "(frac == 0.5 && (q & 1u))", "(frac == 0.5)"),
     ("bf16 truncation", "if (frac > 0.5 || (frac == 0.5 && (q & 1u)))", "if (0)"),
     ("bf16 subnormal quantum", "(lead < -126) ? -133 : lead - 7", "(lead < -126) ? -134 : lead - 7"),
