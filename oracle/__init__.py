@@ -12,7 +12,8 @@ with the host C compiler and marshals numpy arrays through ctypes.  Every
 function cites the passage it follows in ``oracle.c`` / ``oracle.h``:
 "Chapter 12 -- RMSNorm and the dual-epsilon sandwich" (sections 12.1, 12.3,
 12.4.3, 12.4.4) and the Hesper "RMSNorm Layer" API page (rmsNormThenAddKernel,
-rmsNormThenAddThenBroadcastScaleKernel, residualAddRmsNormKernel).
+rmsNormThenAddThenBroadcastScaleKernel, residualAddRmsNormKernel,
+fusedRMSNormQ8_1Kernel).
 
 ctypes releases the GIL during a foreign call, so callers may run disjoint row
 blocks on several threads (the oracle itself stays single-threaded code).
@@ -91,6 +92,15 @@ class Oracle:
         lib.oracle_rmsnorm_then_add_scale.argtypes = [_f64p, _f64p, _f64p, ctypes.c_double,
                                                       _f64p, _i64, _i64, ctypes.c_double]
         lib.oracle_rmsnorm_then_add_scale.restype = None
+        lib.oracle_rmsnorm_q8_1.argtypes = [_f64p, _f64p, _i64, _i64, ctypes.c_double, _f64p,
+                                            _f64p, ctypes.POINTER(ctypes.c_int8)]
+        lib.oracle_rmsnorm_q8_1.restype = None
+        lib.oracle_q8_round.argtypes = [ctypes.c_double]
+        lib.oracle_q8_round.restype = ctypes.c_int
+        lib.oracle_f16_from_double.argtypes = [ctypes.c_double]
+        lib.oracle_f16_from_double.restype = ctypes.c_uint16
+        lib.oracle_double_from_f16.argtypes = [ctypes.c_uint16]
+        lib.oracle_double_from_f16.restype = ctypes.c_double
         lib.oracle_bf16_from_double.argtypes = [ctypes.c_double]
         lib.oracle_bf16_from_double.restype = ctypes.c_uint16
         lib.oracle_double_from_bf16.argtypes = [ctypes.c_uint16]
@@ -172,6 +182,33 @@ class Oracle:
                                                _ptr(out), rows, n, float(eps))
         return out.reshape(x.shape)
 
+    def rmsnorm_q8_1(self, x, gamma, eps: float):
+        """RMSNorm then Q8_1 block quantisation (Hesper fusedRMSNormQ8_1Kernel).
+        Returns (d [rows x n/32], qreal [rows x n], q [rows x n] int8)."""
+        x = _as_f64(x)
+        g = _as_f64(gamma)
+        rows, n = _shape2(x)
+        assert g.shape == (n,) and n % 32 == 0
+        d = np.empty((rows, n // 32), dtype=np.float64)
+        qreal = np.empty((rows, n), dtype=np.float64)
+        q = np.empty((rows, n), dtype=np.int8)
+        self.lib.oracle_rmsnorm_q8_1(_ptr(x), _ptr(g), rows, n, float(eps), _ptr(d),
+                                     _ptr(qreal), q.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)))
+        return d, qreal, q
+
+    def q8_round(self, qreal: float) -> int:
+        return self.lib.oracle_q8_round(float(qreal))
+
+    def f16_from_double(self, v) -> np.ndarray:
+        v = _as_f64(v)
+        return np.array([self.lib.oracle_f16_from_double(float(t)) for t in v.ravel()],
+                        dtype=np.uint16).reshape(v.shape)
+
+    def double_from_f16(self, bits) -> np.ndarray:
+        b = np.asarray(bits, dtype=np.uint16)
+        return np.array([self.lib.oracle_double_from_f16(int(t)) for t in b.ravel()],
+                        dtype=np.float64).reshape(b.shape)
+
     # -- bf16 conversions -----------------------------------------------------
     def bf16_from_double(self, v) -> np.ndarray:
         """Round to nearest bf16, ties to even; returns uint16 bit patterns."""
@@ -223,6 +260,18 @@ def add_rmsnorm(a, b, gamma, eps, sum_bf16=False):
 
 def rmsnorm_then_add_scale(x, gamma, residual, out_scale, eps):
     return default().rmsnorm_then_add_scale(x, gamma, residual, out_scale, eps)
+
+
+def rmsnorm_q8_1(x, gamma, eps):
+    return default().rmsnorm_q8_1(x, gamma, eps)
+
+
+def f16_from_double(v):
+    return default().f16_from_double(v)
+
+
+def double_from_f16(bits):
+    return default().double_from_f16(bits)
 
 
 def bf16_from_double(v):

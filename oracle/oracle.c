@@ -116,6 +116,93 @@ void oracle_rmsnorm_then_add_scale(const double *x, const double *gamma,
     }
 }
 
+int oracle_q8_round(double qreal)
+{
+    double r = nearbyint(qreal);          /* default rounding: nearest, ties to even */
+    if (r > 127.0)
+        r = 127.0;
+    if (r < -128.0)
+        r = -128.0;
+    return (int)r;
+}
+
+void oracle_rmsnorm_q8_1(const double *x, const double *gamma, int64_t rows, int64_t n,
+                         double eps, double *d, double *qreal, int8_t *q)
+{
+    const int64_t blocks = n / 32;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * n;
+        double inv_rms = row_inv_rms(xr, n, eps);
+        for (int64_t b = 0; b < blocks; ++b) {
+            double normed[32];
+            double amax = 0.0;
+            for (int l = 0; l < 32; ++l) {
+                int64_t j = b * 32 + l;
+                normed[l] = xr[j] * gamma[j] * inv_rms;
+                if (fabs(normed[l]) > amax)
+                    amax = fabs(normed[l]);
+            }
+            double scale = amax / 127.0;
+            d[r * blocks + b] = scale;
+            for (int l = 0; l < 32; ++l) {
+                int64_t j = r * n + b * 32 + l;
+                qreal[j] = (scale == 0.0) ? 0.0 : normed[l] / scale;
+                q[j] = (int8_t)oracle_q8_round(qreal[j]);
+            }
+        }
+    }
+}
+
+/*
+ * binary16: normal numbers (1 + f/1024) * 2^(e-15), e in 1..30; subnormals
+ * f * 2^-24; e = 31 holds infinities and NaNs.  Same rounding rule as bf16.
+ */
+uint16_t oracle_f16_from_double(double v)
+{
+    if (isnan(v))
+        return (uint16_t)0x7E00u;
+    uint16_t sign = signbit(v) ? (uint16_t)0x8000u : (uint16_t)0;
+    double a = fabs(v);
+    if (isinf(a))
+        return (uint16_t)(sign | 0x7C00u);
+    if (a == 0.0)
+        return sign;
+    int e2;
+    (void)frexp(a, &e2);
+    int lead = e2 - 1;
+    int quantum = (lead < -14) ? -24 : lead - 10;
+    double scaled = ldexp(a, -quantum);
+    double whole = floor(scaled);
+    double frac = scaled - whole;
+    uint64_t q = (uint64_t)whole;
+    if (frac > 0.5 || (frac == 0.5 && (q & 1u)))
+        q += 1;
+    if (lead < -14)
+        return (uint16_t)(sign | (uint16_t)q);     /* q == 1024 is the smallest normal */
+    if (q == 2048) {
+        q = 1024;
+        lead += 1;
+    }
+    if (lead > 15)
+        return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | (uint16_t)(((lead + 15) << 10) | (int)(q - 1024)));
+}
+
+double oracle_double_from_f16(uint16_t bits)
+{
+    int sign = (bits >> 15) & 1;
+    int field = (bits >> 10) & 0x1F;
+    int frac = bits & 0x3FF;
+    double v;
+    if (field == 0x1F)
+        v = frac ? NAN : INFINITY;
+    else if (field == 0)
+        v = ldexp((double)frac, -24);
+    else
+        v = ldexp((double)(1024 + frac), field - 15 - 10);
+    return sign ? -v : v;
+}
+
 /*
  * bf16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits.  Normal
  * numbers are (1 + f/128) * 2^(e-127) for e in 1..254; e = 0 holds the

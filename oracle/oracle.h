@@ -17,7 +17,9 @@
  *        output = RMSNorm(layer_out) * scale + residual;
  *        rmsNormThenAddThenBroadcastScaleKernel: the same times out_scale[0];
  *        residualAddRmsNormKernel: residualOut = a + b,
- *        output = RMSNorm(residualOut) * scale.
+ *        output = RMSNorm(residualOut) * scale;
+ *        fusedRMSNormQ8_1Kernel: the norm followed by per-32-block
+ *        d = amax/127, q = round(x/d), s = 0.
  *
  * Layout: every row operand is a contiguous row-major [rows x n] array of
  * double, row r at base + r*n; gamma is [n] and shared by all rows.  Inputs
@@ -79,6 +81,26 @@ void oracle_add_rmsnorm(const double *a, const double *b, const double *gamma,
 void oracle_rmsnorm_then_add_scale(const double *x, const double *gamma,
                                    const double *residual, double out_scale, double *out,
                                    int64_t rows, int64_t n, double eps);
+
+/*
+ * RMSNorm fused with Q8_1 block quantisation      [P4 fusedRMSNormQ8_1Kernel]
+ *   x_normed_j = x_j * gamma_j * inv_rms            (the page's product order)
+ *   per block of 32 elements: amax = max |x_normed|, d = amax / 127,
+ *   qreal_j = x_normed_j / d   (0 for every element when d == 0),
+ *   q_j = qreal_j rounded half to even, clamped to [-128, 127]
+ * n must be a multiple of 32.  Outputs: d [rows x n/32], qreal [rows x n]
+ * (the value before rounding, so a test can see how close a code is to a
+ * rounding boundary) and q [rows x n].
+ */
+void oracle_rmsnorm_q8_1(const double *x, const double *gamma, int64_t rows, int64_t n,
+                         double eps, double *d, double *qreal, int8_t *q);
+/* The code of one quotient: nearest integer, ties to even, clamped to int8. */
+int oracle_q8_round(double qreal);
+
+/* IEEE binary16 (1 sign, 5 exponent, 10 fraction bits): round a double to the
+ * nearest (ties to even), and widen a pattern exactly. */
+uint16_t oracle_f16_from_double(double v);
+double oracle_double_from_f16(uint16_t bits);
 
 /* Round a double to the nearest bf16 (ties to even); returns the bit pattern. */
 uint16_t oracle_bf16_from_double(double v);

@@ -288,6 +288,74 @@ def parity_sandwich(b, res, gp, gq, eps_post, eps_pre, dtype, rows_sample=None,
     return es, eo
 
 
+def call_add_rmsnorm(a, b, g, s, o, rows, n, eps, dtype):
+    return mrn.mrn_add_rmsnorm(a.data_ptr(), b.data_ptr(), g.data_ptr(), _p(s), _p(o), rows, n,
+                               eps, code(dtype), stream_handle())
+
+
+def call_then_add_scale(x, g, r, sc, out, rows, n, eps, dtype):
+    return mrn.mrn_rmsnorm_then_add_scale(x.data_ptr(), g.data_ptr(), r.data_ptr(),
+                                          sc.data_ptr(), _p(out), rows, n, eps, code(dtype),
+                                          stream_handle())
+
+
+def parity_add_rmsnorm(a, b, gamma, eps, dtype, rows_sample=None, what="add_rmsnorm",
+                       inplace=None):
+    """inplace: None, "a" or "b" (residual_out == that input)."""
+    rows, n = a.shape
+    da, db, dg = to_device(a, dtype), to_device(b, dtype), to_device(gamma, dtype)
+    o = Guarded(rows, n, dtype)
+    s_t = {"a": da, "b": db}.get(inplace) if inplace else Guarded(rows, n, dtype)
+    st = call_add_rmsnorm(da, db, dg, s_t, o, rows, n, eps, dtype)
+    assert st == 0, f"{what}: status {mrn.STATUS.get(st)}"
+    torch.cuda.synchronize()
+    o.check(what + " normed")
+    if isinstance(s_t, Guarded):
+        s_t.check(what + " residual_out")
+        got_s = s_t.host()
+    else:
+        got_s = to_host(s_t, dtype)
+    got_o = o.host()
+    sel = slice(None) if rows_sample is None else rows_sample
+    as_, bs, gs = widen(a[sel], dtype), widen(b[sel], dtype), widen(gamma, dtype)
+    e = float(np.float32(eps))
+    if dtype == "f32":
+        want_s, want_o = oracle.add_rmsnorm(as_, bs, gs, e)
+        # the f32 sum of two f32 values is correctly rounded: bit-exact
+        assert np.array_equal(got_s[sel], want_s.astype(np.float32)), what + " residual_out"
+        return check_f32_norm(got_o[sel], want_o, what + " normed")
+    raw_s, _ = oracle.add_rmsnorm(as_, bs, gs, e, sum_bf16=False)
+    want_s, want_o = oracle.add_rmsnorm(as_, bs, gs, e, sum_bf16=True)
+    check_bf16(got_s[sel], raw_s, np.abs(as_) + np.abs(bs), what + " residual_out")
+    carried = sandwich_normed_scale(want_s, bf16_ulp(raw_s), gs, e)
+    return check_bf16(got_o[sel], want_o, np.abs(want_o) + carried / F32_TOL, what + " normed")
+
+
+def parity_then_add_scale(x, gamma, res, scale, eps, dtype, rows_sample=None,
+                          what="then_add_scale"):
+    rows, n = x.shape
+    dx, dg, dr = to_device(x, dtype), to_device(gamma, dtype), to_device(res, dtype)
+    sc_host = np.array([scale], dtype=np.float32)
+    if dtype == "bf16":
+        sc_host = oracle.bf16_from_double(sc_host.astype(np.float64))
+    dsc = to_device(sc_host, dtype)
+    out = Guarded(rows, n, dtype)
+    st = call_then_add_scale(dx, dg, dr, dsc, out, rows, n, eps, dtype)
+    assert st == 0, f"{what}: status {mrn.STATUS.get(st)}"
+    torch.cuda.synchronize()
+    out.check(what)
+    got = out.host()
+    sel = slice(None) if rows_sample is None else rows_sample
+    xs, gs, rs = widen(x[sel], dtype), widen(gamma, dtype), widen(res[sel], dtype)
+    s64 = float(widen(sc_host, dtype)[0])
+    e = float(np.float32(eps))
+    want = oracle.rmsnorm_then_add_scale(xs, gs, rs, s64, e)
+    scale_t = (np.abs(oracle.rmsnorm(xs, gs, e)) + np.abs(rs)) * abs(s64)
+    if dtype == "f32":
+        return check_f32_sum(got[sel], want, scale_t, what)
+    return check_bf16(got[sel], want, scale_t, what)
+
+
 def sample_rows(rows, count, seed, must=()):
     g = np.random.Generator(np.random.PCG64(seed))
     pick = set(int(v) for v in g.choice(rows, size=min(rows, count), replace=False))

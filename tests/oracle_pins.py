@@ -54,8 +54,9 @@ def _assert_close(got, want, tol, what):
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     err = np.abs(got - want)
-    bad = err > tol
-    assert not np.any(bad), (f"{what}: max err {err.max():.3e} > tol; "
+    bad = ~(err <= tol)                    # a NaN anywhere fails
+    assert not np.any(bad), (f"{what}: max err {np.nanmax(err):.3e} > tol, "
+                             f"{int(np.isnan(err).sum())} NaN; "
                              f"got {got[bad][:4]} want {want[bad][:4]}")
 
 
@@ -386,6 +387,62 @@ def check_then_add_scale(orc):
     _assert_close(got, (p + r) * 0.37, 1e-12 * 0.37 * (np.abs(p) + np.abs(r)), "vs torch")
 
 
+def check_q8_round(orc):
+    """WGSL round(): nearest integer, ties to even; clamped to int8."""
+    cases = {2.5: 2, 3.5: 4, -2.5: -2, -3.5: -4, 0.5: 0, 1.5: 2, 0.49999: 0, -0.51: -1,
+             126.5: 126, 127.4: 127, 127.6: 127, 200.0: 127, -127.5: -128, -128.4: -128,
+             -128.6: -128, -300.0: -128}
+    for v, want in cases.items():
+        assert orc.q8_round(v) == want, (v, orc.q8_round(v), want)
+
+
+def check_rmsnorm_q8_1(orc):
+    """RMSNorm + Q8_1 (Hesper fusedRMSNormQ8_1Kernel): d = amax/127 of the torch
+    float64 norm per 32-block, q = nearest of x_normed/d, each non-zero block
+    reaches |q| = 127 at its amax, dequantisation within d/2, zero blocks give
+    d = q = 0."""
+    g = _rng(28)
+    rows, n = 6, 2560                     # D = 2560 is the page's example width
+    x = g.standard_normal((rows, n)) * 10.0 ** g.uniform(-2, 2, size=(rows, 1))
+    x[2, 64:96] = 0.0                     # one all-zero block
+    gamma = 1.0 + 0.1 * g.standard_normal(n)
+    d, qreal, q = orc.rmsnorm_q8_1(x, gamma, 1e-6)
+    xn = _torch_rms(x, gamma, 1e-6)
+    amax = np.abs(xn).reshape(rows, n // 32, 32).max(axis=2)
+    _assert_rel(d, amax / 127.0, 1e-13, "d = amax / 127")
+    assert d[2, 2] == 0.0 and np.all(q[2, 64:96] == 0), "zero block"
+    blocks = np.abs(q.astype(np.int64)).reshape(rows, n // 32, 32).max(axis=2)
+    assert np.all((blocks == 127) | (amax == 0)), "every non-zero block reaches 127"
+    dd = np.repeat(d, 32, axis=1)
+    nz = dd > 0
+    ref = np.where(nz, xn / np.where(nz, dd, 1.0), 0.0)
+    _assert_close(qreal, ref, 1e-12 * (1 + np.abs(ref)), "x_normed / d")
+    margin = np.abs(np.abs(ref - np.floor(ref)) - 0.5)
+    safe = margin > 1e-9
+    assert np.array_equal(q[safe], np.clip(np.rint(ref[safe]), -128, 127).astype(np.int8)), \
+        "q = nearest integer of x_normed / d"
+    _assert_close(q * dd, xn, 0.5 * dd * (1 + 1e-9) + 1e-300, "dequantisation within d/2")
+
+
+def check_f16_conversions(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    sample = bits[::37]
+    got = orc.double_from_f16(sample)
+    want = sample.view(np.float16).astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan])
+    g = _rng(29)
+    v = np.concatenate([g.standard_normal(3000) * 10.0 ** g.uniform(-9, 5, 3000),
+                        [65504.0, 65519.9, 65520.0, 2.0 ** -24, 3 * 2.0 ** -25, 2.0 ** -25,
+                         0.0, -0.0, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11,
+                         # rounding that carries into the next binade, odd and even fields
+                         2047.5, -2047.75, 4095.5, 1.0 - 2.0 ** -12, 0.5 - 2.0 ** -13,
+                         2.0 ** -14 - 2.0 ** -26]])
+    with np.errstate(over="ignore"):
+        ref = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(orc.f16_from_double(v), ref), "f16 rounding vs numpy"
+
+
 # ---------------------------------------------------------------------------
 # bf16 conversions
 # ---------------------------------------------------------------------------
@@ -468,6 +525,9 @@ ALL_CHECKS = [
     check_sandwich_degenerate,
     check_add_rmsnorm,
     check_then_add_scale,
+    check_q8_round,
+    check_rmsnorm_q8_1,
+    check_f16_conversions,
     check_bf16_widen_all_patterns,
     check_bf16_round_against_torch,
     check_bf16_sandwich_stream,

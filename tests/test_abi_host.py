@@ -66,6 +66,32 @@ def sand(b=A, r=B, gp=G, gq=H, s=Y, o=Z, rows=4, n=64, e1=1e-8, e2=1e-5, dt=mrn.
     return mrn.mrn_norm_residual_norm(b, r, gp, gq, s, o, rows, n, e1, e2, dt, 0)
 
 
+def addn(a=A, b=B, g=G, s=Y, o=Z, rows=4, n=64, eps=1e-5, dt=mrn.MRN_F32):
+    return mrn.mrn_add_rmsnorm(a, b, g, s, o, rows, n, eps, dt, 0)
+
+
+def tscale(x=A, g=G, r=B, sc=H, o=Y, rows=4, n=64, eps=1e-5, dt=mrn.MRN_F32):
+    return mrn.mrn_rmsnorm_then_add_scale(x, g, r, sc, o, rows, n, eps, dt, 0)
+
+
+def test_more_ops_validation():
+    assert addn(n=0) == mrn.MRN_ERR_INVALID_SIZE
+    assert tscale(eps=0.0) == mrn.MRN_ERR_INVALID_EPS
+    assert addn(dt=5) == mrn.MRN_ERR_UNSUPPORTED_DTYPE
+    assert addn(a=None, b=None, g=None, s=None, o=None, rows=0) == mrn.MRN_OK
+    for kw in ("a", "b", "g", "s", "o"):
+        assert addn(**{kw: None}) == mrn.MRN_ERR_NULL_POINTER, kw
+    for kw in ("x", "g", "r", "sc", "o"):
+        assert tscale(**{kw: None}) == mrn.MRN_ERR_NULL_POINTER, kw
+    assert tscale(sc=H + 2) == mrn.MRN_ERR_MISALIGNED
+    assert addn(o=Y) == mrn.MRN_ERR_ALIASING                 # normed == residual_out
+    assert addn(s=A + 8) == mrn.MRN_ERR_ALIASING             # partial over a
+    assert addn(o=G) == mrn.MRN_ERR_ALIASING                 # normed over gamma
+    assert tscale(sc=Y + 4) == mrn.MRN_ERR_ALIASING          # out over the scale
+    assert tscale(o=B + 4) == mrn.MRN_ERR_ALIASING           # partial over residual
+    assert mrn.mrn_launch_count() == 0
+
+
 def test_size_validation():
     assert rms(n=0) == mrn.MRN_ERR_INVALID_SIZE
     assert rms(n=-3) == mrn.MRN_ERR_INVALID_SIZE
@@ -129,7 +155,7 @@ def test_geometry_covers_every_row_width():
                   4096, 5120, 6656, 6657, 8192, 16384, 32768, 65536, 131072, 262144, 1 << 20]:
             for rows in (1, 4, 64, 4096, 65536):
                 for a16 in (True, False):
-                    for op in (0, 1, 2):
+                    for op in (0, 1, 2, 3, 4):
                         g = mrn.mrn_query_geometry(op, rows, n, dt, a16, 152)
                         vec = g["vec"]
                         assert vec == (16 // e if a16 and (n * e) % 16 == 0 else 1)

@@ -53,6 +53,18 @@ MUTANTS = [
     ("then-add-scale: scale dropped", "+ rr[j]) * out_scale;", "+ rr[j]);"),
     ("then-add-scale: scale on the norm only", "outr[j] = (xr[j] * inv_rms * gamma[j] + rr[j]) * out_scale;",
      "outr[j] = xr[j] * inv_rms * gamma[j] * out_scale + rr[j];"),
+    ("q8: ties away from zero", "double r = nearbyint(qreal);", "double r = round(qreal);"),
+    ("q8: truncation", "double r = nearbyint(qreal);", "double r = trunc(qreal);"),
+    ("q8: clamp at 128", "if (r > 127.0)\n        r = 127.0;", "if (r > 128.0)\n        r = 128.0;"),
+    ("q8: d = amax / 128", "double scale = amax / 127.0;", "double scale = amax / 128.0;"),
+    ("q8: signed max", "if (fabs(normed[l]) > amax)\n                    amax = fabs(normed[l]);",
+     "if (normed[l] > amax)\n                    amax = normed[l];"),
+    ("q8: gamma dropped", "normed[l] = xr[j] * gamma[j] * inv_rms;", "normed[l] = xr[j] * inv_rms;"),
+    ("q8: zero block divides by zero", "qreal[j] = (scale == 0.0) ? 0.0 : normed[l] / scale;",
+     "qreal[j] = normed[l] / scale;"),
+    ("f16: no carry", "if (q == 2048) {", "if (0) {"),
+    ("f16: subnormal quantum", "(lead < -14) ? -24 : lead - 10", "(lead < -14) ? -25 : lead - 10"),
+    ("f16: widening bias", "field - 15 - 10", "field - 15 - 11"),
     ("bf16 ties away from zero", "(frac == 0.5 && (q & 1u))", "(frac == 0.5)"),
     ("bf16 truncation", "if (frac > 0.5 || (frac == 0.5 && (q & 1u)))", "if (0)"),
     ("bf16 subnormal quantum", "(lead < -126) ? -133 : lead - 7", "(lead < -126) ? -134 : lead - 7"),
