@@ -3,8 +3,10 @@
 //
 // Operations: RMSNorm ("Chapter 12 -- RMSNorm and the dual-epsilon
 // sandwich", section 12.1), post norm then residual add (Hesper "RMSNorm
-// Layer", rmsNormThenAddKernel) and the dual-epsilon sandwich tail (section
-// 12.4.3).  This layer holds no arithmetic of the method; it checks
+// Layer", rmsNormThenAddKernel), the dual-epsilon sandwich tail (section
+// 12.4.3), residual add then norm (Hesper residualAddRmsNormKernel), post
+// norm, add, broadcast scale (Hesper rmsNormThenAddThenBroadcastScaleKernel)
+// and RMSNorm with Q8_1 quantisation (Hesper fusedRMSNormQ8_1Kernel).  This layer holds no arithmetic of the method; it checks
 // arguments, picks a register geometry from (n, rows, dtype, alignment) and
 // hands the call to the launcher of the operation.
 #include "mrn.h"
@@ -25,6 +27,7 @@ std::atomic<uint64_t> g_launch_count{0};
 thread_local int t_last_cuda_error = 0;
 thread_local bool t_forced = false;
 thread_local Geometry t_forced_geometry = {};
+thread_local uint32_t t_launch_options = 0;
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -90,6 +93,24 @@ void pick_threads(int64_t per, int *k_out, int *t_out, int (*max_threads)(int) =
 
 int tma_group_cap(int k) { return mrn::tma_group_max_threads(k); }
 
+// For batches in the register kernel: among (k, t) with at most 1/8 of the
+// slots idle, the one with t nearest 256 (measured best on GB300 for the
+// residual add + norm: 7 x 256 at n = 6656 f32, 2 x 256 at n = 4096 bf16).
+void pick_threads_batch(int64_t per, int *k_out, int *t_out) {
+    double best = 1e30;
+    for (int k = 1; k <= mrn::kMaxK; ++k) {
+        const int64_t t = ceil_div(ceil_div(per, k), 32) * 32;
+        if (t > mrn::cta_max_threads(k) || (t * k - per) * 8 > per) continue;
+        const double d = std::fabs(std::log2(static_cast<double>(t) / 256.0));
+        if (d < best) {
+            best = d;
+            *k_out = k;
+            *t_out = static_cast<int>(t);
+        }
+    }
+    if (best > 1e29) pick_threads(per, k_out, t_out);
+}
+
 // Dynamic shared memory the staged kernel may use (the rest of the 227 KB
 // holds its static reduction slots and barriers).
 constexpr int64_t kTmaSharedBudget = mrn::kSharedBytesPerCta - 1024;
@@ -111,10 +132,14 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     g.cluster = 1;
     const int64_t nvec = ceil_div(n, g.vec);
     if (nvec <= 32 * mrn::kMaxK) {
+        // About four loads per thread (measured on GB300: per-head n = 128 rows
+        // run ~15% faster with 4 slots x 4..8 lanes than with 1 slot x 16..32).
         g.kind = mrn::kRowsPerWarp;
         g.threads = mrn::kWarpKernelThreads;
-        g.lanes = nvec <= 32 ? static_cast<int>(pow2_ceil(nvec)) : 32;
-        g.k = static_cast<int>(ceil_div(nvec, 32));
+        g.lanes = static_cast<int>(std::min<int64_t>(32, pow2_ceil(ceil_div(nvec, 4))));
+        if (op == mrn::kRmsnormQ8)   // a Q8_1 block must sit on consecutive lanes
+            g.lanes = std::max(g.lanes, mrn::kQ8Block / g.vec);
+        g.k = static_cast<int>(ceil_div(nvec, g.lanes));
         g.rows_per_cta = g.threads / g.lanes;
         return g;
     }
@@ -125,7 +150,12 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     // deeper per-CTA prefetch; groups of about 128 threads with more register
     // slots each beat wider groups.)
     const int64_t row_bytes = n * elem_bytes(dt);
-    if (aligned16 && rows >= sms && nvec <= 2 * 1024) {
+    // The residual add + norm stores its sum before its only reduction, and the
+    // Q8_1 pass has more arithmetic per byte; both run faster in the register
+    // kernel with many CTAs per SM than in the staged one (measured on GB300:
+    // add+norm 6.45 vs 6.03 TB/s at 4096 x 6656 f32).
+    const bool staged_pays = op != mrn::kAddRmsnorm && op != mrn::kRmsnormQ8;
+    if (staged_pays && aligned16 && rows >= sms && nvec <= 2 * 1024) {
         const int stages = 2;
         if (mrn::tma_shared_bytes(op, row_bytes, stages) <= kTmaSharedBudget) {
             g.kind = mrn::kTma;
@@ -157,7 +187,11 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
         const int64_t by_width = pow2_floor(std::max<int64_t>(1, nvec / 192));
         cl = std::max(cl, std::min<int64_t>(8, std::min(by_rows, by_width)));
     }
-    pick_threads(ceil_div(nvec, cl), &g.k, &g.threads);
+    if (!staged_pays && rows >= sms) {
+        pick_threads_batch(ceil_div(nvec, cl), &g.k, &g.threads);
+    } else {
+        pick_threads(ceil_div(nvec, cl), &g.k, &g.threads);
+    }
     g.kind = mrn::kCta;
     g.cluster = static_cast<int>(cl);
     g.lanes = 0;
@@ -206,6 +240,7 @@ bool resolve_forced(Geometry g, mrn::Op op, int64_t n, mrn_dtype dt, bool aligne
         g.rows_per_cta = g.groups;
     } else if (g.kind == mrn::kRowsPerWarp) {
         if (static_cast<int64_t>(g.lanes) * g.k < nvec) return false;
+        if (op == mrn::kRmsnormQ8 && g.lanes < mrn::kQ8Block / g.vec) return false;
         g.cluster = 1;
         g.rows_per_cta = g.threads / g.lanes;
     } else if (g.kind == mrn::kCta) {
@@ -266,6 +301,7 @@ mrn_status launch(const Call &c, bool aligned16, cudaStream_t stream) {
     } else {
         g = choose_geometry(c.op, c.rows, c.n, c.dt, aligned16, sm_count_of_current_device());
     }
+    g.pdl = (t_launch_options & MRN_LAUNCH_PDL) ? 1 : 0;
     KernelArgs a = c.args;
     a.n = c.n;
     a.nvec = ceil_div(c.n, g.vec);
@@ -275,7 +311,14 @@ mrn_status launch(const Call &c, bool aligned16, cudaStream_t stream) {
     switch (c.op) {
     case mrn::kRmsnorm: err = mrn::launch_rmsnorm(bf16, g, a, c.rows, stream, &launched); break;
     case mrn::kThenAdd: err = mrn::launch_then_add(bf16, g, a, c.rows, stream, &launched); break;
-    default: err = mrn::launch_sandwich(bf16, g, a, c.rows, stream, &launched); break;
+    case mrn::kSandwich: err = mrn::launch_sandwich(bf16, g, a, c.rows, stream, &launched); break;
+    case mrn::kAddRmsnorm:
+        err = mrn::launch_add_rmsnorm(bf16, g, a, c.rows, stream, &launched);
+        break;
+    case mrn::kThenAddScale:
+        err = mrn::launch_then_add_scale(bf16, g, a, c.rows, stream, &launched);
+        break;
+    default: err = mrn::launch_rmsnorm_q8_1(bf16, g, a, c.rows, stream, &launched); break;
     }
     g_launch_count.fetch_add(launched, std::memory_order_relaxed);
     if (err != cudaSuccess) {
@@ -375,6 +418,93 @@ mrn_status mrn_norm_residual_norm(const void *block_out, const void *residual,
     return launch(c, a16, stream);
 }
 
+mrn_status mrn_add_rmsnorm(const void *a, const void *b, const void *gamma, void *residual_out,
+                           void *normed, int64_t rows, int64_t n, float eps, mrn_dtype dtype,
+                           cudaStream_t stream) {
+    mrn_status st = check_common(rows, n, dtype, eps, eps);
+    if (st != MRN_OK || rows == 0) return st;
+    if (!a || !b || !gamma || !residual_out || !normed) return MRN_ERR_NULL_POINTER;
+    const int64_t e = elem_bytes(dtype);
+    if (!aligned_to(a, e) || !aligned_to(b, e) || !aligned_to(gamma, e) ||
+        !aligned_to(residual_out, e) || !aligned_to(normed, e))
+        return MRN_ERR_MISALIGNED;
+    const int64_t row_bytes = rows * n * e;
+    const Span sa = span_of(a, row_bytes), sb = span_of(b, row_bytes);
+    const Span sg = span_of(gamma, n * e);
+    const Span ss = span_of(residual_out, row_bytes), sn = span_of(normed, row_bytes);
+    if (!output_vs_row_input_ok(ss, sa) || !output_vs_row_input_ok(ss, sb) ||
+        !output_vs_row_input_ok(sn, sa) || !output_vs_row_input_ok(sn, sb) || overlaps(ss, sn) ||
+        overlaps(ss, sg) || overlaps(sn, sg))
+        return MRN_ERR_ALIASING;
+    const bool a16 = (n * e) % 16 == 0 && aligned_to(a, 16) && aligned_to(b, 16) &&
+                     aligned_to(gamma, 16) && aligned_to(residual_out, 16) &&
+                     aligned_to(normed, 16);
+    Call c{mrn::kAddRmsnorm, dtype, rows, n, KernelArgs{}};
+    c.args.x = a;
+    c.args.res = b;
+    c.args.g1 = gamma;
+    c.args.y = residual_out;
+    c.args.y2 = normed;
+    c.args.eps1 = eps;
+    c.args.eps2 = eps;
+    return launch(c, a16, stream);
+}
+
+mrn_status mrn_rmsnorm_then_add_scale(const void *x, const void *gamma, const void *residual,
+                                      const void *out_scale, void *out, int64_t rows, int64_t n,
+                                      float eps, mrn_dtype dtype, cudaStream_t stream) {
+    mrn_status st = check_common(rows, n, dtype, eps, eps);
+    if (st != MRN_OK || rows == 0) return st;
+    if (!x || !gamma || !residual || !out_scale || !out) return MRN_ERR_NULL_POINTER;
+    const int64_t e = elem_bytes(dtype);
+    if (!aligned_to(x, e) || !aligned_to(gamma, e) || !aligned_to(residual, e) ||
+        !aligned_to(out_scale, e) || !aligned_to(out, e))
+        return MRN_ERR_MISALIGNED;
+    const int64_t row_bytes = rows * n * e;
+    const Span sx = span_of(x, row_bytes), sr = span_of(residual, row_bytes);
+    const Span sg = span_of(gamma, n * e), sc = span_of(out_scale, e);
+    const Span so = span_of(out, row_bytes);
+    if (!output_vs_row_input_ok(so, sx) || !output_vs_row_input_ok(so, sr) || overlaps(so, sg) ||
+        overlaps(so, sc))
+        return MRN_ERR_ALIASING;
+    const bool a16 = (n * e) % 16 == 0 && aligned_to(x, 16) && aligned_to(gamma, 16) &&
+                     aligned_to(residual, 16) && aligned_to(out, 16);
+    Call c{mrn::kThenAddScale, dtype, rows, n, KernelArgs{}};
+    c.args.x = x;
+    c.args.res = residual;
+    c.args.g1 = gamma;
+    c.args.scale = out_scale;
+    c.args.y = out;
+    c.args.eps1 = eps;
+    c.args.eps2 = eps;
+    return launch(c, a16, stream);
+}
+
+mrn_status mrn_rmsnorm_q8_1(const void *x, const void *gamma, void *blocks, int64_t rows,
+                            int64_t n, float eps, mrn_dtype dtype, cudaStream_t stream) {
+    mrn_status st = check_common(rows, n, dtype, eps, eps);
+    if (st != MRN_OK) return st;
+    if (n % mrn::kQ8Block != 0) return MRN_ERR_INVALID_SIZE;
+    if (rows > 0 && rows > INT64_MAX / ((n / mrn::kQ8Block) * mrn::kQ8BlockBytes))
+        return MRN_ERR_INVALID_SIZE;
+    if (rows == 0) return MRN_OK;
+    if (!x || !gamma || !blocks) return MRN_ERR_NULL_POINTER;
+    const int64_t e = elem_bytes(dtype);
+    if (!aligned_to(x, e) || !aligned_to(gamma, e) || !aligned_to(blocks, 4))
+        return MRN_ERR_MISALIGNED;
+    const Span sx = span_of(x, rows * n * e), sg = span_of(gamma, n * e);
+    const Span so = span_of(blocks, rows * (n / mrn::kQ8Block) * mrn::kQ8BlockBytes);
+    if (overlaps(so, sx) || overlaps(so, sg)) return MRN_ERR_ALIASING;
+    const bool a16 = (n * e) % 16 == 0 && aligned_to(x, 16) && aligned_to(gamma, 16);
+    Call c{mrn::kRmsnormQ8, dtype, rows, n, KernelArgs{}};
+    c.args.x = x;
+    c.args.g1 = gamma;
+    c.args.y = blocks;
+    c.args.eps1 = eps;
+    c.args.eps2 = eps;
+    return launch(c, a16, stream);
+}
+
 const char *mrn_status_string(mrn_status status) {
     switch (status) {
     case MRN_OK: return "ok";
@@ -396,8 +526,7 @@ int mrn_last_cuda_error(void) { return t_last_cuda_error; }
 mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtype,
                               int32_t aligned16, int32_t sm_count, mrn_geometry *out) {
     if (!out) return MRN_ERR_NULL_POINTER;
-    if (op != MRN_OP_RMSNORM && op != MRN_OP_THEN_ADD && op != MRN_OP_SANDWICH)
-        return MRN_ERR_INVALID_GEOMETRY;
+    if (op < MRN_OP_RMSNORM || op > MRN_OP_RMSNORM_Q8_1) return MRN_ERR_INVALID_GEOMETRY;
     mrn_status st = check_common(rows, n, dtype, 1.0f, 1.0f);
     if (st != MRN_OK) return st;
     const bool a16 = aligned16 != 0 && (n * elem_bytes(dtype)) % 16 == 0;
@@ -449,15 +578,29 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry) {
 
 uint64_t mrn_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
+mrn_status mrn_set_launch_options(uint32_t options) {
+    if (options & ~static_cast<uint32_t>(MRN_LAUNCH_PDL)) return MRN_ERR_INVALID_GEOMETRY;
+    t_launch_options = options;
+    return MRN_OK;
+}
+
+uint32_t mrn_launch_options(void) { return t_launch_options; }
+
 int mrn_wait_timeouts(void) {
-    const int a = mrn::take_wait_timeouts_rmsnorm();
-    const int b = mrn::take_wait_timeouts_then_add();
-    const int c = mrn::take_wait_timeouts_sandwich();
-    if (a < 0 || b < 0 || c < 0) {
-        (void)cudaGetLastError();
-        return -1;
+    const int counts[] = {mrn::take_wait_timeouts_rmsnorm(), mrn::take_wait_timeouts_then_add(),
+                          mrn::take_wait_timeouts_sandwich(),
+                          mrn::take_wait_timeouts_add_rmsnorm(),
+                          mrn::take_wait_timeouts_then_add_scale(),
+                          mrn::take_wait_timeouts_rmsnorm_q8_1()};
+    int total = 0;
+    for (int v : counts) {
+        if (v < 0) {
+            (void)cudaGetLastError();
+            return -1;
+        }
+        total += v;
     }
-    return a + b + c;
+    return total;
 }
 
 }  // extern "C"

@@ -5,19 +5,45 @@
 #include <cstdint>
 #include <cuda_runtime_api.h>
 
+// Helpers used both by the host layer and inside kernels.
+#if defined(__CUDACC__)
+#define MRN_HOST_DEVICE __host__ __device__
+#else
+#define MRN_HOST_DEVICE
+#endif
+
 namespace mrn {
 
-enum Op : int { kRmsnorm = 0, kThenAdd = 1, kSandwich = 2 };
+enum Op : int {
+    kRmsnorm = 0,
+    kThenAdd = 1,
+    kSandwich = 2,
+    kAddRmsnorm = 3,
+    kThenAddScale = 4,
+    kRmsnormQ8 = 5,   // RMSNorm then Q8_1 blocks: 32 codes + (f16 d, f16 s) per 36 bytes
+};
+constexpr int kQ8Block = 32;        // elements per Q8_1 block
+constexpr int kQ8BlockBytes = 36;   // f16 d, f16 s, int8 q[32]
+
+// Row operands each operation reads, and the gamma vectors it uses.
+MRN_HOST_DEVICE constexpr int op_row_inputs(int op) {
+    return (op == kRmsnorm || op == kRmsnormQ8) ? 1 : 2;
+}
+MRN_HOST_DEVICE constexpr int op_gammas(int op) { return op == kSandwich ? 2 : 1; }
 enum Kind : int { kAuto = 0, kRowsPerWarp = 1, kCta = 2, kStream = 3, kTma = 4 };
 
 // Launch-time view of one call.  Pointers are device pointers; row operands
 // are [rows x n] row-major.  For the sandwich, x = block_out, res = residual,
-// g1 = gamma_post, g2 = gamma_pre, y = out_stream, y2 = normed.
+// g1 = gamma_post, g2 = gamma_pre, y = out_stream, y2 = normed.  For the
+// residual add + norm, x = a, res = b, y = residual_out, y2 = normed.  For
+// then-add-scale, scale points at the one broadcast element.  For Q8_1, y
+// points at the output blocks.
 struct KernelArgs {
     const void *x;
     const void *res;
     const void *g1;
     const void *g2;
+    const void *scale;
     void *y;
     void *y2;
     int64_t n;         // elements per row
@@ -39,6 +65,7 @@ struct Geometry {
     int stages;        // shared-memory row stages (kTma)
     int ctas;          // CTAs launched (kTma: persistent grid), 0 = from rows
     int groups;        // warp groups per CTA (kTma), each on its own rows
+    int pdl;           // launch with programmatic stream serialisation
 };
 
 // Register-slot limits per thread count: the kernels are compiled with these
@@ -64,15 +91,25 @@ cudaError_t launch_then_add(bool bf16, const Geometry &g, const KernelArgs &a, i
                             cudaStream_t stream, uint64_t *launches);
 cudaError_t launch_sandwich(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
                             cudaStream_t stream, uint64_t *launches);
+cudaError_t launch_add_rmsnorm(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
+                               cudaStream_t stream, uint64_t *launches);
+cudaError_t launch_then_add_scale(bool bf16, const Geometry &g, const KernelArgs &a,
+                                  int64_t rows, cudaStream_t stream, uint64_t *launches);
+cudaError_t launch_rmsnorm_q8_1(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
+                                cudaStream_t stream, uint64_t *launches);
 
-// Dynamic shared memory of the staged (kTma) kernel for one operation.
+// Dynamic shared memory of the staged (kTma) kernel for one operation: the
+// gammas once, plus each stage's row operands.
 constexpr int64_t tma_shared_bytes(int op, int64_t row_bytes, int stages) {
-    return row_bytes * ((op == kSandwich ? 2 : 1) + stages * (op == kRmsnorm ? 1 : 2));
+    return row_bytes * (op_gammas(op) + stages * op_row_inputs(op));
 }
 
 // Number of bounded waits that ran out since the last call (and reset them).
 int take_wait_timeouts_rmsnorm();
 int take_wait_timeouts_then_add();
 int take_wait_timeouts_sandwich();
+int take_wait_timeouts_add_rmsnorm();
+int take_wait_timeouts_then_add_scale();
+int take_wait_timeouts_rmsnorm_q8_1();
 
 }  // namespace mrn

@@ -33,6 +33,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "mrn_internal.h"
@@ -252,6 +253,16 @@ __device__ __forceinline__ float cta_allsum(float v, ReduceSlots &s, unsigned cl
     return t;
 }
 
+// Programmatic dependent launch.  Every kernel starts by waiting for the
+// grid it depends on (the previous kernel on the stream) to complete and
+// publish its memory -- a no-op unless the launch allowed programmatic
+// serialisation -- and then lets its own dependent grid be scheduled, so that
+// the next launch's set-up overlaps this kernel instead of following it.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float inv_rms(float sum_sq, int64_t n, float eps) {
     return 1.0f / sqrtf(sum_sq / static_cast<float>(n) + eps);
 }
@@ -296,6 +307,106 @@ __device__ __forceinline__ Frag<T, VEC> apply_norm_add(const Frag<T, VEC> &x, fl
     return out;
 }
 
+// out = fma(x * inv, g, r) * scale   (then-add-then-broadcast-scale)
+template <class T, int VEC>
+__device__ __forceinline__ Frag<T, VEC> apply_norm_add_scale(const Frag<T, VEC> &x, float inv,
+                                                              const Frag<T, VEC> &g,
+                                                              const Frag<T, VEC> &r, float sc) {
+    float o[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) o[i] = fmaf(x.get(i) * inv, g.get(i), r.get(i)) * sc;
+    Frag<T, VEC> out;
+    out.put(o);
+    return out;
+}
+
+// s = a + b, rounded once to T   (the residual add of add+norm)
+template <class T, int VEC>
+__device__ __forceinline__ Frag<T, VEC> add_frags(const Frag<T, VEC> &a, const Frag<T, VEC> &b) {
+    float o[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) o[i] = a.get(i) + b.get(i);
+    Frag<T, VEC> out;
+    out.put(o);
+    return out;
+}
+
+// The broadcast scale of then-add-scale (one element of type T), as f32.
+template <int OP, class T>
+__device__ __forceinline__ float load_out_scale(const void *p) {
+    if (OP != kThenAddScale) return 1.0f;
+    Frag<T, 1> f;
+    ld_ro(f, p);
+    return f.get(0);
+}
+
+// The output of the single-norm operations for one fragment.
+template <int OP, class T, int VEC>
+__device__ __forceinline__ Frag<T, VEC> single_norm_output(const Frag<T, VEC> &x, float inv,
+                                                           const Frag<T, VEC> &g,
+                                                           const Frag<T, VEC> &r, float sc) {
+    if (OP == kRmsnorm) return apply_norm(x, inv, g);
+    if (OP == kThenAdd) return apply_norm_add(x, inv, g, r);
+    return apply_norm_add_scale(x, inv, g, r, sc);
+}
+
+// RMSNorm + Q8_1 output of one fragment (Hesper fusedRMSNormQ8_1Kernel):
+// x_normed = (x * gamma) * inv; a 32-element block is held by VPB = 32/VEC
+// consecutive lanes (one register slot each), which agree on the block's
+// amax by a butterfly max; d = amax / 127; q = x_normed / d rounded to
+// nearest, ties to even, clamped to int8 (0 when d == 0).  The quotient is
+// formed as x_normed * (127 / amax) -- one IEEE division per block instead of
+// one per element, which keeps the pass memory-bound; it can differ from
+// x_normed / d only within a few f32 ulps of a rounding tie.  Lane 0 of the
+// block writes the header (f16 d, f16 s = 0), every lane its VEC codes.
+// Every lane of the warp must call this (it shuffles); `valid` only gates
+// the stores.  v is the fragment's index within the row.
+template <class T, int VEC>
+__device__ __forceinline__ void q8_1_output(const Frag<T, VEC> &x, const Frag<T, VEC> &g,
+                                            float inv, bool valid, char *row_blocks,
+                                            int64_t v) {
+    constexpr int VPB = kQ8Block / VEC;
+    float xn[VEC];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        xn[i] = (x.get(i) * g.get(i)) * inv;
+        amax = fmaxf(amax, fabsf(xn[i]));
+    }
+#pragma unroll
+    for (int o = VPB / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (!valid) return;
+    const float d = amax / 127.0f;
+    const float id = amax > 0.0f ? 127.0f / amax : 0.0f;
+    uint32_t packed[(VEC + 3) / 4] = {};
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const int q = min(127, max(-128, __float2int_rn(xn[i] * id)));
+        packed[i / 4] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i % 4));
+    }
+    char *block = row_blocks + (v / VPB) * kQ8BlockBytes;
+    const int j = static_cast<int>(v % VPB);
+    if (j == 0) {
+        const uint32_t header = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(d)));
+        asm volatile("st.global.u32 [%0], %1;" :: "l"(block), "r"(header) : "memory");
+    }
+    char *codes = block + 4 + j * VEC;
+    if (VEC >= 4) {
+#pragma unroll
+        for (int w = 0; w < VEC / 4; ++w)
+            asm volatile("st.global.u32 [%0], %1;" :: "l"(codes + 4 * w), "r"(packed[w])
+                         : "memory");
+    } else {
+        const unsigned short b = static_cast<unsigned short>(packed[0] & 0xFFu);
+        asm volatile("st.global.u8 [%0], %1;" :: "l"(codes), "h"(b) : "memory");
+    }
+}
+
+// First byte of a row's Q8_1 blocks.
+__device__ __forceinline__ char *q8_row_blocks(const KernelArgs &a, int64_t row) {
+    return static_cast<char *>(a.y) + row * (a.n / kQ8Block) * kQ8BlockBytes;
+}
+
 // ---------------------------------------------------------------------------
 // Row body shared by the register-resident kernels.  A "slot" k of this
 // thread holds load index v = first + k * stride of the row (masked when
@@ -320,7 +431,7 @@ __device__ __forceinline__ void row_body(const KernelArgs &a, int64_t row, bool 
         const int64_t e = row_elem + v * VEC;
         if (ok[k]) {
             ld_stream(xv[k], elem_ptr<T>(a.x, e));
-            if (OP != kRmsnorm) ld_stream(rv[k], elem_ptr<T>(a.res, e));
+            if (op_row_inputs(OP) == 2) ld_stream(rv[k], elem_ptr<T>(a.res, e));
         } else {
             xv[k].zero();
             rv[k].zero();
@@ -331,19 +442,49 @@ __device__ __forceinline__ void row_body(const KernelArgs &a, int64_t row, bool 
         if (ok[k]) ld_ro(gv[k], elem_ptr<T>(a.g1, (first + k * stride) * VEC));
     }
 
+    const float sc = load_out_scale<OP, T>(a.scale);
+
     float ss = 0.0f;
+    if (OP == kAddRmsnorm) {
+        // residual_out = a + b (rounded to T), stored; its stored value is normed
 #pragma unroll
-    for (int k = 0; k < K; ++k) ss += frag_sum_sq(xv[k]);
+        for (int k = 0; k < K; ++k) {
+            if (!ok[k]) continue;
+            rv[k] = add_frags(xv[k], rv[k]);
+            st_global(elem_ptr<T>(a.y, row_elem + (first + k * stride) * VEC), rv[k]);
+            ss += frag_sum_sq(rv[k]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < K; ++k) ss += frag_sum_sq(xv[k]);
+    }
     const float inv1 = inv_rms(reduce1(ss), a.n, a.eps1);
 
-    if (OP == kRmsnorm || OP == kThenAdd) {
+    if (OP == kAddRmsnorm) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             if (!ok[k]) continue;
             const int64_t v = first + k * stride;
-            const Fr o = (OP == kRmsnorm) ? apply_norm(xv[k], inv1, gv[k])
-                                          : apply_norm_add(xv[k], inv1, gv[k], rv[k]);
-            st_global(elem_ptr<T>(a.y, row_elem + v * VEC), o);
+            st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(rv[k], inv1, gv[k]));
+        }
+        return;
+    }
+    if (OP == kRmsnormQ8) {
+        char *blocks = q8_row_blocks(a, row);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {   // no early exit: every lane shuffles
+            if (!ok[k]) gv[k].zero();
+            q8_1_output(xv[k], gv[k], inv1, ok[k], blocks, first + k * stride);
+        }
+        return;
+    }
+    if (OP != kSandwich) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (!ok[k]) continue;
+            const int64_t v = first + k * stride;
+            st_global(elem_ptr<T>(a.y, row_elem + v * VEC),
+                      single_norm_output<OP>(xv[k], inv1, gv[k], rv[k], sc));
         }
         return;
     }
@@ -377,6 +518,7 @@ __device__ __forceinline__ void row_body(const KernelArgs &a, int64_t row, bool 
 template <int OP, class T, int VEC, int K>
 __global__ void __launch_bounds__(kWarpKernelThreads)
 mrn_rows_per_warp_kernel(const KernelArgs a, const int lanes) {
+    pdl_enter();
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t row = a.row0 + gtid / lanes;
     const int lane_in_row = threadIdx.x & (lanes - 1);
@@ -391,6 +533,7 @@ __global__ void __launch_bounds__(cta_max_threads(K))
 mrn_cta_kernel(const KernelArgs a) {
     __shared__ ReduceSlots slots1;
     __shared__ ReduceSlots slots2;
+    pdl_enter();
     const unsigned cl = cluster_nctarank();
     const unsigned crank = cluster_ctarank();
     if (cl > 1) cluster_arrive_relaxed();
@@ -415,23 +558,85 @@ mrn_stream_kernel(const KernelArgs a) {
     constexpr int U = kStreamUnroll;
     __shared__ ReduceSlots slots1;
     __shared__ ReduceSlots slots2;
+    pdl_enter();
     const int64_t row = a.row0 + blockIdx.x;
     const int64_t row_elem = row * a.n;
     const int64_t nt = blockDim.x;
 
+    const float sc = load_out_scale<OP, T>(a.scale);
     float ss = 0.0f;
     for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
-        Fr x[U];
+        Fr x[U], r[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t v = v0 + u * nt;
-            if (v < a.nvec) ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
-            else x[u].zero();
+            if (v < a.nvec) {
+                ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
+                if (OP == kAddRmsnorm) ld_stream(r[u], elem_ptr<T>(a.res, row_elem + v * VEC));
+            } else {
+                x[u].zero();
+                r[u].zero();
+            }
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) ss += frag_sum_sq(x[u]);
+        for (int u = 0; u < U; ++u) {
+            if (OP == kAddRmsnorm) {
+                const int64_t v = v0 + u * nt;
+                if (v >= a.nvec) continue;
+                x[u] = add_frags(x[u], r[u]);       // residual_out, stored and normed below
+                st_global(elem_ptr<T>(a.y, row_elem + v * VEC), x[u]);
+            }
+            ss += frag_sum_sq(x[u]);
+        }
     }
     const float inv1 = inv_rms(cta_allsum(ss, slots1, 1, 0, false), a.n, a.eps1);
+
+    if (OP == kAddRmsnorm) {
+        // re-read the sums this same thread stored
+        for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
+            Fr sm[U], g[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < a.nvec) {
+                    ld_plain(sm[u], elem_ptr<T>(a.y, row_elem + v * VEC));
+                    ld_ro(g[u], elem_ptr<T>(a.g1, v * VEC));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < a.nvec)
+                    st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(sm[u], inv1, g[u]));
+            }
+        }
+        return;
+    }
+    if (OP == kRmsnormQ8) {
+        // The trip count is uniform across each warp (the q8 output shuffles).
+        char *blocks = q8_row_blocks(a, row);
+        const int64_t lane = threadIdx.x & 31;
+        for (int64_t v0 = threadIdx.x; v0 - lane < a.nvec; v0 += nt * U) {
+            Fr x[U], g[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < a.nvec) {
+                    ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
+                    ld_ro(g[u], elem_ptr<T>(a.g1, v * VEC));
+                } else {
+                    x[u].zero();
+                    g[u].zero();
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                q8_1_output(x[u], g[u], inv1, v < a.nvec, blocks, v);
+            }
+        }
+        return;
+    }
 
     float ss2 = 0.0f;
     for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
@@ -450,12 +655,12 @@ mrn_stream_kernel(const KernelArgs a) {
             const int64_t v = v0 + u * nt;
             if (v >= a.nvec) continue;
             const int64_t e = row_elem + v * VEC;
-            if (OP == kRmsnorm) {
-                st_global(elem_ptr<T>(a.y, e), apply_norm(x[u], inv1, g[u]));
-            } else {
+            if (OP == kSandwich) {
                 const Fr o = apply_norm_add(x[u], inv1, g[u], r[u]);
                 st_global(elem_ptr<T>(a.y, e), o);
-                if (OP == kSandwich) ss2 += frag_sum_sq(o);
+                ss2 += frag_sum_sq(o);
+            } else {
+                st_global(elem_ptr<T>(a.y, e), single_norm_output<OP>(x[u], inv1, g[u], r[u], sc));
             }
         }
     }
@@ -627,8 +832,9 @@ __global__ void __launch_bounds__(tma_max_threads(K, G), 1)
 mrn_tma_kernel(const KernelArgs a, const int stages) {
     constexpr int VEC = 16 / T::kBytes;
     using Fr = Frag<T, VEC>;
-    constexpr int NS = (OP == kRmsnorm) ? 1 : 2;   // row operands staged per row
-    constexpr int NG = (OP == kSandwich) ? 2 : 1;  // gammas kept in shared memory
+    pdl_enter();
+    constexpr int NS = op_row_inputs(OP);   // row operands staged per row
+    constexpr int NG = op_gammas(OP);       // gammas kept in shared memory
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ ReduceSlots slots1[G];
     __shared__ ReduceSlots slots2[G];
@@ -675,6 +881,7 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
         }
     }
     int failed = (my_rows > 0 && !mbar_wait_bounded(&bars[stages], 0)) ? 1 : 0;
+    const float sc = load_out_scale<OP, T>(a.scale);
 
     for (int64_t it = grp; it < my_rows; it += G) {
         const int s = static_cast<int>(it % stages);
@@ -696,9 +903,21 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
                 rv[k].zero();
             }
         }
+        const int64_t row_elem = row * a.n;
         float ss = 0.0f;
+        if (OP == kAddRmsnorm) {
 #pragma unroll
-        for (int k = 0; k < K; ++k) ss += frag_sum_sq(xv[k]);
+            for (int k = 0; k < K; ++k) {
+                const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+                if (v >= a.nvec || failed) continue;
+                rv[k] = add_frags(xv[k], rv[k]);
+                st_global(elem_ptr<T>(a.y, row_elem + v * VEC), rv[k]);
+                ss += frag_sum_sq(rv[k]);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < K; ++k) ss += frag_sum_sq(xv[k]);
+        }
         int any_failed;
         const float tot = wg_allsum<true>(ss, slots1[grp], bar_id, gsize, gtid,
                                              failed | abort_flag, &any_failed);
@@ -717,18 +936,42 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             }
         }
         const float inv1 = inv_rms(tot, a.n, a.eps1);
-        const int64_t row_elem = row * a.n;
 
-        if (OP == kRmsnorm || OP == kThenAdd) {
+        if (OP == kAddRmsnorm) {
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
                 if (v >= a.nvec) continue;
                 Fr g;
                 ld_shared(g, gsm + v * 16);
-                const Fr o = (OP == kRmsnorm) ? apply_norm(xv[k], inv1, g)
-                                              : apply_norm_add(xv[k], inv1, g, rv[k]);
-                st_global(elem_ptr<T>(a.y, row_elem + v * VEC), o);
+                st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(rv[k], inv1, g));
+            }
+            continue;
+        }
+        if (OP == kRmsnormQ8) {
+            char *blocks = q8_row_blocks(a, row);
+#pragma unroll
+            for (int k = 0; k < K; ++k) {   // no early exit: every lane shuffles
+                const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+                Fr g;
+                if (v < a.nvec) {
+                    ld_shared(g, gsm + v * 16);
+                } else {
+                    g.zero();
+                }
+                q8_1_output(xv[k], g, inv1, v < a.nvec, blocks, v);
+            }
+            continue;
+        }
+        if (OP != kSandwich) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+                if (v >= a.nvec) continue;
+                Fr g;
+                ld_shared(g, gsm + v * 16);
+                st_global(elem_ptr<T>(a.y, row_elem + v * VEC),
+                          single_norm_output<OP>(xv[k], inv1, g, rv[k], sc));
             }
             continue;
         }
@@ -874,6 +1117,13 @@ cudaError_t launch_tma(const Geometry &g, KernelArgs a, int64_t rows, cudaStream
         cfg.blockDim = dim3(g.threads, 1, 1);
         cfg.dynamicSmemBytes = static_cast<size_t>(shared);
         cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        if (g.pdl) {
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+        }
         err = cudaLaunchKernelEx(&cfg, fn, a, g.stages);
         if (err != cudaSuccess) return err;
         ++*launches;
@@ -899,10 +1149,17 @@ cudaError_t launch_typed(const Geometry &g, KernelArgs a, int64_t rows, cudaStre
         a.row0 = r0;
         a.rows_end = r0 + nrows;
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         cfg.blockDim = dim3(g.threads, 1, 1);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 0;
+        if (g.pdl) {
+            attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+            ++cfg.numAttrs;
+        }
         cudaError_t err;
         if (g.kind == kRowsPerWarp) {
             const int64_t rpc = g.threads / g.lanes;
@@ -917,12 +1174,11 @@ cudaError_t launch_typed(const Geometry &g, KernelArgs a, int64_t rows, cudaStre
                                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
                     if (err != cudaSuccess) return err;
                 }
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = static_cast<unsigned>(g.cluster);
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
+                cudaLaunchAttribute &c = attr[cfg.numAttrs++];
+                c.id = cudaLaunchAttributeClusterDimension;
+                c.val.clusterDim.x = static_cast<unsigned>(g.cluster);
+                c.val.clusterDim.y = 1;
+                c.val.clusterDim.z = 1;
             }
             err = cudaLaunchKernelEx(&cfg, fn, a);
         } else {

@@ -25,12 +25,18 @@ MRN_BF16 = 1
 MRN_OP_RMSNORM = 0
 MRN_OP_THEN_ADD = 1
 MRN_OP_SANDWICH = 2
+MRN_OP_ADD_RMSNORM = 3
+MRN_OP_THEN_ADD_SCALE = 4
+MRN_OP_RMSNORM_Q8_1 = 5
+Q8_1_BLOCK_BYTES = 36
 
 MRN_GEOM_AUTO = 0
 MRN_GEOM_ROWS_PER_WARP = 1
 MRN_GEOM_CTA = 2
 MRN_GEOM_STREAM = 3
 MRN_GEOM_TMA = 4
+
+MRN_LAUNCH_PDL = 1
 
 STATUS = {
     0: "MRN_OK",
@@ -48,8 +54,10 @@ for _code, _name in STATUS.items():
     globals()[_name] = _code
 
 EXPORTS = ("mrn_rmsnorm", "mrn_rmsnorm_then_add", "mrn_norm_residual_norm",
+           "mrn_add_rmsnorm", "mrn_rmsnorm_then_add_scale", "mrn_rmsnorm_q8_1",
            "mrn_status_string", "mrn_last_cuda_error", "mrn_query_geometry",
-           "mrn_force_geometry", "mrn_launch_count", "mrn_wait_timeouts")
+           "mrn_force_geometry", "mrn_launch_count", "mrn_wait_timeouts",
+           "mrn_set_launch_options", "mrn_launch_options")
 
 
 class MrnError(RuntimeError):
@@ -98,7 +106,12 @@ def lib() -> ctypes.CDLL:
             L.mrn_rmsnorm_then_add.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _f, _i, _vp]
             L.mrn_norm_residual_norm.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
                                                  _f, _f, _i, _vp]
-            for fn in (L.mrn_rmsnorm, L.mrn_rmsnorm_then_add, L.mrn_norm_residual_norm):
+            L.mrn_add_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f, _i, _vp]
+            L.mrn_rmsnorm_then_add_scale.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f,
+                                                     _i, _vp]
+            L.mrn_rmsnorm_q8_1.argtypes = [_vp, _vp, _vp, _i64, _i64, _f, _i, _vp]
+            for fn in (L.mrn_rmsnorm, L.mrn_rmsnorm_then_add, L.mrn_norm_residual_norm,
+                       L.mrn_add_rmsnorm, L.mrn_rmsnorm_then_add_scale, L.mrn_rmsnorm_q8_1):
                 fn.restype = _i
             L.mrn_status_string.argtypes = [_i]
             L.mrn_status_string.restype = ctypes.c_char_p
@@ -113,6 +126,10 @@ def lib() -> ctypes.CDLL:
             L.mrn_launch_count.restype = ctypes.c_uint64
             L.mrn_wait_timeouts.argtypes = []
             L.mrn_wait_timeouts.restype = _i
+            L.mrn_set_launch_options.argtypes = [ctypes.c_uint32]
+            L.mrn_set_launch_options.restype = _i
+            L.mrn_launch_options.argtypes = []
+            L.mrn_launch_options.restype = ctypes.c_uint32
             _lib = L
     return _lib
 
@@ -132,6 +149,20 @@ def mrn_norm_residual_norm(block_out, residual, gamma_post, gamma_pre, out_strea
                            rows, n, eps_post, eps_pre, dtype, stream=0) -> int:
     return lib().mrn_norm_residual_norm(block_out, residual, gamma_post, gamma_pre, out_stream,
                                         normed, rows, n, eps_post, eps_pre, dtype, stream)
+
+
+def mrn_add_rmsnorm(a, b, gamma, residual_out, normed, rows, n, eps, dtype, stream=0) -> int:
+    return lib().mrn_add_rmsnorm(a, b, gamma, residual_out, normed, rows, n, eps, dtype, stream)
+
+
+def mrn_rmsnorm_then_add_scale(x, gamma, residual, out_scale, out, rows, n, eps, dtype,
+                               stream=0) -> int:
+    return lib().mrn_rmsnorm_then_add_scale(x, gamma, residual, out_scale, out, rows, n, eps,
+                                            dtype, stream)
+
+
+def mrn_rmsnorm_q8_1(x, gamma, blocks, rows, n, eps, dtype, stream=0) -> int:
+    return lib().mrn_rmsnorm_q8_1(x, gamma, blocks, rows, n, eps, dtype, stream)
 
 
 def mrn_status_string(status: int) -> str:
@@ -161,6 +192,15 @@ def mrn_force_geometry(geometry: dict | None) -> int:
 
 def mrn_launch_count() -> int:
     return lib().mrn_launch_count()
+
+
+def mrn_set_launch_options(options: int) -> int:
+    """Launch options of the calling thread (MRN_LAUNCH_PDL or 0)."""
+    return lib().mrn_set_launch_options(options)
+
+
+def mrn_launch_options() -> int:
+    return lib().mrn_launch_options()
 
 
 def mrn_wait_timeouts() -> int:
@@ -256,3 +296,63 @@ def norm_residual_norm(block_out, residual, gamma_post, gamma_pre, eps_post: flo
     if st != 0:
         raise MrnError(st, "mrn_norm_residual_norm")
     return out_stream, normed
+
+
+def add_rmsnorm(a, b, gamma, eps: float, residual_out=None, normed=None):
+    """(a + b, RMSNorm(a + b) * gamma); residual_out may be a or b (in place)."""
+    import torch
+    dt = _dtype_code(a)
+    _check(a, "a", a.dtype)
+    rows, n = _rows_n(a)
+    _check(b, "b", a.dtype, a.shape)
+    _check(gamma, "gamma", a.dtype, (n,))
+    residual_out = torch.empty_like(a) if residual_out is None else residual_out
+    normed = torch.empty_like(a) if normed is None else normed
+    _check(residual_out, "residual_out", a.dtype, a.shape)
+    _check(normed, "normed", a.dtype, a.shape)
+    st = mrn_add_rmsnorm(a.data_ptr(), b.data_ptr(), gamma.data_ptr(), residual_out.data_ptr(),
+                         normed.data_ptr(), rows, n, eps, dt, _stream(a))
+    if st != 0:
+        raise MrnError(st, "mrn_add_rmsnorm")
+    return residual_out, normed
+
+
+def rmsnorm_then_add_scale(x, gamma, residual, out_scale, eps: float, out=None):
+    """(RMSNorm(x) * gamma + residual) * out_scale[0]; out_scale is a one-element
+    device tensor of x's dtype."""
+    import torch
+    dt = _dtype_code(x)
+    _check(x, "x", x.dtype)
+    rows, n = _rows_n(x)
+    _check(gamma, "gamma", x.dtype, (n,))
+    _check(residual, "residual", x.dtype, x.shape)
+    _check(out_scale, "out_scale", x.dtype, (1,))
+    out = torch.empty_like(x) if out is None else out
+    _check(out, "out", x.dtype, x.shape)
+    st = mrn_rmsnorm_then_add_scale(x.data_ptr(), gamma.data_ptr(), residual.data_ptr(),
+                                    out_scale.data_ptr(), out.data_ptr(), rows, n, eps, dt,
+                                    _stream(x))
+    if st != 0:
+        raise MrnError(st, "mrn_rmsnorm_then_add_scale")
+    return out
+
+
+def rmsnorm_q8_1(x, gamma, eps: float, blocks=None):
+    """RMSNorm then Q8_1 blocks: returns a uint8 tensor [rows, n/32, 36] (f16 d,
+    f16 s = 0, int8 q[32] per block)."""
+    import torch
+    dt = _dtype_code(x)
+    _check(x, "x", x.dtype)
+    rows, n = _rows_n(x)
+    _check(gamma, "gamma", x.dtype, (n,))
+    if n % 32:
+        raise ValueError("n must be a multiple of 32")
+    if blocks is None:
+        blocks = torch.empty((rows, n // 32, Q8_1_BLOCK_BYTES), dtype=torch.uint8,
+                             device=x.device)
+    _check(blocks, "blocks", torch.uint8, (rows, n // 32, Q8_1_BLOCK_BYTES))
+    st = mrn_rmsnorm_q8_1(x.data_ptr(), gamma.data_ptr(), blocks.data_ptr(), rows, n, eps, dt,
+                          _stream(x))
+    if st != 0:
+        raise MrnError(st, "mrn_rmsnorm_q8_1")
+    return blocks

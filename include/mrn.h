@@ -20,8 +20,8 @@
  * residual add, row-major batch) and rmsNormThenAddBatchInPlaceKernel (in-place
  * residual update).
  *
- * Common conventions for the three operations
- * -------------------------------------------
+ * Common conventions for the operations
+ * -------------------------------------
  * Pointers   All data pointers are CUDA device pointers (or managed memory)
  *            owned by the caller.  The library allocates no memory, keeps no
  *            per-call state and never frees anything.
@@ -128,6 +128,57 @@ mrn_status mrn_norm_residual_norm(const void *block_out, const void *residual,
                                   float eps_post, float eps_pre,
                                   mrn_dtype dtype, cudaStream_t stream);
 
+/*
+ * Residual add, then RMSNorm of the sum, in one kernel (Hesper "RMSNorm Layer",
+ * residualAddRmsNormKernel / forwardResidualAdd; the pre-norm shape: the stream
+ * is updated, then normalised for the next sub-block):
+ *   residual_out[r,j] = a[r,j] + b[r,j]
+ *   normed[r,j]       = residual_out[r,j] * inv(residual_out[r,:]; eps) * gamma[j]
+ *   a, b          [rows x n]  the two summands (stream and sub-block output)
+ *   gamma         [n]
+ *   residual_out  [rows x n]  the sum; may be a or b (in-place accumulate)
+ *   normed        [rows x n]  may be a or b, never overlapping residual_out
+ * bf16: the sum is rounded once to bf16, stored, and that rounded value is
+ * normalised (the same publication boundary as the sandwich's stream).
+ */
+mrn_status mrn_add_rmsnorm(const void *a, const void *b, const void *gamma,
+                           void *residual_out, void *normed,
+                           int64_t rows, int64_t n, float eps,
+                           mrn_dtype dtype, cudaStream_t stream);
+
+/*
+ * Post norm, residual add, then a broadcast scalar (Hesper "RMSNorm Layer",
+ * rmsNormThenAddThenBroadcastScaleKernel; a per-layer output scale):
+ *   out[r,j] = (x[r,j] * inv(x[r,:]; eps) * gamma[j] + residual[r,j]) * out_scale[0]
+ *   out_scale  one element of `dtype` in device memory, read by the kernel
+ *   out        [rows x n]  may be x or residual; must not overlap out_scale
+ * Arithmetic: fma(x * inv, gamma, residual) in f32, times out_scale, rounded
+ * once to the output type.
+ */
+mrn_status mrn_rmsnorm_then_add_scale(const void *x, const void *gamma, const void *residual,
+                                      const void *out_scale, void *out,
+                                      int64_t rows, int64_t n, float eps,
+                                      mrn_dtype dtype, cudaStream_t stream);
+
+/*
+ * RMSNorm fused with Q8_1 block quantisation (Hesper "RMSNorm Layer",
+ * fusedRMSNormQ8_1Kernel: the norm's output goes straight to the quantised
+ * input of the next matvec, with no f32 round trip through memory):
+ *   x_normed[j] = x[r,j] * gamma[j] * inv(x[r,:]; eps)            (f32)
+ *   per block of 32 consecutive elements of a row:
+ *     d = max |x_normed| / 127,  q = round(x_normed / d)  (nearest, ties to
+ *     even; clamped to [-128, 127]; q = 0 and d = 0 for an all-zero block)
+ *   x       [rows x n]  f32 or bf16 (dtype); n must be a multiple of 32
+ *   gamma   [n]         same dtype
+ *   blocks  [rows x n/32] blocks of 36 bytes: f16 d (bytes 0-1), f16 s = 0
+ *           (bytes 2-3; unused by the page's consumer), int8 q[32]
+ *           (bytes 4-35); 4-byte aligned; must not overlap x or gamma
+ * n % 32 != 0 gives MRN_ERR_INVALID_SIZE.
+ */
+mrn_status mrn_rmsnorm_q8_1(const void *x, const void *gamma, void *blocks,
+                            int64_t rows, int64_t n, float eps,
+                            mrn_dtype dtype, cudaStream_t stream);
+
 /* Static, human-readable name of a status code; never NULL. */
 const char *mrn_status_string(mrn_status status);
 
@@ -143,7 +194,10 @@ int mrn_last_cuda_error(void);
 typedef enum mrn_op {
     MRN_OP_RMSNORM = 0,
     MRN_OP_THEN_ADD = 1,
-    MRN_OP_SANDWICH = 2
+    MRN_OP_SANDWICH = 2,
+    MRN_OP_ADD_RMSNORM = 3,
+    MRN_OP_THEN_ADD_SCALE = 4,
+    MRN_OP_RMSNORM_Q8_1 = 5
 } mrn_op;
 
 typedef enum mrn_geometry_kind {
@@ -194,6 +248,23 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry);
 
 /* Number of kernels this library has launched in the process (all threads). */
 uint64_t mrn_launch_count(void);
+
+/*
+ * Launch options of the calling thread's later calls (0 = none, the default).
+ *   MRN_LAUNCH_PDL  programmatic dependent launch: a kernel may be scheduled
+ *                   before the previous kernel on the stream has finished.
+ *                   Every kernel of this library first waits for that
+ *                   previous grid to complete and publish its memory
+ *                   (griddepcontrol.wait), so results are unchanged; the
+ *                   launch latency of a short call overlaps the previous
+ *                   kernel instead of following it.  Useful for decode-size
+ *                   calls in a chain; the previous kernel need not be ours.
+ * Unknown bits give MRN_ERR_INVALID_GEOMETRY.  Not on the pages: a launch
+ * option of this library.
+ */
+#define MRN_LAUNCH_PDL 1u
+mrn_status mrn_set_launch_options(uint32_t options);
+uint32_t mrn_launch_options(void);
 
 /*
  * Number of bounded waits (on the shared-memory copy barriers of the

@@ -356,6 +356,67 @@ def parity_then_add_scale(x, gamma, res, scale, eps, dtype, rows_sample=None,
     return check_bf16(got[sel], want, scale_t, what)
 
 
+Q8_TIE_MARGIN = 5e-3   # codes this close to a rounding tie may differ by one
+
+
+def decode_q8_1(raw):
+    """uint8 [rows, n/32, 36] -> (d f16 bits [rows, n/32], s bits, q int8 [rows, n])."""
+    raw = np.ascontiguousarray(raw)
+    d_bits = raw[:, :, 0:2].copy().view(np.uint16)[:, :, 0]
+    s_bits = raw[:, :, 2:4].copy().view(np.uint16)[:, :, 0]
+    q = raw[:, :, 4:36].copy().view(np.int8).reshape(raw.shape[0], -1)
+    return d_bits, s_bits, q
+
+
+def f16_ulps(a_bits, b_bits):
+    def ordered(b):
+        b = b.astype(np.int64)
+        return np.where(b & 0x8000, -(b & 0x7FFF), b & 0x7FFF)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+def parity_q8_1(x, gamma, eps, dtype, rows_sample=None, what="q8_1", x_offset=0):
+    """RMSNorm + Q8_1 against the oracle: header s == 0, d within one f16 ulp
+    of the oracle's d, codes equal except within Q8_TIE_MARGIN of a tie (one
+    off allowed there: the GPU's f32 norm may land on the other side of a
+    tie), zero blocks exactly zero.  64-byte guard bands around the blocks."""
+    rows, n = x.shape
+    if x_offset:
+        base = to_device(np.concatenate([np.zeros(x_offset, x.dtype), x.ravel()]), dtype)
+        dx = base[x_offset:].view(rows, n)
+    else:
+        dx = to_device(x, dtype)
+    dg = to_device(gamma, dtype)
+    nb = n // 32
+    guard = 64
+    raw = torch.full((rows * nb * 36 + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
+    blocks = raw[guard:guard + rows * nb * 36]
+    st = mrn.mrn_rmsnorm_q8_1(dx.data_ptr(), dg.data_ptr(), blocks.data_ptr(), rows, n, eps,
+                              code(dtype), stream_handle())
+    assert st == 0, f"{what}: status {mrn.STATUS.get(st)}"
+    torch.cuda.synchronize()
+    host = raw.cpu().numpy()
+    assert np.all(host[:guard] == 0xA5) and np.all(host[-guard:] == 0xA5), what + ": guard bands"
+    d_bits, s_bits, q = decode_q8_1(host[guard:-guard].reshape(rows, nb, 36))
+    sel = slice(None) if rows_sample is None else rows_sample
+    d64, qreal, q64 = oracle.rmsnorm_q8_1(widen(x[sel], dtype), widen(gamma, dtype),
+                                          float(np.float32(eps)))
+    assert np.all(s_bits[sel] == 0), what + ": s must be 0"
+    ulps = f16_ulps(d_bits[sel], oracle.f16_from_double(d64))
+    assert ulps.max() <= 1, f"{what}: d off by {ulps.max()} f16 ulps"
+    zero = np.repeat(d64 == 0, 32, axis=1)
+    assert np.all(q[sel][zero] == 0), what + ": zero blocks"
+    margin = np.abs(np.abs(qreal - np.floor(qreal)) - 0.5)
+    diff = np.abs(q[sel].astype(np.int64) - q64.astype(np.int64))
+    near_tie = margin < Q8_TIE_MARGIN
+    bad = (diff > 1) | ((diff == 1) & ~near_tie)
+    if np.any(bad):
+        i = np.flatnonzero(bad.ravel())[:5]
+        raise AssertionError(f"{what}: {bad.sum()} codes differ; got {q[sel].ravel()[i]} "
+                             f"want {q64.ravel()[i]} qreal {qreal.ravel()[i]}")
+    return int(np.sum(diff == 1)), int(near_tie.sum())
+
+
 def sample_rows(rows, count, seed, must=()):
     g = np.random.Generator(np.random.PCG64(seed))
     pick = set(int(v) for v in g.choice(rows, size=min(rows, count), replace=False))

@@ -92,6 +92,17 @@ def test_more_ops_validation():
     assert mrn.mrn_launch_count() == 0
 
 
+def test_q8_1_validation():
+    q8 = mrn.mrn_rmsnorm_q8_1
+    assert q8(A, G, Y, 4, 100, 1e-5, mrn.MRN_F32, 0) == mrn.MRN_ERR_INVALID_SIZE   # n % 32
+    assert q8(A, G, Y + 2, 4, 64, 1e-5, mrn.MRN_F32, 0) == mrn.MRN_ERR_MISALIGNED
+    assert q8(A, G, A + 64, 4, 64, 1e-5, mrn.MRN_F32, 0) == mrn.MRN_ERR_ALIASING
+    assert q8(A, G, G, 4, 64, 1e-5, mrn.MRN_BF16, 0) == mrn.MRN_ERR_ALIASING
+    assert q8(None, None, None, 0, 64, 1e-5, mrn.MRN_F32, 0) == mrn.MRN_OK
+    assert q8(A, None, Y, 4, 64, 1e-5, mrn.MRN_F32, 0) == mrn.MRN_ERR_NULL_POINTER
+    assert mrn.mrn_launch_count() == 0
+
+
 def test_size_validation():
     assert rms(n=0) == mrn.MRN_ERR_INVALID_SIZE
     assert rms(n=-3) == mrn.MRN_ERR_INVALID_SIZE
@@ -155,13 +166,17 @@ def test_geometry_covers_every_row_width():
                   4096, 5120, 6656, 6657, 8192, 16384, 32768, 65536, 131072, 262144, 1 << 20]:
             for rows in (1, 4, 64, 4096, 65536):
                 for a16 in (True, False):
-                    for op in (0, 1, 2, 3, 4):
+                    for op in (0, 1, 2, 3, 4, 5):
+                        if op == 5 and n % 32:
+                            continue
                         g = mrn.mrn_query_geometry(op, rows, n, dt, a16, 152)
                         vec = g["vec"]
                         assert vec == (16 // e if a16 and (n * e) % 16 == 0 else 1)
                         nvec = -(-n // vec)
                         if g["kind"] == mrn.MRN_GEOM_ROWS_PER_WARP:
                             assert g["lanes_per_row"] * g["k"] >= nvec
+                            if op == 5:
+                                assert g["lanes_per_row"] >= 32 // vec
                             assert g["threads"] == 256 and 32 % g["lanes_per_row"] == 0
                         elif g["kind"] == mrn.MRN_GEOM_CTA:
                             assert g["cluster"] * g["threads"] * g["k"] >= nvec
