@@ -511,9 +511,27 @@ def decode_latency(args, dev, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     hot_us = e0.elapsed_time(e1) * 1e3 / (reps * per_graph)
+    # the rotating graph again with programmatic dependent launch
+    mrn.mrn_set_launch_options(mrn.MRN_LAUNCH_PDL)
+    g_pdl = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_pdl, stream=side):
+            for i in range(per_graph):
+                call(i, side.cuda_stream)
+    mrn.mrn_set_launch_options(0)
+    stream.wait_stream(side)
+    g_pdl.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        g_pdl.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    pdl_us = e0.elapsed_time(e1) * 1e3 / (reps * per_graph)
     geometry = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, 1, n, mrn.MRN_F32, True)
     return {"workload": w.name, "us_per_call_stream": stream_us,
             "us_per_call_graph": graph_us, "us_per_call_graph_l2_hot": hot_us,
+            "us_per_call_graph_pdl": pdl_us,
             "bytes_per_call": sandwich_bytes(1, n), "rotating_sets": nsets,
             "geometry": geometry}
 
@@ -567,6 +585,7 @@ def secondary_workloads(dev, stream):
                      "geometry": mrn.mrn_query_geometry(op, rows, n, mrn.MRN_BF16, True)}
     del sets, outs
     torch.cuda.empty_cache()
+    out.update(more_ops(dev, stream))
 
     w = wl.plain_decode_rows()
     nsets = 512
@@ -598,6 +617,78 @@ def secondary_workloads(dev, stream):
     us = e0.elapsed_time(e1) * 1e3 / (reps * nsets)
     out[w.name] = {"us_per_call_graph": us, "bytes_per_call": (2 * w.rows * w.n + w.n) * 4,
                    "geometry": mrn.mrn_query_geometry(0, w.rows, w.n, mrn.MRN_F32, True)}
+    return out
+
+
+def more_ops(dev, stream):
+    """The operations beyond the three of the benchmark spec, timed the same way
+    (GB/s of algorithmic bytes, two rotating buffer sets larger than L2,
+    seeded torch inputs): residual add + norm at the benchmark's width,
+    then-add-scale and RMSNorm + Q8_1 at 16384 x 4096 bf16, and the per-head
+    QK-norm shape (163840 rows of 128, bf16)."""
+    import torch
+
+    from dual_epsilon_sandwich_gb300 import mrn
+    sh = stream.cuda_stream
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20261202)
+    out = {}
+
+    def run(name, op, dtype, rows, n, nbytes, launch):
+        tdt = torch.float32 if dtype == mrn.MRN_F32 else torch.bfloat16
+        sets = []
+        for _ in range(2):
+            x = torch.randn(rows, n, device=dev, generator=gen).to(tdt)
+            r = torch.randn(rows, n, device=dev, generator=gen).to(tdt)
+            g = (1 + 0.1 * torch.randn(n, device=dev, generator=gen)).to(tdt)
+            y = torch.empty_like(x)
+            y2 = torch.empty((rows * (n // 32) * 36 + 16,), dtype=torch.uint8, device=dev) \
+                if op == mrn.MRN_OP_RMSNORM_Q8_1 else torch.empty_like(x)
+            sc = torch.full((1,), 0.5, device=dev).to(tdt)
+            sets.append((x, r, g, y, y2, sc))
+        for i in range(20):
+            launch(sets[i % 2])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        iters = 400
+        e0.record(stream)
+        for i in range(iters):
+            launch(sets[i % 2])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / iters
+        out[name] = {"GB_per_s": nbytes / (us * 1e-6) / 1e9, "us_per_call": us,
+                     "rows_per_s": rows / (us * 1e-6), "bytes_per_call": nbytes,
+                     "geometry": mrn.mrn_query_geometry(op, rows, n, dtype, True)}
+        del sets
+        torch.cuda.empty_cache()
+
+    def check(st, what):
+        if st != 0:
+            raise mrn.MrnError(st, what)
+
+    F, B = mrn.MRN_F32, mrn.MRN_BF16
+    rows, n = 4096, 6656
+    run("add_rmsnorm_f32_rows4096_n6656", mrn.MRN_OP_ADD_RMSNORM, F, rows, n,
+        (4 * rows * n + n) * 4,
+        lambda t: check(mrn.mrn_add_rmsnorm(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(),
+                                            t[3].data_ptr(), t[4].data_ptr(), rows, n, 1e-5, F,
+                                            sh), "add_rmsnorm"))
+    rows, n = 16384, 4096
+    run("then_add_scale_bf16_rows16384_n4096", mrn.MRN_OP_THEN_ADD_SCALE, B, rows, n,
+        (3 * rows * n + n + 1) * 2,
+        lambda t: check(mrn.mrn_rmsnorm_then_add_scale(t[0].data_ptr(), t[2].data_ptr(),
+                                                       t[1].data_ptr(), t[5].data_ptr(),
+                                                       t[3].data_ptr(), rows, n, 1e-6, B, sh),
+                        "then_add_scale"))
+    run("rmsnorm_q8_1_bf16_rows16384_n4096", mrn.MRN_OP_RMSNORM_Q8_1, B, rows, n,
+        (rows * n + n) * 2 + rows * (n // 32) * 36,
+        lambda t: check(mrn.mrn_rmsnorm_q8_1(t[0].data_ptr(), t[2].data_ptr(), t[4].data_ptr(),
+                                             rows, n, 1e-6, B, sh), "q8_1"))
+    rows, n = 163840, 128
+    run("qk_norm_bf16_rows163840_n128", mrn.MRN_OP_RMSNORM, B, rows, n, (2 * rows * n + n) * 2,
+        lambda t: check(mrn.mrn_rmsnorm(t[0].data_ptr(), t[2].data_ptr(), t[3].data_ptr(), rows,
+                                        n, 1e-6, B, sh), "qk_norm"))
     return out
 
 
