@@ -13,7 +13,8 @@ function cites the passage it follows in ``oracle.c`` / ``oracle.h``:
 "Chapter 12 -- RMSNorm and the dual-epsilon sandwich" (sections 12.1, 12.3,
 12.4.3, 12.4.4) and the Hesper "RMSNorm Layer" API page (rmsNormThenAddKernel,
 rmsNormThenAddThenBroadcastScaleKernel, residualAddRmsNormKernel,
-fusedRMSNormQ8_1Kernel).
+fusedRMSNormQ8_1Kernel), and section 12.7's cross-vendor seam (the weightless
+norm stored in F16, the weight applied as a second F16 operation).
 
 ctypes releases the GIL during a foreign call, so callers may run disjoint row
 blocks on several threads (the oracle itself stays single-threaded code).
@@ -95,6 +96,9 @@ class Oracle:
         lib.oracle_rmsnorm_q8_1.argtypes = [_f64p, _f64p, _i64, _i64, ctypes.c_double, _f64p,
                                             _f64p, ctypes.POINTER(ctypes.c_int8)]
         lib.oracle_rmsnorm_q8_1.restype = None
+        lib.oracle_rmsnorm_seam.argtypes = [_f64p, _f64p, _f64p, _f64p, _i64, _i64,
+                                             ctypes.c_double, ctypes.c_int]
+        lib.oracle_rmsnorm_seam.restype = None
         lib.oracle_q8_round.argtypes = [ctypes.c_double]
         lib.oracle_q8_round.restype = ctypes.c_int
         lib.oracle_f16_from_double.argtypes = [ctypes.c_double]
@@ -196,6 +200,21 @@ class Oracle:
                                      _ptr(qreal), q.ctypes.data_as(ctypes.POINTER(ctypes.c_int8)))
         return d, qreal, q
 
+    def rmsnorm_seam(self, x, gamma, eps: float, seam: str = "f16"):
+        """Split-norm seam (Chapter 12, section 12.7): u = T(x * inv_rms),
+        y = T(u * gamma), T = binary16 ("f16") or bf16 ("bf16"); gamma holds
+        values of T.  Returns (u, y), exact values of T patterns, as f64."""
+        assert seam in ("f16", "bf16")
+        x = _as_f64(x)
+        g = _as_f64(gamma)
+        rows, n = _shape2(x)
+        assert g.shape == (n,)
+        u = np.empty((rows, n), dtype=np.float64)
+        y = np.empty((rows, n), dtype=np.float64)
+        self.lib.oracle_rmsnorm_seam(_ptr(x), _ptr(g), _ptr(u), _ptr(y), rows, n, float(eps),
+                                     1 if seam == "bf16" else 0)
+        return u, y
+
     def q8_round(self, qreal: float) -> int:
         return self.lib.oracle_q8_round(float(qreal))
 
@@ -264,6 +283,10 @@ def rmsnorm_then_add_scale(x, gamma, residual, out_scale, eps):
 
 def rmsnorm_q8_1(x, gamma, eps):
     return default().rmsnorm_q8_1(x, gamma, eps)
+
+
+def rmsnorm_seam(x, gamma, eps, seam="f16"):
+    return default().rmsnorm_seam(x, gamma, eps, seam)
 
 
 def f16_from_double(v):

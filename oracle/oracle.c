@@ -153,6 +153,31 @@ void oracle_rmsnorm_q8_1(const double *x, const double *gamma, int64_t rows, int
     }
 }
 
+/* value of the nearest T (binary16 or bf16) to v */
+static double round_to_seam(double v, int seam_bf16)
+{
+    if (seam_bf16)
+        return oracle_double_from_bf16(oracle_bf16_from_double(v));
+    return oracle_double_from_f16(oracle_f16_from_double(v));
+}
+
+void oracle_rmsnorm_seam(const double *x, const double *gamma, double *u, double *y,
+                         int64_t rows, int64_t n, double eps, int seam_bf16)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *xr = x + r * n;
+        double *ur = u + r * n;
+        double *yr = y + r * n;
+        double inv_rms = row_inv_rms(xr, n, eps);
+        /* first operation: the weightless norm, published in T */
+        for (int64_t j = 0; j < n; ++j)
+            ur[j] = round_to_seam(xr[j] * inv_rms, seam_bf16);
+        /* second operation: the weight multiply, rounded to T again */
+        for (int64_t j = 0; j < n; ++j)
+            yr[j] = round_to_seam(ur[j] * gamma[j], seam_bf16);
+    }
+}
+
 /*
  * binary16: normal numbers (1 + f/1024) * 2^(e-15), e in 1..30; subnormals
  * f * 2^-24; e = 31 holds infinities and NaNs.  Same rounding rule as bf16.

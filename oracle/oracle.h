@@ -11,7 +11,9 @@
  *   [P1] "Chapter 12 -- RMSNorm and the dual-epsilon sandwich", section 12.1
  *        (definition), 12.3 (worked example), 12.4.3 (the dual-eps tail:
  *        hidden += rms_norm(src, eps1) * w1; output = rms_norm(hidden, eps2) * w2),
- *        12.4.4 (the split route's f32 publication boundary between the norms).
+ *        12.4.4 (the split route's f32 publication boundary between the norms),
+ *        12.7 (the cross-vendor seam: the weightless norm materialised in F16,
+ *        the learned-weight multiply applied as a second F16 operation).
  *   [P4] "RMSNorm Layer - Root Mean Square Normalization" (Hesper API docs),
  *        rmsNormThenAddKernel / rmsNormThenAddBatchKernel:
  *        output = RMSNorm(layer_out) * scale + residual;
@@ -96,6 +98,20 @@ void oracle_rmsnorm_q8_1(const double *x, const double *gamma, int64_t rows, int
                          double eps, double *d, double *qreal, int8_t *q);
 /* The code of one quotient: nearest integer, ties to even, clamped to int8. */
 int oracle_q8_round(double qreal);
+
+/*
+ * Split-norm seam: the rounding point between the weightless norm and the
+ * weight multiply kept                                   [P1 12.7, cross-vendor seam]
+ *   u[r,j] = round_T(x[r,j] * inv_rms(x[r,:]; eps))     weightless norm, stored in T
+ *   y[r,j] = round_T(u[r,j] * gamma[j])                  weight multiply as a T operation
+ * T is IEEE binary16 when seam_bf16 == 0, bf16 otherwise; round_T is round to
+ * nearest, ties to even.  gamma holds values of T (the caller widens the
+ * patterns).  u and y receive the exact values of their T patterns.  The
+ * product u * gamma of two T values is exact in double, so y is the
+ * correctly rounded T product.
+ */
+void oracle_rmsnorm_seam(const double *x, const double *gamma, double *u, double *y,
+                         int64_t rows, int64_t n, double eps, int seam_bf16);
 
 /* IEEE binary16 (1 sign, 5 exponent, 10 fraction bits): round a double to the
  * nearest (ties to even), and widen a pattern exactly. */

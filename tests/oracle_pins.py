@@ -14,7 +14,9 @@ oracle disagrees with:
   rows (the identity mean(x^2) = sigma^2 + mu^2 of section 12.2);
 * exact rational / 50-digit decimal arithmetic on tiny inputs;
 * structural invariants (row and column permutations);
-* torch's float32 -> bfloat16 conversion for the bf16 rounding routine.
+* torch's float32 -> bfloat16 conversion for the bf16 rounding routine;
+* numpy's float64 -> float16 cast (correctly rounded, ties to even) and exact
+  rational rounding for the split-norm seam of section 12.7.
 
 ``ALL_CHECKS`` lists them; the mutation test runs every check against each
 planted mistake and expects at least one to fail.
@@ -507,6 +509,140 @@ def check_bf16_sandwich_stream(orc):
     assert not np.array_equal(s32, s), "rounding must change the stream"
 
 
+# ---------------------------------------------------------------------------
+# Split-norm seam (section 12.7): u = T(x * inv), y = T(u * gamma)
+# ---------------------------------------------------------------------------
+def _nearest_in_format(v: Fraction, frac_bits: int, min_exp: int, max_exp: int) -> Fraction:
+    """Exact nearest value (ties to even) of a binary format with `frac_bits`
+    fraction bits, normal exponents [min_exp, max_exp] and gradual underflow;
+    beyond the largest finite value by half a unit, infinity (as None)."""
+    if v == 0:
+        return Fraction(0)
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, min_exp)
+    quantum = Fraction(2) ** (e - frac_bits)
+    k, rem = divmod(a, quantum)
+    if rem * 2 > quantum or (rem * 2 == quantum and k % 2 == 1):
+        k += 1
+    r = k * quantum
+    if r >= Fraction(2) ** (max_exp + 1):
+        return None
+    return r if v > 0 else -r
+
+
+def _exact_seam(x_row, gamma, eps, frac_bits, min_exp, max_exp):
+    """u and y of one row by exact rationals and a 60-digit square root."""
+    getcontext().prec = 60
+    inv = _decimal_inv_rms(x_row, eps)
+    u, y = [], []
+    for xj, gj in zip(x_row, gamma):
+        p = Fraction(Decimal(xj) * inv)
+        uj = _nearest_in_format(p, frac_bits, min_exp, max_exp)
+        yj = _nearest_in_format(uj * Fraction(gj), frac_bits, min_exp, max_exp)
+        u.append(float(uj))
+        y.append(float(yj) if yj is not None else np.copysign(np.inf, float(uj * Fraction(gj))))
+    return np.array(u), np.array(y)
+
+
+F16_FORMAT = (10, -14, 15)
+BF16_FORMAT = (7, -126, 127)
+
+
+def check_seam_worked_example(orc):
+    """Section 12.3's row x = [3, 4, 0, 0], eps = 1e-5, with the page's shaped
+    gamma [2, 0.5, 1, 1], through the seam.  x * inv = 1.19999904..,
+    1.59999872..; binary16 has spacing 2^-10 on [1, 2), so u = 1229/1024 and
+    1638/1024 (1228.799.. and 1638.398.. units); bf16 has spacing 2^-7, so
+    u = 154/128 and 205/128.  The power-of-two gammas scale u exactly."""
+    g = load_golden("rmsnorm_worked_example.txt")
+    eps = g["eps"][0][0]
+    x = g["x"][0][None, :]
+    gamma = g["gamma_shaped"][0]
+    u, y = orc.rmsnorm_seam(x, gamma, eps, "f16")
+    _assert_close(u[0], [1229 / 1024, 1638 / 1024, 0, 0], 0.0, "f16 seam u")
+    _assert_close(y[0], [2 * 1229 / 1024, 0.5 * 1638 / 1024, 0, 0], 0.0, "f16 seam y")
+    u, y = orc.rmsnorm_seam(x, gamma, eps, "bf16")
+    _assert_close(u[0], [154 / 128, 205 / 128, 0, 0], 0.0, "bf16 seam u")
+    _assert_close(y[0], [2 * 154 / 128, 0.5 * 205 / 128, 0, 0], 0.0, "bf16 seam y")
+
+
+def check_seam_exact_small(orc):
+    """n <= 8 rows (f32-valued x, T-valued gamma, some products in the T
+    subnormal range and some beyond its largest value) against exact rational
+    rounding of the exact norm."""
+    g = _rng(41)
+    for seam, fmt in (("f16", F16_FORMAT), ("bf16", BF16_FORMAT)):
+        for n in range(1, 9):
+            x = g.standard_normal((3, n)).astype(np.float32).astype(np.float64)
+            x[1] *= 1e-3
+            gamma = 1.0 + 0.3 * g.standard_normal(n)
+            if seam == "f16":
+                gamma[0] = 3e4 if n > 2 else gamma[0]        # may overflow binary16
+                gamma[-1] *= 1e-6                             # binary16 subnormal products
+                gamma = gamma.astype(np.float16).astype(np.float64)
+            else:
+                gamma[-1] *= 1e-39
+                gamma = orc.double_from_bf16(orc.bf16_from_double(gamma))
+            u, y = orc.rmsnorm_seam(x, gamma, 1e-5, seam)
+            for r in range(3):
+                wu, wy = _exact_seam(x[r], gamma, 1e-5, *fmt)
+                assert np.array_equal(u[r], wu), f"{seam} exact u n={n}: {u[r]} vs {wu}"
+                assert np.array_equal(y[r], wy), f"{seam} exact y n={n}: {y[r]} vs {wy}"
+
+
+def check_seam_against_numpy_f16(orc):
+    """binary16 seam against torch's float64 rms_norm (gamma = 1) and numpy's
+    float64 -> float16 cast, element by element; elements whose x * inv lies
+    within 1e-12 of a rounding tie are left to the exact check."""
+    g = _rng(42)
+    rows, n = 8, 1000
+    x = (g.standard_normal((rows, n)) * 10.0 ** g.uniform(-3, 3, size=(rows, 1)))
+    x = x.astype(np.float32).astype(np.float64)
+    gamma = (1.0 + 0.1 * g.standard_normal(n)).astype(np.float16).astype(np.float64)
+    gamma[:50] = (g.standard_normal(50) * 1e-5).astype(np.float16)   # subnormal products
+    u, y = orc.rmsnorm_seam(x, gamma, 1e-6, "f16")
+    p = _torch_rms(x, np.ones(n), 1e-6)
+    wu = p.astype(np.float16).astype(np.float64)
+    wy = (wu * gamma).astype(np.float16).astype(np.float64)
+    lo = np.nextafter(p.astype(np.float16), np.float16(-np.inf)).astype(np.float64)
+    hi = np.nextafter(p.astype(np.float16), np.float16(np.inf)).astype(np.float64)
+    mid_gap = np.minimum(np.abs(p - (wu + lo) / 2), np.abs(p - (wu + hi) / 2))
+    safe = mid_gap > 1e-12 * np.abs(p)
+    assert safe.mean() > 0.99
+    assert np.array_equal(u[safe], wu[safe]), "u = float16(x * inv)"
+    assert np.array_equal(y[safe], wy[safe]), "y = float16(u * gamma)"
+
+
+def check_seam_rounding_point(orc):
+    """The seam keeps its intermediate rounding: gamma = 1 gives y = u; a
+    power-of-two gamma scales u exactly; a general gamma gives results that
+    differ from a single rounding of x * inv * gamma for some elements, each
+    within two units of the last place of y."""
+    g = _rng(43)
+    rows, n = 4, 4096
+    x = g.standard_normal((rows, n))
+    for seam in ("f16", "bf16"):
+        u1, y1 = orc.rmsnorm_seam(x, np.ones(n), 1e-5, seam)
+        assert np.array_equal(y1, u1), f"{seam}: gamma = 1"
+        u4, y4 = orc.rmsnorm_seam(x, np.full(n, 4.0), 1e-5, seam)   # |4u| << max, exact
+        assert np.array_equal(u4, u1) and np.array_equal(y4, 4.0 * u1), f"{seam}: gamma = 4"
+        gamma = 1.0 + 0.1 * g.standard_normal(n)
+        gamma = (gamma.astype(np.float16).astype(np.float64) if seam == "f16"
+                 else orc.double_from_bf16(orc.bf16_from_double(gamma)))
+        u, y = orc.rmsnorm_seam(x, gamma, 1e-5, seam)
+        one = orc.rmsnorm(x, gamma, 1e-5)
+        one_t = (one.astype(np.float16).astype(np.float64) if seam == "f16"
+                 else orc.double_from_bf16(orc.bf16_from_double(one)))
+        assert np.array_equal(u, u1), f"{seam}: u does not depend on gamma"
+        assert np.sum(y != one_t) > 0, f"{seam}: the intermediate rounding must show"
+        bits = 10 if seam == "f16" else 7
+        ulp = 2.0 ** (np.floor(np.log2(np.abs(one_t))) - bits)
+        _assert_close(y, one, 2 * ulp, f"{seam}: within two units of one rounding")
+
+
 ALL_CHECKS = [
     check_worked_example,
     check_constant_rows,
@@ -531,4 +667,8 @@ ALL_CHECKS = [
     check_bf16_widen_all_patterns,
     check_bf16_round_against_torch,
     check_bf16_sandwich_stream,
+    check_seam_worked_example,
+    check_seam_exact_small,
+    check_seam_against_numpy_f16,
+    check_seam_rounding_point,
 ]

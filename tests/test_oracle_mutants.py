@@ -71,6 +71,19 @@ MUTANTS = [
     ("bf16 no carry into next binade", "if (q == 256) {", "if (0) {"),
     ("bf16 widening exponent bias", "field - 127 - 7", "field - 127 - 8"),
     ("bf16 NaN as infinity", "v = frac ? NAN : INFINITY;", "v = INFINITY;"),
+    ("seam: intermediate rounding skipped", "ur[j] = round_to_seam(xr[j] * inv_rms, seam_bf16);",
+     "ur[j] = xr[j] * inv_rms;"),
+    ("seam: second rounding skipped", "yr[j] = round_to_seam(ur[j] * gamma[j], seam_bf16);",
+     "yr[j] = ur[j] * gamma[j];"),
+    ("seam: gamma dropped", "yr[j] = round_to_seam(ur[j] * gamma[j], seam_bf16);",
+     "yr[j] = round_to_seam(ur[j], seam_bf16);"),
+    ("seam: weight on the unrounded product", "yr[j] = round_to_seam(ur[j] * gamma[j], seam_bf16);",
+     "yr[j] = round_to_seam(xr[j] * inv_rms * gamma[j], seam_bf16);"),
+    ("seam: formats swapped", "    if (seam_bf16)\n        return oracle_double_from_bf16",
+     "    if (!seam_bf16)\n        return oracle_double_from_bf16"),
+    ("seam: u row offset lost", "double *ur = u + r * n;", "double *ur = u;"),
+    ("seam: eps dropped in the seam's norm", "double inv_rms = row_inv_rms(xr, n, eps);\n        /* first operation",
+     "double inv_rms = row_inv_rms(xr, n, 0.0);\n        /* first operation"),
 ]
 
 
