@@ -22,7 +22,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "-I", INCLUDE, "-I", CSRC]
 SOURCES = ["mrn_api.cpp", "mrn_ops_rmsnorm.cu", "mrn_ops_then_add.cu", "mrn_ops_sandwich.cu",
-           "mrn_ops_add_rmsnorm.cu", "mrn_ops_then_add_scale.cu", "mrn_ops_rmsnorm_q8_1.cu"]
+           "mrn_ops_add_rmsnorm.cu", "mrn_ops_then_add_scale.cu", "mrn_ops_rmsnorm_q8_1.cu",
+           "mrn_ops_seam_f16.cu", "mrn_ops_seam_bf16.cu", "mrn_seam_scale.cu"]
 
 
 def nvcc() -> str:

@@ -6,9 +6,12 @@
 // Layer", rmsNormThenAddKernel), the dual-epsilon sandwich tail (section
 // 12.4.3), residual add then norm (Hesper residualAddRmsNormKernel), post
 // norm, add, broadcast scale (Hesper rmsNormThenAddThenBroadcastScaleKernel)
-// and RMSNorm with Q8_1 quantisation (Hesper fusedRMSNormQ8_1Kernel).  This layer holds no arithmetic of the method; it checks
-// arguments, picks a register geometry from (n, rows, dtype, alignment) and
-// hands the call to the launcher of the operation.
+// RMSNorm with Q8_1 quantisation (Hesper fusedRMSNormQ8_1Kernel) and the
+// split-norm seam (section 12.7: the weightless norm published in F16 or
+// bf16, the weight applied as a second operation in that format).  This layer
+// holds no arithmetic of the method; it checks arguments, picks a register
+// geometry from (n, rows, dtype, alignment) and hands the call to the
+// launcher of the operation.
 #include "mrn.h"
 
 #include <algorithm>
@@ -94,14 +97,16 @@ void pick_threads(int64_t per, int *k_out, int *t_out, int (*max_threads)(int) =
 int tma_group_cap(int k) { return mrn::tma_group_max_threads(k); }
 
 // For batches in the register kernel: among (k, t) with at most 1/8 of the
-// slots idle, the one with t nearest 256 (measured best on GB300 for the
-// residual add + norm: 7 x 256 at n = 6656 f32, 2 x 256 at n = 4096 bf16).
-void pick_threads_batch(int64_t per, int *k_out, int *t_out) {
+// slots idle, the one with t nearest `target` (measured best on GB300: 256
+// for the residual add + norm, 7 x 256 at n = 6656 f32; 128 for the Q8_1
+// pass, 4 x 128 at n = 4096 bf16, whose more registers per slot want fewer
+// threads per CTA).
+void pick_threads_batch(int64_t per, int *k_out, int *t_out, double target) {
     double best = 1e30;
     for (int k = 1; k <= mrn::kMaxK; ++k) {
         const int64_t t = ceil_div(ceil_div(per, k), 32) * 32;
         if (t > mrn::cta_max_threads(k) || (t * k - per) * 8 > per) continue;
-        const double d = std::fabs(std::log2(static_cast<double>(t) / 256.0));
+        const double d = std::fabs(std::log2(static_cast<double>(t) / target));
         if (d < best) {
             best = d;
             *k_out = k;
@@ -154,7 +159,8 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     // Q8_1 pass has more arithmetic per byte; both run faster in the register
     // kernel with many CTAs per SM than in the staged one (measured on GB300:
     // add+norm 6.45 vs 6.03 TB/s at 4096 x 6656 f32).
-    const bool staged_pays = op != mrn::kAddRmsnorm && op != mrn::kRmsnormQ8;
+    const bool staged_pays = op != mrn::kAddRmsnorm && op != mrn::kRmsnormQ8 &&
+                             !mrn::op_is_seam(op);   // (the seam has no staged kernel)
     if (staged_pays && aligned16 && rows >= sms && nvec <= 2 * 1024) {
         const int stages = 2;
         if (mrn::tma_shared_bytes(op, row_bytes, stages) <= kTmaSharedBudget) {
@@ -188,7 +194,8 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
         cl = std::max(cl, std::min<int64_t>(8, std::min(by_rows, by_width)));
     }
     if (!staged_pays && rows >= sms) {
-        pick_threads_batch(ceil_div(nvec, cl), &g.k, &g.threads);
+        pick_threads_batch(ceil_div(nvec, cl), &g.k, &g.threads,
+                           op == mrn::kRmsnormQ8 ? 128.0 : 256.0);
     } else {
         pick_threads(ceil_div(nvec, cl), &g.k, &g.threads);
     }
@@ -231,6 +238,7 @@ bool resolve_forced(Geometry g, mrn::Op op, int64_t n, mrn_dtype dt, bool aligne
     if (g.vec != 1 && !(g.vec == natural_vec(dt) && aligned16)) return false;
     const int64_t nvec = ceil_div(n, g.vec);
     if (g.kind == mrn::kTma) {
+        if (mrn::op_is_seam(op)) return false;   // no staged kernel for the seam
         if (!aligned16 || g.vec != natural_vec(dt)) return false;
         if (static_cast<int64_t>(g.threads / g.groups) * g.k < nvec) return false;
         if (mrn::tma_shared_bytes(op, n * elem_bytes(dt), g.stages) > kTmaSharedBudget)
@@ -318,7 +326,14 @@ mrn_status launch(const Call &c, bool aligned16, cudaStream_t stream) {
     case mrn::kThenAddScale:
         err = mrn::launch_then_add_scale(bf16, g, a, c.rows, stream, &launched);
         break;
-    default: err = mrn::launch_rmsnorm_q8_1(bf16, g, a, c.rows, stream, &launched); break;
+    case mrn::kRmsnormQ8:
+        err = mrn::launch_rmsnorm_q8_1(bf16, g, a, c.rows, stream, &launched);
+        break;
+    default:
+        err = mrn::op_seam_bf16(c.op)
+                  ? mrn::launch_seam_bf16(c.op, bf16, g, a, c.rows, stream, &launched)
+                  : mrn::launch_seam_f16(c.op, bf16, g, a, c.rows, stream, &launched);
+        break;
     }
     g_launch_count.fetch_add(launched, std::memory_order_relaxed);
     if (err != cudaSuccess) {
@@ -327,6 +342,37 @@ mrn_status launch(const Call &c, bool aligned16, cudaStream_t stream) {
         return MRN_ERR_CUDA;
     }
     return MRN_OK;
+}
+
+// The seam norms: the fused form (weighted) and the split route's weightless
+// first operation.  x is f32 or bf16; the output (and gamma) hold 16-bit
+// values of `seam`.  The output may be x itself only when x also holds 16-bit
+// elements, so that element (r, j) of both sits at the same address.
+mrn_status seam_norm(bool weighted, const void *x, const void *gamma, void *y, int64_t rows,
+                     int64_t n, float eps, mrn_dtype dtype, mrn_dtype seam, cudaStream_t stream) {
+    mrn_status st = check_common(rows, n, dtype, eps, eps);
+    if (st != MRN_OK) return st;
+    if (seam != MRN_F16 && seam != MRN_BF16) return MRN_ERR_UNSUPPORTED_DTYPE;
+    if (rows == 0) return MRN_OK;
+    if (!x || !y || (weighted && !gamma)) return MRN_ERR_NULL_POINTER;
+    const int64_t e = elem_bytes(dtype);
+    if (!aligned_to(x, e) || !aligned_to(y, 2) || (weighted && !aligned_to(gamma, 2)))
+        return MRN_ERR_MISALIGNED;
+    const Span sx = span_of(x, rows * n * e), sy = span_of(y, rows * n * 2);
+    if (e == 2 ? !output_vs_row_input_ok(sy, sx) : overlaps(sy, sx)) return MRN_ERR_ALIASING;
+    if (weighted && overlaps(sy, span_of(gamma, n * 2))) return MRN_ERR_ALIASING;
+    const bool a16 = (n * e) % 16 == 0 && aligned_to(x, 16) && aligned_to(y, 16) &&
+                     (!weighted || aligned_to(gamma, 16));
+    const bool bf = seam == MRN_BF16;
+    const mrn::Op op = weighted ? (bf ? mrn::kSeamBF16 : mrn::kSeamF16)
+                                : (bf ? mrn::kUnweightedBF16 : mrn::kUnweightedF16);
+    Call c{op, dtype, rows, n, KernelArgs{}};
+    c.args.x = x;
+    c.args.g1 = gamma;
+    c.args.y = y;
+    c.args.eps1 = eps;
+    c.args.eps2 = eps;
+    return launch(c, a16, stream);
 }
 
 }  // namespace
@@ -505,6 +551,42 @@ mrn_status mrn_rmsnorm_q8_1(const void *x, const void *gamma, void *blocks, int6
     return launch(c, a16, stream);
 }
 
+mrn_status mrn_rmsnorm_seam(const void *x, const void *gamma, void *y, int64_t rows, int64_t n,
+                            float eps, mrn_dtype dtype, mrn_dtype seam, cudaStream_t stream) {
+    return seam_norm(true, x, gamma, y, rows, n, eps, dtype, seam, stream);
+}
+
+mrn_status mrn_rmsnorm_unweighted(const void *x, void *u, int64_t rows, int64_t n, float eps,
+                                  mrn_dtype dtype, mrn_dtype seam, cudaStream_t stream) {
+    return seam_norm(false, x, nullptr, u, rows, n, eps, dtype, seam, stream);
+}
+
+mrn_status mrn_seam_scale(const void *u, const void *gamma, void *y, int64_t rows, int64_t n,
+                          mrn_dtype seam, cudaStream_t stream) {
+    if (seam != MRN_F16 && seam != MRN_BF16) return MRN_ERR_UNSUPPORTED_DTYPE;
+    if (n < 1 || rows < 0) return MRN_ERR_INVALID_SIZE;
+    if (n > INT64_MAX / 2 || (rows > 0 && rows > INT64_MAX / (n * 2))) return MRN_ERR_INVALID_SIZE;
+    if (rows == 0) return MRN_OK;
+    if (!u || !gamma || !y) return MRN_ERR_NULL_POINTER;
+    if (!aligned_to(u, 2) || !aligned_to(gamma, 2) || !aligned_to(y, 2)) return MRN_ERR_MISALIGNED;
+    const Span su = span_of(u, rows * n * 2), sg = span_of(gamma, n * 2);
+    const Span sy = span_of(y, rows * n * 2);
+    if (!output_vs_row_input_ok(sy, su) || overlaps(sy, sg)) return MRN_ERR_ALIASING;
+    const bool a16 = (n * 2) % 16 == 0 && aligned_to(u, 16) && aligned_to(gamma, 16) &&
+                     aligned_to(y, 16);
+    uint64_t launched = 0;
+    const cudaError_t err = mrn::launch_seam_scale(
+        seam == MRN_BF16, u, gamma, y, rows, n, a16 ? 8 : 1, sm_count_of_current_device(),
+        (t_launch_options & MRN_LAUNCH_PDL) != 0, stream, &launched);
+    g_launch_count.fetch_add(launched, std::memory_order_relaxed);
+    if (err != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(err);
+        (void)cudaGetLastError();
+        return MRN_ERR_CUDA;
+    }
+    return MRN_OK;
+}
+
 const char *mrn_status_string(mrn_status status) {
     switch (status) {
     case MRN_OK: return "ok";
@@ -526,16 +608,20 @@ int mrn_last_cuda_error(void) { return t_last_cuda_error; }
 mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtype,
                               int32_t aligned16, int32_t sm_count, mrn_geometry *out) {
     if (!out) return MRN_ERR_NULL_POINTER;
-    if (op < MRN_OP_RMSNORM || op > MRN_OP_RMSNORM_Q8_1) return MRN_ERR_INVALID_GEOMETRY;
+    if (op < MRN_OP_RMSNORM || op > MRN_OP_RMSNORM_UNWEIGHTED) return MRN_ERR_INVALID_GEOMETRY;
     mrn_status st = check_common(rows, n, dtype, 1.0f, 1.0f);
     if (st != MRN_OK) return st;
     const bool a16 = aligned16 != 0 && (n * elem_bytes(dtype)) % 16 == 0;
+    // (the seam's geometry does not depend on its 16-bit format)
+    const mrn::Op iop = op == MRN_OP_RMSNORM_SEAM         ? mrn::kSeamF16
+                        : op == MRN_OP_RMSNORM_UNWEIGHTED ? mrn::kUnweightedF16
+                                                          : static_cast<mrn::Op>(op);
     Geometry g;
     if (t_forced) {
-        if (!resolve_forced(t_forced_geometry, static_cast<mrn::Op>(op), n, dtype, a16, &g))
+        if (!resolve_forced(t_forced_geometry, iop, n, dtype, a16, &g))
             return MRN_ERR_INVALID_GEOMETRY;
     } else {
-        g = choose_geometry(static_cast<mrn::Op>(op), rows, n, dtype, a16,
+        g = choose_geometry(iop, rows, n, dtype, a16,
                             sm_count > 0 ? sm_count : sm_count_of_current_device());
     }
     out->kind = g.kind;

@@ -21,15 +21,28 @@ enum Op : int {
     kAddRmsnorm = 3,
     kThenAddScale = 4,
     kRmsnormQ8 = 5,   // RMSNorm then Q8_1 blocks: 32 codes + (f16 d, f16 s) per 36 bytes
+    // Split-norm seam: the weightless norm rounded to a 16-bit format S, and
+    // (the weighted forms) the weight multiply as a second S operation.
+    kSeamF16 = 6,          // y = f16(f16(x * inv) * gamma), gamma in f16
+    kSeamBF16 = 7,         // the same with S = bf16
+    kUnweightedF16 = 8,    // u = f16(x * inv): the split route's first operation
+    kUnweightedBF16 = 9,   // the same with S = bf16
 };
 constexpr int kQ8Block = 32;        // elements per Q8_1 block
 constexpr int kQ8BlockBytes = 36;   // f16 d, f16 s, int8 q[32]
 
+// The seam operations (their output and gamma are 16-bit values of S).
+MRN_HOST_DEVICE constexpr bool op_is_seam(int op) { return op >= kSeamF16 && op <= kUnweightedBF16; }
+MRN_HOST_DEVICE constexpr bool op_seam_bf16(int op) { return op == kSeamBF16 || op == kUnweightedBF16; }
+MRN_HOST_DEVICE constexpr bool op_seam_weighted(int op) { return op == kSeamF16 || op == kSeamBF16; }
+
 // Row operands each operation reads, and the gamma vectors it uses.
 MRN_HOST_DEVICE constexpr int op_row_inputs(int op) {
-    return (op == kRmsnorm || op == kRmsnormQ8) ? 1 : 2;
+    return (op == kRmsnorm || op == kRmsnormQ8 || op_is_seam(op)) ? 1 : 2;
 }
-MRN_HOST_DEVICE constexpr int op_gammas(int op) { return op == kSandwich ? 2 : 1; }
+MRN_HOST_DEVICE constexpr int op_gammas(int op) {
+    return op == kSandwich ? 2 : (op == kUnweightedF16 || op == kUnweightedBF16) ? 0 : 1;
+}
 enum Kind : int { kAuto = 0, kRowsPerWarp = 1, kCta = 2, kStream = 3, kTma = 4 };
 
 // Launch-time view of one call.  Pointers are device pointers; row operands
@@ -37,7 +50,8 @@ enum Kind : int { kAuto = 0, kRowsPerWarp = 1, kCta = 2, kStream = 3, kTma = 4 }
 // g1 = gamma_post, g2 = gamma_pre, y = out_stream, y2 = normed.  For the
 // residual add + norm, x = a, res = b, y = residual_out, y2 = normed.  For
 // then-add-scale, scale points at the one broadcast element.  For Q8_1, y
-// points at the output blocks.
+// points at the output blocks.  For the seam operations, y is the 16-bit
+// output (u or y of the seam) and g1 the 16-bit gamma of the weighted forms.
 struct KernelArgs {
     const void *x;
     const void *res;
@@ -97,6 +111,17 @@ cudaError_t launch_then_add_scale(bool bf16, const Geometry &g, const KernelArgs
                                   int64_t rows, cudaStream_t stream, uint64_t *launches);
 cudaError_t launch_rmsnorm_q8_1(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
                                 cudaStream_t stream, uint64_t *launches);
+// The seam operations: op is kSeamF16 or kUnweightedF16 (f16 launcher),
+// kSeamBF16 or kUnweightedBF16 (bf16 launcher); bf16 is the input dtype.
+cudaError_t launch_seam_f16(int op, bool bf16, const Geometry &g, const KernelArgs &a,
+                            int64_t rows, cudaStream_t stream, uint64_t *launches);
+cudaError_t launch_seam_bf16(int op, bool bf16, const Geometry &g, const KernelArgs &a,
+                             int64_t rows, cudaStream_t stream, uint64_t *launches);
+// The split route's second operation: y[r,j] = S(u[r,j] * gamma[j]) over
+// 16-bit values of S; vec is 8 (16-byte aligned rows) or 1.
+cudaError_t launch_seam_scale(bool seam_bf16, const void *u, const void *gamma, void *y,
+                              int64_t rows, int64_t n, int vec, int sms, bool pdl,
+                              cudaStream_t stream, uint64_t *launches);
 
 // Dynamic shared memory of the staged (kTma) kernel for one operation: the
 // gammas once, plus each stage's row operands.

@@ -354,18 +354,28 @@ __device__ __forceinline__ Frag<T, VEC> single_norm_output(const Frag<T, VEC> &x
 // x_normed = (x * gamma) * inv; a 32-element block is held by VPB = 32/VEC
 // consecutive lanes (one register slot each), which agree on the block's
 // amax by a butterfly max; d = amax / 127; q = x_normed / d rounded to
-// nearest, ties to even, clamped to int8 (0 when d == 0).  The quotient is
-// formed as x_normed * (127 / amax) -- one IEEE division per block instead of
-// one per element, which keeps the pass memory-bound; it can differ from
-// x_normed / d only within a few f32 ulps of a rounding tie.  Lane 0 of the
-// block writes the header (f16 d, f16 s = 0), every lane its VEC codes.
-// Every lane of the warp must call this (it shuffles); `valid` only gates
-// the stores.  v is the fragment's index within the row.
+// nearest, ties to even, clamped to int8 (0 when d == 0).
+//
+// The quotient is formed as x_normed * (127 / amax), the reciprocal taken
+// once per block by the approximate divide: it can differ from x_normed / d
+// only within a few f32 ulps of a rounding tie.  Rounding to the nearest integer,
+// ties to even, is one fused multiply-add: fma(x_normed, 127/amax, 1.5 * 2^23)
+// lands in [2^23, 2^24), where the f32 spacing is exactly 1, so the single
+// rounding of the fma is the integer rounding and the low byte of the
+// result's bits is the two's-complement code (|x_normed * 127/amax| <= 127.5
+// by construction, so no clamp is needed on this path).  For an amax outside
+// [2^-100, 2^100] (zero, tiny or huge) the codes fall back to per-element
+// IEEE division and an explicit clamp.  Lane 0 of the block writes the header (f16 d,
+// f16 s = 0), every lane its VEC codes.  Every lane of the warp must call
+// this (it shuffles); `valid` only gates the stores.  v is the fragment's
+// index within the row.
 template <class T, int VEC>
 __device__ __forceinline__ void q8_1_output(const Frag<T, VEC> &x, const Frag<T, VEC> &g,
                                             float inv, bool valid, char *row_blocks,
                                             int64_t v) {
+    static_assert(VEC == 1 || VEC % 4 == 0, "codes are stored one byte or whole words at a time");
     constexpr int VPB = kQ8Block / VEC;
+    constexpr float kRoundShift = 12582912.0f;   // 1.5 * 2^23
     float xn[VEC];
     float amax = 0.0f;
 #pragma unroll
@@ -376,17 +386,37 @@ __device__ __forceinline__ void q8_1_output(const Frag<T, VEC> &x, const Frag<T,
 #pragma unroll
     for (int o = VPB / 2; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
     if (!valid) return;
-    const float d = amax / 127.0f;
-    const float id = amax > 0.0f ? 127.0f / amax : 0.0f;
-    uint32_t packed[(VEC + 3) / 4] = {};
+    uint32_t code[VEC];   // the code in the low byte
+    if (amax >= 0x1p-100f && amax <= 0x1p100f) {
+        // 127/amax by the approximate divide (within 2 ulp for a divisor in
+        // [2^-126, 2^126]); the quotient moves by a few ulps at most.
+        const float id = __fdividef(127.0f, amax);
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-        const int q = min(127, max(-128, __float2int_rn(xn[i] * id)));
-        packed[i / 4] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i % 4));
+        for (int i = 0; i < VEC; ++i) code[i] = __float_as_uint(fmaf(xn[i], id, kRoundShift));
+    } else {
+        const float d = amax / 127.0f;
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            const int q = d > 0.0f ? min(127, max(-128, __float2int_rn(xn[i] / d))) : 0;
+            code[i] = static_cast<uint32_t>(q);
+        }
     }
-    char *block = row_blocks + (v / VPB) * kQ8BlockBytes;
-    const int j = static_cast<int>(v % VPB);
+    uint32_t packed[(VEC + 3) / 4];
+    if (VEC >= 4) {
+#pragma unroll
+        for (int w = 0; w < VEC / 4; ++w) {
+            const uint32_t lo = __byte_perm(code[4 * w], code[4 * w + 1], 0x0040);
+            const uint32_t hi = __byte_perm(code[4 * w + 2], code[4 * w + 3], 0x0040);
+            packed[w] = __byte_perm(lo, hi, 0x5410);
+        }
+    } else {
+        packed[0] = code[0] & 0xFFu;
+    }
+    const uint64_t uv = static_cast<uint64_t>(v);   // v >= 0
+    char *block = row_blocks + (uv / VPB) * kQ8BlockBytes;
+    const int j = static_cast<int>(uv % VPB);
     if (j == 0) {
+        const float d = amax / 127.0f;
         const uint32_t header = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(d)));
         asm volatile("st.global.u32 [%0], %1;" :: "l"(block), "r"(header) : "memory");
     }
@@ -405,6 +435,114 @@ __device__ __forceinline__ void q8_1_output(const Frag<T, VEC> &x, const Frag<T,
 // First byte of a row's Q8_1 blocks.
 __device__ __forceinline__ char *q8_row_blocks(const KernelArgs &a, int64_t row) {
     return static_cast<char *>(a.y) + row * (a.n / kQ8Block) * kQ8BlockBytes;
+}
+
+// ---------------------------------------------------------------------------
+// Split-norm seam ("Chapter 12 -- RMSNorm and the dual-epsilon sandwich",
+// section 12.7, the cross-vendor seam): the weightless norm is published in a
+// 16-bit format S (binary16 or bf16), u = S(x * inv), and the weighted forms
+// apply the weight as a second S operation, y = S(u * gamma) with gamma given
+// in S.  u * gamma multiplies two S values; their product has at most 22
+// significant bits and is exact in f32 (for bf16, unless it falls below
+// 2^-126), so the one rounding to S is the correctly rounded S product.
+// ---------------------------------------------------------------------------
+template <int VEC> struct H16 {   // VEC 16-bit values, two per word (low first)
+    uint32_t w[(VEC + 1) / 2];
+};
+
+template <bool BF> __device__ __forceinline__ uint32_t seam_pack2(float lo, float hi) {
+    if (BF) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+template <bool BF> __device__ __forceinline__ uint32_t seam_pack1(float v) {
+    if (BF) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    return __half_as_ushort(__float2half_rn(v));
+}
+// Exact f32 value of the low / high S value of a word.
+template <bool BF> __device__ __forceinline__ float seam_lo(uint32_t w) {
+    if (BF) return __uint_as_float(w << 16);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+template <bool BF> __device__ __forceinline__ float seam_hi(uint32_t w) {
+    if (BF) return __uint_as_float(w & 0xFFFF0000u);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// gamma of the seam (read-only, cached), the split route's u (streamed), and
+// the 16-bit output.
+__device__ __forceinline__ void ld_h16(H16<8> &f, const void *p) {
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p));
+}
+__device__ __forceinline__ void ld_h16(H16<4> &f, const void *p) {
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(f.w[0]), "=r"(f.w[1]) : "l"(p));
+}
+__device__ __forceinline__ void ld_h16(H16<1> &f, const void *p) {
+    unsigned short h;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(h) : "l"(p));
+    f.w[0] = h;
+}
+__device__ __forceinline__ void ld_stream_h16(H16<8> &f, const void *p) {
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p));
+}
+__device__ __forceinline__ void ld_stream_h16(H16<1> &f, const void *p) {
+    unsigned short h;
+    asm volatile("ld.global.L1::no_allocate.u16 %0, [%1];" : "=h"(h) : "l"(p));
+    f.w[0] = h;
+}
+__device__ __forceinline__ void st_h16(void *p, const H16<8> &f) {
+    asm volatile(MRN_ST_OP ".v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(f.w[0]), "r"(f.w[1]), "r"(f.w[2]), "r"(f.w[3]) : "memory");
+}
+__device__ __forceinline__ void st_h16(void *p, const H16<4> &f) {
+    asm volatile(MRN_ST_OP ".v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(f.w[0]), "r"(f.w[1])
+                 : "memory");
+}
+__device__ __forceinline__ void st_h16(void *p, const H16<1> &f) {
+    const unsigned short h = static_cast<unsigned short>(f.w[0] & 0xFFFFu);
+    asm volatile(MRN_ST_OP ".u16 [%0], %1;" :: "l"(p), "h"(h) : "memory");
+}
+
+// S(u * gamma) of VEC values of S held two per word.
+template <bool BF, int VEC>
+__device__ __forceinline__ H16<VEC> seam_scale_frag(const H16<VEC> &u, const H16<VEC> &g) {
+    H16<VEC> out;
+    if (VEC == 1) {
+        out.w[0] = seam_pack1<BF>(seam_lo<BF>(u.w[0]) * seam_lo<BF>(g.w[0]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i)
+            out.w[i] = seam_pack2<BF>(seam_lo<BF>(u.w[i]) * seam_lo<BF>(g.w[i]),
+                                      seam_hi<BF>(u.w[i]) * seam_hi<BF>(g.w[i]));
+    }
+    return out;
+}
+
+// Seam output of one fragment of x at row-element offset e: u = S(x * inv),
+// and for the weighted forms y = S(u * gamma); 16-bit values stored at y.
+template <int OP, class T, int VEC>
+__device__ __forceinline__ void seam_output(const Frag<T, VEC> &x, float inv, const H16<VEC> &g,
+                                            void *y, int64_t e) {
+    constexpr bool BF = op_seam_bf16(OP);
+    H16<VEC> u;
+    if (VEC == 1) {
+        u.w[0] = seam_pack1<BF>(x.get(0) * inv);
+    } else {
+#pragma unroll
+        for (int i = 0; i < VEC / 2; ++i)
+            u.w[i] = seam_pack2<BF>(x.get(2 * i) * inv, x.get(2 * i + 1) * inv);
+    }
+    void *p = static_cast<char *>(y) + e * 2;
+    if (op_seam_weighted(OP)) {
+        st_h16(p, seam_scale_frag<BF, VEC>(u, g));
+    } else {
+        st_h16(p, u);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -437,9 +575,16 @@ __device__ __forceinline__ void row_body(const KernelArgs &a, int64_t row, bool 
             rv[k].zero();
         }
     }
+    H16<VEC> hg[K];   // the seam's 16-bit gamma
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-        if (ok[k]) ld_ro(gv[k], elem_ptr<T>(a.g1, (first + k * stride) * VEC));
+        if (!ok[k]) continue;
+        const int64_t ge = (first + k * stride) * VEC;
+        if (op_seam_weighted(OP)) {
+            ld_h16(hg[k], static_cast<const char *>(a.g1) + ge * 2);
+        } else if (!op_is_seam(OP)) {
+            ld_ro(gv[k], elem_ptr<T>(a.g1, ge));
+        }
     }
 
     const float sc = load_out_scale<OP, T>(a.scale);
@@ -475,6 +620,15 @@ __device__ __forceinline__ void row_body(const KernelArgs &a, int64_t row, bool 
         for (int k = 0; k < K; ++k) {   // no early exit: every lane shuffles
             if (!ok[k]) gv[k].zero();
             q8_1_output(xv[k], gv[k], inv1, ok[k], blocks, first + k * stride);
+        }
+        return;
+    }
+    if (op_is_seam(OP)) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            if (!ok[k]) continue;
+            const int64_t v = first + k * stride;
+            seam_output<OP, T, VEC>(xv[k], inv1, hg[k], a.y, row_elem + v * VEC);
         }
         return;
     }
@@ -633,6 +787,27 @@ mrn_stream_kernel(const KernelArgs a) {
             for (int u = 0; u < U; ++u) {
                 const int64_t v = v0 + u * nt;
                 q8_1_output(x[u], g[u], inv1, v < a.nvec, blocks, v);
+            }
+        }
+        return;
+    }
+    if (op_is_seam(OP)) {
+        for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
+            Fr x[U];
+            H16<VEC> g[U] = {};
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < a.nvec) {
+                    ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
+                    if (op_seam_weighted(OP))
+                        ld_h16(g[u], static_cast<const char *>(a.g1) + v * VEC * 2);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < a.nvec) seam_output<OP, T, VEC>(x[u], inv1, g[u], a.y, row_elem + v * VEC);
             }
         }
         return;
@@ -1189,6 +1364,19 @@ cudaError_t launch_typed(const Geometry &g, KernelArgs a, int64_t rows, cudaStre
         ++*launches;
     }
     return cudaSuccess;
+}
+
+// Operations without a staged (kTma) kernel: the register and looped kernels.
+template <int OP>
+cudaError_t launch_op_registers(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
+                                cudaStream_t stream, uint64_t *launches) {
+    if (g.kind == kTma) return cudaErrorInvalidConfiguration;
+    if (bf16) {
+        return g.vec == 1 ? launch_typed<OP, BF16, 1>(g, a, rows, stream, launches)
+                          : launch_typed<OP, BF16, 8>(g, a, rows, stream, launches);
+    }
+    return g.vec == 1 ? launch_typed<OP, F32, 1>(g, a, rows, stream, launches)
+                      : launch_typed<OP, F32, 4>(g, a, rows, stream, launches);
 }
 
 template <int OP>

@@ -21,6 +21,7 @@ LIBRARY = os.path.join(PKG, "libmrn.so")
 
 MRN_F32 = 0
 MRN_BF16 = 1
+MRN_F16 = 2      # only as the seam's 16-bit publication format
 
 MRN_OP_RMSNORM = 0
 MRN_OP_THEN_ADD = 1
@@ -28,6 +29,8 @@ MRN_OP_SANDWICH = 2
 MRN_OP_ADD_RMSNORM = 3
 MRN_OP_THEN_ADD_SCALE = 4
 MRN_OP_RMSNORM_Q8_1 = 5
+MRN_OP_RMSNORM_SEAM = 6
+MRN_OP_RMSNORM_UNWEIGHTED = 7
 Q8_1_BLOCK_BYTES = 36
 
 MRN_GEOM_AUTO = 0
@@ -57,7 +60,8 @@ EXPORTS = ("mrn_rmsnorm", "mrn_rmsnorm_then_add", "mrn_norm_residual_norm",
            "mrn_add_rmsnorm", "mrn_rmsnorm_then_add_scale", "mrn_rmsnorm_q8_1",
            "mrn_status_string", "mrn_last_cuda_error", "mrn_query_geometry",
            "mrn_force_geometry", "mrn_launch_count", "mrn_wait_timeouts",
-           "mrn_set_launch_options", "mrn_launch_options")
+           "mrn_set_launch_options", "mrn_launch_options", "mrn_rmsnorm_seam",
+           "mrn_rmsnorm_unweighted", "mrn_seam_scale")
 
 
 class MrnError(RuntimeError):
@@ -110,8 +114,12 @@ def lib() -> ctypes.CDLL:
             L.mrn_rmsnorm_then_add_scale.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f,
                                                      _i, _vp]
             L.mrn_rmsnorm_q8_1.argtypes = [_vp, _vp, _vp, _i64, _i64, _f, _i, _vp]
+            L.mrn_rmsnorm_seam.argtypes = [_vp, _vp, _vp, _i64, _i64, _f, _i, _i, _vp]
+            L.mrn_rmsnorm_unweighted.argtypes = [_vp, _vp, _i64, _i64, _f, _i, _i, _vp]
+            L.mrn_seam_scale.argtypes = [_vp, _vp, _vp, _i64, _i64, _i, _vp]
             for fn in (L.mrn_rmsnorm, L.mrn_rmsnorm_then_add, L.mrn_norm_residual_norm,
-                       L.mrn_add_rmsnorm, L.mrn_rmsnorm_then_add_scale, L.mrn_rmsnorm_q8_1):
+                       L.mrn_add_rmsnorm, L.mrn_rmsnorm_then_add_scale, L.mrn_rmsnorm_q8_1,
+                       L.mrn_rmsnorm_seam, L.mrn_rmsnorm_unweighted, L.mrn_seam_scale):
                 fn.restype = _i
             L.mrn_status_string.argtypes = [_i]
             L.mrn_status_string.restype = ctypes.c_char_p
@@ -163,6 +171,18 @@ def mrn_rmsnorm_then_add_scale(x, gamma, residual, out_scale, out, rows, n, eps,
 
 def mrn_rmsnorm_q8_1(x, gamma, blocks, rows, n, eps, dtype, stream=0) -> int:
     return lib().mrn_rmsnorm_q8_1(x, gamma, blocks, rows, n, eps, dtype, stream)
+
+
+def mrn_rmsnorm_seam(x, gamma, y, rows, n, eps, dtype, seam, stream=0) -> int:
+    return lib().mrn_rmsnorm_seam(x, gamma, y, rows, n, eps, dtype, seam, stream)
+
+
+def mrn_rmsnorm_unweighted(x, u, rows, n, eps, dtype, seam, stream=0) -> int:
+    return lib().mrn_rmsnorm_unweighted(x, u, rows, n, eps, dtype, seam, stream)
+
+
+def mrn_seam_scale(u, gamma, y, rows, n, seam, stream=0) -> int:
+    return lib().mrn_seam_scale(u, gamma, y, rows, n, seam, stream)
 
 
 def mrn_status_string(status: int) -> str:
@@ -356,3 +376,63 @@ def rmsnorm_q8_1(x, gamma, eps: float, blocks=None):
     if st != 0:
         raise MrnError(st, "mrn_rmsnorm_q8_1")
     return blocks
+
+
+def _seam_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return MRN_F16
+    if t.dtype == torch.bfloat16:
+        return MRN_BF16
+    raise TypeError(f"seam tensors hold float16 or bfloat16, not {t.dtype}")
+
+
+def rmsnorm_seam(x, gamma, eps: float, out=None):
+    """Split-norm seam in one kernel: S(S(x * inv_rms) * gamma), S = gamma's
+    dtype (float16 or bfloat16); x is float32 or bfloat16.  out may be x when
+    x is bfloat16."""
+    import torch
+    dt = _dtype_code(x)
+    _check(x, "x", x.dtype)
+    rows, n = _rows_n(x)
+    seam = _seam_code(gamma)
+    _check(gamma, "gamma", gamma.dtype, (n,))
+    out = torch.empty(x.shape, dtype=gamma.dtype, device=x.device) if out is None else out
+    _check(out, "out", gamma.dtype, x.shape)
+    st = mrn_rmsnorm_seam(x.data_ptr(), gamma.data_ptr(), out.data_ptr(), rows, n, eps, dt, seam,
+                          _stream(x))
+    if st != 0:
+        raise MrnError(st, "mrn_rmsnorm_seam")
+    return out
+
+
+def rmsnorm_unweighted(x, eps: float, seam_dtype, out=None):
+    """The seam's first operation: S(x * inv_rms) in seam_dtype (torch.float16
+    or torch.bfloat16)."""
+    import torch
+    dt = _dtype_code(x)
+    _check(x, "x", x.dtype)
+    rows, n = _rows_n(x)
+    out = torch.empty(x.shape, dtype=seam_dtype, device=x.device) if out is None else out
+    seam = _seam_code(out)
+    _check(out, "out", seam_dtype, x.shape)
+    st = mrn_rmsnorm_unweighted(x.data_ptr(), out.data_ptr(), rows, n, eps, dt, seam, _stream(x))
+    if st != 0:
+        raise MrnError(st, "mrn_rmsnorm_unweighted")
+    return out
+
+
+def seam_scale(u, gamma, out=None):
+    """The seam's second operation: S(u * gamma), u and gamma of one 16-bit
+    dtype; out may be u."""
+    import torch
+    seam = _seam_code(u)
+    _check(u, "u", u.dtype)
+    rows, n = _rows_n(u)
+    _check(gamma, "gamma", u.dtype, (n,))
+    out = torch.empty_like(u) if out is None else out
+    _check(out, "out", u.dtype, u.shape)
+    st = mrn_seam_scale(u.data_ptr(), gamma.data_ptr(), out.data_ptr(), rows, n, seam, _stream(u))
+    if st != 0:
+        raise MrnError(st, "mrn_seam_scale")
+    return out

@@ -61,6 +61,28 @@ def to_bf16_bits(a) -> np.ndarray:
     return f.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
 
 
+def to_f16_bits(a) -> np.ndarray:
+    """Round to IEEE binary16 through numpy's float64 -> float16 cast; uint16 bits."""
+    with np.errstate(over="ignore"):
+        return np.asarray(a, dtype=np.float64).astype(np.float16).view(np.uint16).copy()
+
+
+def to_seam_bits(a, seam: str) -> np.ndarray:
+    """16-bit patterns of the seam format "f16" or "bf16"."""
+    return to_f16_bits(a) if seam == "f16" else to_bf16_bits(a)
+
+
+def seam_rows(seed, rows: int, n: int, dtype: str = "f32", seam: str = "f16",
+              scale: float = 1.0):
+    """Rows for the split-norm seam: x ~ N(0, scale^2) in dtype, gamma =
+    1 + 0.1 N(0,1) rounded to the seam format."""
+    g = rng(seed)
+    x = scale * g.standard_normal((rows, n))
+    gamma = gamma_like(g, n)
+    conv = to_f32 if dtype == "f32" else to_bf16_bits
+    return {"x": conv(x), "gamma": to_seam_bits(gamma, seam)}
+
+
 def gamma_like(g: np.random.Generator, n: int) -> np.ndarray:
     """gamma = 1 + 0.1 N(0,1) in float64 (rounded by the caller)."""
     return 1.0 + 0.1 * g.standard_normal(n)

@@ -65,7 +65,9 @@ extern "C" {
 
 typedef enum mrn_dtype {
     MRN_F32 = 0,
-    MRN_BF16 = 1
+    MRN_BF16 = 1,
+    MRN_F16 = 2    /* IEEE binary16: only as the publication format of the seam
+                      operations below; every other use is MRN_ERR_UNSUPPORTED_DTYPE */
 } mrn_dtype;
 
 typedef enum mrn_status {
@@ -73,7 +75,8 @@ typedef enum mrn_status {
     MRN_ERR_NULL_POINTER = 1,      /* a required pointer is NULL (rows > 0) */
     MRN_ERR_INVALID_SIZE = 2,      /* n < 1, rows < 0, or rows*n*size overflows */
     MRN_ERR_INVALID_EPS = 3,       /* eps not finite or not > 0 */
-    MRN_ERR_UNSUPPORTED_DTYPE = 4, /* dtype not MRN_F32 / MRN_BF16 */
+    MRN_ERR_UNSUPPORTED_DTYPE = 4, /* dtype not MRN_F32 / MRN_BF16 (seam format not
+                                      MRN_F16 / MRN_BF16) */
     MRN_ERR_ALIASING = 5,          /* a forbidden overlap between buffers */
     MRN_ERR_MISALIGNED = 6,        /* a pointer not aligned to its element size */
     MRN_ERR_CUDA = 7,              /* the CUDA runtime refused the launch */
@@ -179,6 +182,37 @@ mrn_status mrn_rmsnorm_q8_1(const void *x, const void *gamma, void *blocks,
                             int64_t rows, int64_t n, float eps,
                             mrn_dtype dtype, cudaStream_t stream);
 
+/*
+ * Split-norm seam: the rounding point between the weightless norm and the
+ * weight multiply kept ("Chapter 12", section 12.7, the cross-vendor seam: a
+ * producer that publishes the unweighted norm in F16 and applies its scale as
+ * a second F16 operation; a receiver that fuses the two loses that rounding
+ * point).  S is the 16-bit publication format `seam` (MRN_F16 or MRN_BF16),
+ * S(v) rounds an f32 value to S (nearest, ties to even; overflow gives
+ * infinity, gradual underflow).
+ *   mrn_rmsnorm_unweighted  u[r,j] = S(x[r,j] * inv(x[r,:]; eps))
+ *   mrn_seam_scale          y[r,j] = S(u[r,j] * gamma[j])
+ *   mrn_rmsnorm_seam        y[r,j] = S(S(x[r,j] * inv(x[r,:]; eps)) * gamma[j])
+ * The fused form gives, bit for bit, what the two split operations give on the
+ * same rows: u * gamma multiplies two S values, exact in f32 (for bf16, unless
+ * the product falls below 2^-126, where f32 rounds it first), and the
+ * reduction (hence inv) is the same for the fused and the weightless call.
+ *   x      [rows x n]  f32 or bf16 (dtype)
+ *   gamma  [n]         16-bit values of S
+ *   u, y   [rows x n]  16-bit values of S; y may be x itself when dtype is
+ *                      MRN_BF16 (same element positions), and mrn_seam_scale's
+ *                      y may be u itself; no other overlap is allowed
+ * Vector paths need 16-byte aligned pointers and n * element size (of x; of
+ * u for mrn_seam_scale) a multiple of 16; otherwise element-wise.
+ */
+mrn_status mrn_rmsnorm_seam(const void *x, const void *gamma, void *y,
+                            int64_t rows, int64_t n, float eps,
+                            mrn_dtype dtype, mrn_dtype seam, cudaStream_t stream);
+mrn_status mrn_rmsnorm_unweighted(const void *x, void *u, int64_t rows, int64_t n, float eps,
+                                  mrn_dtype dtype, mrn_dtype seam, cudaStream_t stream);
+mrn_status mrn_seam_scale(const void *u, const void *gamma, void *y, int64_t rows, int64_t n,
+                          mrn_dtype seam, cudaStream_t stream);
+
 /* Static, human-readable name of a status code; never NULL. */
 const char *mrn_status_string(mrn_status status);
 
@@ -197,7 +231,9 @@ typedef enum mrn_op {
     MRN_OP_SANDWICH = 2,
     MRN_OP_ADD_RMSNORM = 3,
     MRN_OP_THEN_ADD_SCALE = 4,
-    MRN_OP_RMSNORM_Q8_1 = 5
+    MRN_OP_RMSNORM_Q8_1 = 5,
+    MRN_OP_RMSNORM_SEAM = 6,       /* mrn_rmsnorm_seam (either format) */
+    MRN_OP_RMSNORM_UNWEIGHTED = 7  /* mrn_rmsnorm_unweighted (either format) */
 } mrn_op;
 
 typedef enum mrn_geometry_kind {

@@ -423,3 +423,123 @@ def sample_rows(rows, count, seed, must=()):
     pick.update(int(v) for v in must)
     pick.update({0, rows - 1})
     return np.array(sorted(pick))
+
+
+# ---------------------------------------------------------------------------
+# Split-norm seam: u = S(x * inv), y = S(u * gamma), S = binary16 or bf16
+# ---------------------------------------------------------------------------
+SEAM_TIE_MARGIN = 2e-5     # relative distance of x * inv to an S rounding tie
+
+
+def seam_code(seam):
+    return mrn.MRN_F16 if seam == "f16" else mrn.MRN_BF16
+
+
+def seam_bits_from_double(v, seam):
+    return oracle.f16_from_double(v) if seam == "f16" else oracle.bf16_from_double(v)
+
+
+def seam_double_from_bits(bits, seam):
+    return oracle.double_from_f16(bits) if seam == "f16" else oracle.double_from_bf16(bits)
+
+
+def _seam_step(bits, up):
+    """The neighbouring S pattern above (up) or below; signed-magnitude order."""
+    o = _ordered(bits) + np.where(up, 1, -1)
+    return np.where(o >= 0, o, 0x8000 | (-o)).astype(np.uint16)
+
+
+def seam_expected(x, gamma_bits, eps, dtype, seam, rows_sample=None):
+    """Oracle bit patterns of u and y, the other admissible pair (u', y') for
+    elements whose x * inv lies within SEAM_TIE_MARGIN of a tie between u and
+    its neighbour (the GPU's f32 norm may round to either side there), and
+    the near-tie mask."""
+    sel = slice(None) if rows_sample is None else rows_sample
+    x64 = widen(x[sel], dtype)
+    g64 = seam_double_from_bits(gamma_bits, seam)
+    e = float(np.float32(eps))
+    u, y = oracle.rmsnorm_seam(x64, g64, e, seam)
+    p = oracle.rmsnorm(x64, np.ones(x64.shape[1]), e)          # x * inv in f64
+    u_bits = seam_bits_from_double(u, seam)
+    y_bits = seam_bits_from_double(y, seam)
+    alt_bits = _seam_step(u_bits, p > u)
+    alt = seam_double_from_bits(alt_bits, seam)
+    finite = np.isfinite(alt) & np.isfinite(u)
+    mid = np.where(finite, (u + np.where(finite, alt, 0.0)) / 2, np.inf)
+    near = np.abs(p - mid) <= SEAM_TIE_MARGIN * np.abs(p)
+    y_alt_bits = seam_bits_from_double(np.where(finite, alt, 0.0) * g64, seam)
+    return u_bits, y_bits, alt_bits, y_alt_bits, near
+
+
+def check_seam_bits(got, want, alt, near, what, loose=None):
+    """got == want, or got == alt where near; `loose` marks elements where one
+    step in signed-magnitude order is also admissible (bf16 products below
+    2^-126, rounded first in f32)."""
+    got = np.asarray(got, dtype=np.uint16)
+    ok = (got == want) | (near & (got == alt))
+    if loose is not None:
+        step = (np.abs(_ordered(got) - _ordered(want)) <= 1) | \
+               (np.abs(_ordered(got) - _ordered(alt)) <= 1)
+        ok |= loose & step
+    if not np.all(ok):
+        i = np.flatnonzero(~ok.ravel())[:5]
+        raise AssertionError(f"{what}: {int((~ok).sum())} of {ok.size} differ; got "
+                             f"{[hex(v) for v in got.ravel()[i]]} want "
+                             f"{[hex(v) for v in np.asarray(want).ravel()[i]]}")
+    return int(np.sum(near & (got == alt) & (got != want)))
+
+
+def _guarded_16(rows, n):
+    raw = torch.full((rows * n * 2 + 2 * GUARD_BYTES,), 0xA5, dtype=torch.uint8, device="cuda")
+    return raw, raw[GUARD_BYTES:GUARD_BYTES + rows * n * 2].view(torch.int16)
+
+
+def _unguard_16(raw, rows, n, what):
+    host = raw.cpu().numpy()
+    assert np.all(host[:GUARD_BYTES] == 0xA5) and np.all(host[-GUARD_BYTES:] == 0xA5), \
+        what + ": guard bands"
+    return host[GUARD_BYTES:-GUARD_BYTES].copy().view(np.uint16).reshape(rows, n)
+
+
+def run_seam(x, gamma_bits, eps, dtype, seam, x_offset=0):
+    """(u, y_split, y_fused) bit patterns from the GPU: the weightless norm, the
+    split route's scale of it, and the fused kernel, each in guarded buffers."""
+    rows, n = x.shape
+    if x_offset:
+        base = to_device(np.concatenate([np.zeros(x_offset, x.dtype), x.ravel()]), dtype)
+        dx = base[x_offset:].view(rows, n)
+    else:
+        dx = to_device(x, dtype)
+    dg = torch.from_numpy(np.ascontiguousarray(gamma_bits).view(np.int16)).cuda()
+    ru, du = _guarded_16(rows, n)
+    rs, ds = _guarded_16(rows, n)
+    rf, df = _guarded_16(rows, n)
+    sh, sc = stream_handle(), seam_code(seam)
+    st = mrn.mrn_rmsnorm_unweighted(dx.data_ptr(), du.data_ptr(), rows, n, eps, code(dtype), sc, sh)
+    assert st == 0, f"unweighted: status {mrn.STATUS.get(st)}"
+    st = mrn.mrn_seam_scale(du.data_ptr(), dg.data_ptr(), ds.data_ptr(), rows, n, sc, sh)
+    assert st == 0, f"seam_scale: status {mrn.STATUS.get(st)}"
+    st = mrn.mrn_rmsnorm_seam(dx.data_ptr(), dg.data_ptr(), df.data_ptr(), rows, n, eps,
+                              code(dtype), sc, sh)
+    assert st == 0, f"seam: status {mrn.STATUS.get(st)}"
+    torch.cuda.synchronize()
+    return (_unguard_16(ru, rows, n, "u"), _unguard_16(rs, rows, n, "split y"),
+            _unguard_16(rf, rows, n, "fused y"))
+
+
+def parity_seam(x, gamma_bits, eps, dtype, seam, rows_sample=None, what="seam", x_offset=0,
+                loose_underflow=False):
+    """All three seam calls against the oracle (u and y, near-tie alternatives
+    admitted), and the fused y bit-identical to the split route's y."""
+    u, ys, yf = run_seam(x, gamma_bits, eps, dtype, seam, x_offset)
+    assert np.array_equal(yf, ys), f"{what}: fused differs from split in " \
+                                   f"{int(np.sum(yf != ys))} elements"
+    sel = slice(None) if rows_sample is None else rows_sample
+    ub, yb, ab, yab, near = seam_expected(x, gamma_bits, eps, dtype, seam, rows_sample)
+    loose = None
+    if loose_underflow and seam == "bf16":
+        prod = np.abs(seam_double_from_bits(ub, seam) * seam_double_from_bits(gamma_bits, seam))
+        loose = prod < 2.0 ** -126
+    flips = check_seam_bits(u[sel], ub, ab, near, what + " u")
+    check_seam_bits(yf[sel], yb, yab, near, what + " y", loose)
+    return flips, int(near.sum())

@@ -103,6 +103,57 @@ def test_q8_1_validation():
     assert mrn.mrn_launch_count() == 0
 
 
+def seam(x=A, g=G, y=Y, rows=4, n=64, eps=1e-5, dt=mrn.MRN_F32, s=mrn.MRN_F16):
+    return mrn.mrn_rmsnorm_seam(x, g, y, rows, n, eps, dt, s, 0)
+
+
+def unw(x=A, y=Y, rows=4, n=64, eps=1e-5, dt=mrn.MRN_F32, s=mrn.MRN_F16):
+    return mrn.mrn_rmsnorm_unweighted(x, y, rows, n, eps, dt, s, 0)
+
+
+def scl(u=A, g=G, y=Y, rows=4, n=64, s=mrn.MRN_F16):
+    return mrn.mrn_seam_scale(u, g, y, rows, n, s, 0)
+
+
+def test_seam_validation():
+    for f in (seam, unw):
+        assert f(s=mrn.MRN_F32) == mrn.MRN_ERR_UNSUPPORTED_DTYPE      # S is 16-bit
+        assert f(s=3) == mrn.MRN_ERR_UNSUPPORTED_DTYPE
+        assert f(dt=mrn.MRN_F16) == mrn.MRN_ERR_UNSUPPORTED_DTYPE     # x is f32 or bf16
+        assert f(n=0) == mrn.MRN_ERR_INVALID_SIZE
+        assert f(eps=0.0) == mrn.MRN_ERR_INVALID_EPS
+        assert f(x=None, y=None, rows=0) == mrn.MRN_OK
+        assert f(x=None) == mrn.MRN_ERR_NULL_POINTER
+        assert f(y=Y + 1) == mrn.MRN_ERR_MISALIGNED
+        assert f(y=A) == mrn.MRN_ERR_ALIASING                 # f32 x: 16-bit y cannot share it
+        assert f(y=A + 2, dt=mrn.MRN_BF16) == mrn.MRN_ERR_ALIASING   # partial over bf16 x
+    assert seam(g=None) == mrn.MRN_ERR_NULL_POINTER
+    assert seam(g=G + 1) == mrn.MRN_ERR_MISALIGNED
+    assert seam(y=G - 8) == mrn.MRN_ERR_ALIASING              # output over gamma
+    assert scl(s=mrn.MRN_F32) == mrn.MRN_ERR_UNSUPPORTED_DTYPE
+    assert scl(n=0) == mrn.MRN_ERR_INVALID_SIZE
+    assert scl(rows=2 ** 62) == mrn.MRN_ERR_INVALID_SIZE
+    assert scl(u=None, g=None, y=None, rows=0) == mrn.MRN_OK
+    for kw in ("u", "g", "y"):
+        assert scl(**{kw: None}) == mrn.MRN_ERR_NULL_POINTER, kw
+    assert scl(u=A + 1) == mrn.MRN_ERR_MISALIGNED
+    assert scl(y=A + 2) == mrn.MRN_ERR_ALIASING               # partial over u
+    assert scl(y=G) == mrn.MRN_ERR_ALIASING                   # over gamma
+    assert mrn.mrn_launch_count() == 0
+
+
+def test_seam_geometry():
+    for op in (mrn.MRN_OP_RMSNORM_SEAM, mrn.MRN_OP_RMSNORM_UNWEIGHTED):
+        assert mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True, 152)["kind"] == 2
+        assert mrn.mrn_query_geometry(op, 4096, 128, mrn.MRN_BF16, True, 152)["kind"] == 1
+        assert mrn.mrn_force_geometry({"kind": 4, "k": 4, "threads": 416, "stages": 2}) == 0
+        with pytest.raises(mrn.MrnError):      # the seam has no staged kernel
+            mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True, 152)
+        assert mrn.mrn_force_geometry(None) == 0
+    with pytest.raises(mrn.MrnError):
+        mrn.mrn_query_geometry(8, 4, 64, mrn.MRN_F32, True, 152)
+
+
 def test_size_validation():
     assert rms(n=0) == mrn.MRN_ERR_INVALID_SIZE
     assert rms(n=-3) == mrn.MRN_ERR_INVALID_SIZE
@@ -166,7 +217,7 @@ def test_geometry_covers_every_row_width():
                   4096, 5120, 6656, 6657, 8192, 16384, 32768, 65536, 131072, 262144, 1 << 20]:
             for rows in (1, 4, 64, 4096, 65536):
                 for a16 in (True, False):
-                    for op in (0, 1, 2, 3, 4, 5):
+                    for op in (0, 1, 2, 3, 4, 5, 6, 7):
                         if op == 5 and n % 32:
                             continue
                         g = mrn.mrn_query_geometry(op, rows, n, dt, a16, 152)
@@ -184,7 +235,7 @@ def test_geometry_covers_every_row_width():
                             cap = 1024 if g["k"] <= 2 else (512 if g["k"] <= 4 else 256)
                             assert g["threads"] <= cap
                         elif g["kind"] == mrn.MRN_GEOM_TMA:
-                            assert a16 and rows >= 152
+                            assert a16 and rows >= 152 and op not in (6, 7)
                             per_group = g["threads"] // g["groups"]
                             assert per_group * g["k"] >= nvec and per_group % 32 == 0
                             assert 2 <= g["stages"] <= 4 and g["ctas"] == 0

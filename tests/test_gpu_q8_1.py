@@ -45,6 +45,28 @@ def test_batch_and_zero_blocks(dtype):
     print(f"q8 {dtype}: {off} codes one off, all within {ties} near-tie codes")
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_extreme_block_magnitudes(dtype):
+    """Blocks whose amax is far from 1: tiny (normed values near 1e-34),
+    products that fall below the smallest normal f32, and huge ones (gamma
+    1e33, so d overflows f16 to infinity) -- the codes of such blocks are
+    formed by per-element division rather than by the block reciprocal."""
+    rows, n = 6, 512
+    g = np.random.Generator(np.random.PCG64(77))
+    x = g.standard_normal((rows, n))
+    x[0, :] = 0.0
+    x[0, 0] = 1.0
+    x[0, 32:64] = 1e-35 * g.uniform(0.5, 1.0, size=32)
+    x[0, 64:96] = 3e-39 * g.uniform(0.5, 1.0, size=32)
+    x[1, 96:128] *= 1e-33
+    gamma = 1.0 + 0.1 * g.standard_normal(n)
+    gamma[128:160] = 1e33
+    gamma[160:192] *= 1e-30
+    x = wl.to_f32(x) if dtype == "f32" else wl.to_bf16_bits(x)
+    gamma = wl.to_f32(gamma) if dtype == "f32" else wl.to_bf16_bits(gamma)
+    gu.parity_q8_1(x, gamma, 1e-6, dtype, what=f"q8 extreme magnitudes {dtype}")
+
+
 GEOMS = [   # (geometry, n for f32, n for bf16); 0 = not coverable
     ({"kind": 1, "lanes_per_row": 32, "k": 8}, 1024, 2048),
     ({"kind": 1, "lanes_per_row": 8, "k": 2}, 64, 128),
