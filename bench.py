@@ -59,6 +59,9 @@ def parse_args(argv=None):
                    help="skip the bf16 16384x4096 and f32 4x6656 secondary measurements")
     p.add_argument("--profile-launches", type=int, default=0,
                    help="only run --warmup + this many launches of the timed call (for ncu)")
+    p.add_argument("--profile-op", choices=("sandwich", "seam_f16", "q8_1"), default="sandwich",
+                   help="with --profile-launches: the call to launch -- the timed sandwich, the "
+                        "fused f16 seam at the same shape, or RMSNorm + Q8_1 at 16384 x 4096 bf16")
     return p.parse_args(argv)
 
 
@@ -293,6 +296,9 @@ def run_mrn(args):
     if pg is not None:
         pg.barrier()
     mrn.lib()
+
+    if args.profile_launches and args.profile_op != "sandwich":
+        return profile_other(args, dev)
 
     rows, n = args.rows, args.n
     w = wl.sandwich_prefill(rows=rows, n=n)
@@ -586,6 +592,7 @@ def secondary_workloads(dev, stream):
     del sets, outs
     torch.cuda.empty_cache()
     out.update(more_ops(dev, stream))
+    out.update(seam_ops(dev, stream))
 
     w = wl.plain_decode_rows()
     nsets = 512
@@ -689,6 +696,117 @@ def more_ops(dev, stream):
     run("qk_norm_bf16_rows163840_n128", mrn.MRN_OP_RMSNORM, B, rows, n, (2 * rows * n + n) * 2,
         lambda t: check(mrn.mrn_rmsnorm(t[0].data_ptr(), t[2].data_ptr(), t[3].data_ptr(), rows,
                                         n, 1e-6, B, sh), "qk_norm"))
+    return out
+
+
+def profile_other(args, dev):
+    """--profile-launches for a secondary call: --warmup + --profile-launches
+    launches of it on seeded random inputs (two buffer sets), nothing else."""
+    import torch
+
+    from dual_epsilon_sandwich_gb300 import mrn
+    sh = torch.cuda.current_stream().cuda_stream
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20261204)
+    if args.profile_op == "seam_f16":
+        rows, n = args.rows, args.n
+        sets = [(torch.randn(rows, n, device=dev, generator=gen),
+                 (1 + 0.1 * torch.randn(n, device=dev, generator=gen)).half(),
+                 torch.empty(rows, n, dtype=torch.float16, device=dev)) for _ in range(2)]
+
+        def call(t):
+            return mrn.mrn_rmsnorm_seam(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), rows,
+                                        n, 1e-5, mrn.MRN_F32, mrn.MRN_F16, sh)
+        geometry = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM_SEAM, rows, n, mrn.MRN_F32, True)
+    else:
+        rows, n = 16384, 4096
+        sets = [(torch.randn(rows, n, device=dev, generator=gen).bfloat16(),
+                 (1 + 0.1 * torch.randn(n, device=dev, generator=gen)).bfloat16(),
+                 torch.empty(rows * (n // 32) * mrn.Q8_1_BLOCK_BYTES, dtype=torch.uint8,
+                             device=dev)) for _ in range(2)]
+
+        def call(t):
+            return mrn.mrn_rmsnorm_q8_1(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), rows,
+                                        n, 1e-6, mrn.MRN_BF16, sh)
+        geometry = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM_Q8_1, rows, n, mrn.MRN_BF16, True)
+    for i in range(args.warmup + args.profile_launches):
+        st = call(sets[i % 2])
+        if st != 0:
+            raise mrn.MrnError(st, args.profile_op)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_op": args.profile_op, "rows": rows, "n": n,
+                      "profile_launches": args.profile_launches, "geometry": geometry}))
+    return 0
+
+
+def seam_ops(dev, stream):
+    """The split-norm seam (the weightless norm published in f16 or bf16, the
+    weight applied as a second operation in that format): the fused kernel
+    against the split route (two kernels, the intermediate through HBM), at
+    the benchmark's width with f32 input and at 16384 x 4096 bf16.  Same
+    timing as the other secondary lines; GB/s of each form's own algorithmic
+    bytes."""
+    import torch
+
+    from dual_epsilon_sandwich_gb300 import mrn
+    sh = stream.cuda_stream
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20261203)
+    out = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(launch, sets, iters=300):
+        for i in range(20):
+            launch(sets[i % 2])
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(iters):
+            launch(sets[i % 2])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / iters
+
+    def check(st, what):
+        if st != 0:
+            raise mrn.MrnError(st, what)
+
+    for name, dtype, seam, rows, n in (
+            ("seam_f16_from_f32_rows4096_n6656", mrn.MRN_F32, mrn.MRN_F16, 4096, 6656),
+            ("seam_bf16_from_bf16_rows16384_n4096", mrn.MRN_BF16, mrn.MRN_BF16, 16384, 4096)):
+        tdt = torch.float32 if dtype == mrn.MRN_F32 else torch.bfloat16
+        sdt = torch.float16 if seam == mrn.MRN_F16 else torch.bfloat16
+        e = 4 if dtype == mrn.MRN_F32 else 2
+        sets = []
+        for _ in range(2):
+            x = torch.randn(rows, n, device=dev, generator=gen).to(tdt)
+            g = (1 + 0.1 * torch.randn(n, device=dev, generator=gen)).to(sdt)
+            u = torch.empty(rows, n, dtype=sdt, device=dev)
+            y = torch.empty(rows, n, dtype=sdt, device=dev)
+            sets.append((x, g, u, y))
+
+        def fused(t):
+            check(mrn.mrn_rmsnorm_seam(t[0].data_ptr(), t[1].data_ptr(), t[3].data_ptr(), rows, n,
+                                       1e-5, dtype, seam, sh), name)
+
+        def split(t):
+            check(mrn.mrn_rmsnorm_unweighted(t[0].data_ptr(), t[2].data_ptr(), rows, n, 1e-5,
+                                             dtype, seam, sh), name)
+            check(mrn.mrn_seam_scale(t[2].data_ptr(), t[1].data_ptr(), t[3].data_ptr(), rows, n,
+                                     seam, sh), name)
+
+        us_f = timed(fused, sets)
+        us_s = timed(split, sets)
+        b_f = (e + 2) * rows * n + 2 * n
+        b_s = (e + 2) * rows * n + 4 * rows * n + 2 * n
+        out[name] = {"GB_per_s": b_f / (us_f * 1e-6) / 1e9, "us_per_call": us_f,
+                     "rows_per_s": rows / (us_f * 1e-6), "bytes_per_call": b_f,
+                     "split_route": {"GB_per_s": b_s / (us_s * 1e-6) / 1e9, "us_per_call": us_s,
+                                     "bytes_per_call": b_s, "launches": 2},
+                     "fused_speedup": us_s / us_f,
+                     "geometry": mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM_SEAM, rows, n, dtype,
+                                                        True)}
+        del sets
+        torch.cuda.empty_cache()
     return out
 
 

@@ -43,6 +43,10 @@ MRN_HOST_DEVICE constexpr int op_row_inputs(int op) {
 MRN_HOST_DEVICE constexpr int op_gammas(int op) {
     return op == kSandwich ? 2 : (op == kUnweightedF16 || op == kUnweightedBF16) ? 0 : 1;
 }
+// Gammas the staged (kTma) kernel copies into shared memory: the seam's
+// 16-bit gamma is read through L1 instead (its rows need not be a multiple
+// of 16 bytes when x is f32).
+MRN_HOST_DEVICE constexpr int op_staged_gammas(int op) { return op_is_seam(op) ? 0 : op_gammas(op); }
 enum Kind : int { kAuto = 0, kRowsPerWarp = 1, kCta = 2, kStream = 3, kTma = 4 };
 
 // Launch-time view of one call.  Pointers are device pointers; row operands
@@ -126,7 +130,7 @@ cudaError_t launch_seam_scale(bool seam_bf16, const void *u, const void *gamma, 
 // Dynamic shared memory of the staged (kTma) kernel for one operation: the
 // gammas once, plus each stage's row operands.
 constexpr int64_t tma_shared_bytes(int op, int64_t row_bytes, int stages) {
-    return row_bytes * (op_gammas(op) + stages * op_row_inputs(op));
+    return row_bytes * (op_staged_gammas(op) + stages * op_row_inputs(op));
 }
 
 // Number of bounded waits that ran out since the last call (and reset them).

@@ -442,9 +442,8 @@ __device__ __forceinline__ char *q8_row_blocks(const KernelArgs &a, int64_t row)
 // section 12.7, the cross-vendor seam): the weightless norm is published in a
 // 16-bit format S (binary16 or bf16), u = S(x * inv), and the weighted forms
 // apply the weight as a second S operation, y = S(u * gamma) with gamma given
-// in S.  u * gamma multiplies two S values; their product has at most 22
-// significant bits and is exact in f32 (for bf16, unless it falls below
-// 2^-126), so the one rounding to S is the correctly rounded S product.
+// in S: the S multiply (mul.rn.f16x2 / mul.rn.bf16x2, subnormals kept)
+// rounds the exact product of the two S values once.
 // ---------------------------------------------------------------------------
 template <int VEC> struct H16 {   // VEC 16-bit values, two per word (low first)
     uint32_t w[(VEC + 1) / 2];
@@ -508,18 +507,26 @@ __device__ __forceinline__ void st_h16(void *p, const H16<1> &f) {
     asm volatile(MRN_ST_OP ".u16 [%0], %1;" :: "l"(p), "h"(h) : "memory");
 }
 
-// S(u * gamma) of VEC values of S held two per word.
+// Two S products in one instruction: the IEEE multiply of the format,
+// round to nearest even.
+template <bool BF> __device__ __forceinline__ uint32_t seam_mul2(uint32_t u, uint32_t g) {
+    uint32_t r;
+    if (BF) {
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(u), "r"(g));
+    } else {
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(u), "r"(g));
+    }
+    return r;
+}
+
+// S(u * gamma) of VEC values of S held two per word (VEC == 1: the low half;
+// the high halves are zero and their product is discarded).
 template <bool BF, int VEC>
 __device__ __forceinline__ H16<VEC> seam_scale_frag(const H16<VEC> &u, const H16<VEC> &g) {
     H16<VEC> out;
-    if (VEC == 1) {
-        out.w[0] = seam_pack1<BF>(seam_lo<BF>(u.w[0]) * seam_lo<BF>(g.w[0]));
-    } else {
 #pragma unroll
-        for (int i = 0; i < VEC / 2; ++i)
-            out.w[i] = seam_pack2<BF>(seam_lo<BF>(u.w[i]) * seam_lo<BF>(g.w[i]),
-                                      seam_hi<BF>(u.w[i]) * seam_hi<BF>(g.w[i]));
-    }
+    for (int i = 0; i < (VEC + 1) / 2; ++i) out.w[i] = seam_mul2<BF>(u.w[i], g.w[i]);
+    if (VEC == 1) out.w[0] &= 0xFFFFu;
     return out;
 }
 
@@ -1009,7 +1016,7 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
     using Fr = Frag<T, VEC>;
     pdl_enter();
     constexpr int NS = op_row_inputs(OP);   // row operands staged per row
-    constexpr int NG = op_gammas(OP);       // gammas kept in shared memory
+    constexpr int NG = op_staged_gammas(OP);   // gammas kept in shared memory
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ ReduceSlots slots1[G];
     __shared__ ReduceSlots slots2[G];
@@ -1046,8 +1053,8 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
     }
     __syncthreads();
     if (tid == 0 && my_rows > 0) {
-        mbar_arrive_expect_tx(&bars[stages], NG * rb);
-        bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
+        mbar_arrive_expect_tx(&bars[stages], NG * rb);   // (NG == 0: completes at once)
+        if (NG >= 1) bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
         if (NG == 2) bulk_to_shared(gsm + rb, a.g2, rb, &bars[stages]);
         for (int s = 0; s < stages && s < my_rows; ++s) {
             stage_row<NS>(stage0 + s * NS * rb, xg, rg, (first + s * step) * row_bytes, rb,
@@ -1076,6 +1083,14 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             } else {
                 xv[k].zero();
                 rv[k].zero();
+            }
+        }
+        H16<VEC> hg[K];   // the seam's 16-bit gamma, through L1, in flight over the reduction
+        if (op_seam_weighted(OP)) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+                if (v < a.nvec) ld_h16(hg[k], static_cast<const char *>(a.g1) + v * VEC * 2);
             }
         }
         const int64_t row_elem = row * a.n;
@@ -1120,6 +1135,14 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
                 Fr g;
                 ld_shared(g, gsm + v * 16);
                 st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(rv[k], inv1, g));
+            }
+            continue;
+        }
+        if (op_is_seam(OP)) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+                if (v < a.nvec) seam_output<OP, T, VEC>(xv[k], inv1, hg[k], a.y, row_elem + v * VEC);
             }
             continue;
         }
@@ -1364,19 +1387,6 @@ cudaError_t launch_typed(const Geometry &g, KernelArgs a, int64_t rows, cudaStre
         ++*launches;
     }
     return cudaSuccess;
-}
-
-// Operations without a staged (kTma) kernel: the register and looped kernels.
-template <int OP>
-cudaError_t launch_op_registers(bool bf16, const Geometry &g, const KernelArgs &a, int64_t rows,
-                                cudaStream_t stream, uint64_t *launches) {
-    if (g.kind == kTma) return cudaErrorInvalidConfiguration;
-    if (bf16) {
-        return g.vec == 1 ? launch_typed<OP, BF16, 1>(g, a, rows, stream, launches)
-                          : launch_typed<OP, BF16, 8>(g, a, rows, stream, launches);
-    }
-    return g.vec == 1 ? launch_typed<OP, F32, 1>(g, a, rows, stream, launches)
-                      : launch_typed<OP, F32, 4>(g, a, rows, stream, launches);
 }
 
 template <int OP>

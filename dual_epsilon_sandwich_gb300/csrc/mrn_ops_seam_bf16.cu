@@ -7,9 +7,9 @@ namespace mrn {
 
 cudaError_t launch_seam_bf16(int op, bool bf16, const Geometry &g, const KernelArgs &a,
                              int64_t rows, cudaStream_t stream, uint64_t *launches) {
-    if (op == kSeamBF16) return launch_op_registers<kSeamBF16>(bf16, g, a, rows, stream, launches);
+    if (op == kSeamBF16) return launch_op<kSeamBF16>(bf16, g, a, rows, stream, launches);
     if (op == kUnweightedBF16)
-        return launch_op_registers<kUnweightedBF16>(bf16, g, a, rows, stream, launches);
+        return launch_op<kUnweightedBF16>(bf16, g, a, rows, stream, launches);
     return cudaErrorInvalidValue;
 }
 

@@ -8,9 +8,9 @@ namespace mrn {
 
 cudaError_t launch_seam_f16(int op, bool bf16, const Geometry &g, const KernelArgs &a,
                             int64_t rows, cudaStream_t stream, uint64_t *launches) {
-    if (op == kSeamF16) return launch_op_registers<kSeamF16>(bf16, g, a, rows, stream, launches);
+    if (op == kSeamF16) return launch_op<kSeamF16>(bf16, g, a, rows, stream, launches);
     if (op == kUnweightedF16)
-        return launch_op_registers<kUnweightedF16>(bf16, g, a, rows, stream, launches);
+        return launch_op<kUnweightedF16>(bf16, g, a, rows, stream, launches);
     return cudaErrorInvalidValue;
 }
 

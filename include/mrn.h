@@ -193,10 +193,10 @@ mrn_status mrn_rmsnorm_q8_1(const void *x, const void *gamma, void *blocks,
  *   mrn_rmsnorm_unweighted  u[r,j] = S(x[r,j] * inv(x[r,:]; eps))
  *   mrn_seam_scale          y[r,j] = S(u[r,j] * gamma[j])
  *   mrn_rmsnorm_seam        y[r,j] = S(S(x[r,j] * inv(x[r,:]; eps)) * gamma[j])
- * The fused form gives, bit for bit, what the two split operations give on the
- * same rows: u * gamma multiplies two S values, exact in f32 (for bf16, unless
- * the product falls below 2^-126, where f32 rounds it first), and the
- * reduction (hence inv) is the same for the fused and the weightless call.
+ * The weight multiply is the IEEE multiply of S (the exact product of two S
+ * values rounded once).  The fused form gives, bit for bit, what the two split
+ * operations give on the same rows: the reduction (hence inv) is the same for
+ * the fused and the weightless call.
  *   x      [rows x n]  f32 or bf16 (dtype)
  *   gamma  [n]         16-bit values of S
  *   u, y   [rows x n]  16-bit values of S; y may be x itself when dtype is

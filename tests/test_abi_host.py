@@ -144,11 +144,16 @@ def test_seam_validation():
 
 def test_seam_geometry():
     for op in (mrn.MRN_OP_RMSNORM_SEAM, mrn.MRN_OP_RMSNORM_UNWEIGHTED):
-        assert mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True, 152)["kind"] == 2
+        got = mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True, 152)
+        assert (got["kind"], got["stages"], got["groups"]) == (4, 4, 2)
+        got = mrn.mrn_query_geometry(op, 16384, 4096, mrn.MRN_BF16, True, 152)
+        assert (got["kind"], got["stages"], got["groups"]) == (4, 2, 2)
+        assert mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, False, 152)["kind"] == 2
         assert mrn.mrn_query_geometry(op, 4096, 128, mrn.MRN_BF16, True, 152)["kind"] == 1
-        assert mrn.mrn_force_geometry({"kind": 4, "k": 4, "threads": 416, "stages": 2}) == 0
-        with pytest.raises(mrn.MrnError):      # the seam has no staged kernel
-            mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True, 152)
+        # staged: one row operand per stage, no gamma in shared memory (read through L1)
+        assert mrn.mrn_force_geometry({"kind": 4, "k": 4, "threads": 416, "stages": 4}) == 0
+        got = mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True, 152)
+        assert (got["kind"], got["stages"]) == (4, 4)
         assert mrn.mrn_force_geometry(None) == 0
     with pytest.raises(mrn.MrnError):
         mrn.mrn_query_geometry(8, 4, 64, mrn.MRN_F32, True, 152)
@@ -235,13 +240,13 @@ def test_geometry_covers_every_row_width():
                             cap = 1024 if g["k"] <= 2 else (512 if g["k"] <= 4 else 256)
                             assert g["threads"] <= cap
                         elif g["kind"] == mrn.MRN_GEOM_TMA:
-                            assert a16 and rows >= 152 and op not in (6, 7)
+                            assert a16 and rows >= 152
                             per_group = g["threads"] // g["groups"]
                             assert per_group * g["k"] >= nvec and per_group % 32 == 0
                             assert 2 <= g["stages"] <= 4 and g["ctas"] == 0
                             assert g["groups"] in (1, 2) and g["stages"] % g["groups"] == 0
-                            ng = 2 if op == 2 else 1
-                            ns = 1 if op == 0 else 2
+                            ng = 2 if op == 2 else (0 if op in (6, 7) else 1)
+                            ns = 1 if op in (0, 5, 6, 7) else 2
                             assert (ng + g["stages"] * ns) * n * e <= 232448 - 1024
                         else:
                             assert g["kind"] == mrn.MRN_GEOM_STREAM
