@@ -685,7 +685,9 @@ int mrn_wait_timeouts(void) {
                           mrn::take_wait_timeouts_sandwich(),
                           mrn::take_wait_timeouts_add_rmsnorm(),
                           mrn::take_wait_timeouts_then_add_scale(),
-                          mrn::take_wait_timeouts_rmsnorm_q8_1()};
+                          mrn::take_wait_timeouts_rmsnorm_q8_1(),
+                          mrn::take_wait_timeouts_seam_f16(),
+                          mrn::take_wait_timeouts_seam_bf16()};
     int total = 0;
     for (int v : counts) {
         if (v < 0) {

@@ -140,5 +140,7 @@ int take_wait_timeouts_sandwich();
 int take_wait_timeouts_add_rmsnorm();
 int take_wait_timeouts_then_add_scale();
 int take_wait_timeouts_rmsnorm_q8_1();
+int take_wait_timeouts_seam_f16();
+int take_wait_timeouts_seam_bf16();
 
 }  // namespace mrn

@@ -13,4 +13,6 @@ cudaError_t launch_seam_bf16(int op, bool bf16, const Geometry &g, const KernelA
     return cudaErrorInvalidValue;
 }
 
+int take_wait_timeouts_seam_bf16() { return take_wait_timeouts<kSeamBF16>(); }
+
 }  // namespace mrn

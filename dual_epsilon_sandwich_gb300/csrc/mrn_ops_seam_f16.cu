@@ -14,4 +14,6 @@ cudaError_t launch_seam_f16(int op, bool bf16, const Geometry &g, const KernelAr
     return cudaErrorInvalidValue;
 }
 
+int take_wait_timeouts_seam_f16() { return take_wait_timeouts<kSeamF16>(); }
+
 }  // namespace mrn
