@@ -30,7 +30,7 @@ std::atomic<uint64_t> g_launch_count{0};
 thread_local int t_last_cuda_error = 0;
 thread_local bool t_forced = false;
 thread_local Geometry t_forced_geometry = {};
-thread_local uint32_t t_launch_options = 0;
+thread_local uint32_t t_launch_options = MRN_LAUNCH_PDL;   // the default
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];

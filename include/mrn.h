@@ -286,15 +286,19 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry);
 uint64_t mrn_launch_count(void);
 
 /*
- * Launch options of the calling thread's later calls (0 = none, the default).
+ * Launch options of the calling thread's later calls (default MRN_LAUNCH_PDL;
+ * 0 = plain stream-ordered launches).
  *   MRN_LAUNCH_PDL  programmatic dependent launch: a kernel may be scheduled
  *                   before the previous kernel on the stream has finished.
  *                   Every kernel of this library first waits for that
  *                   previous grid to complete and publish its memory
  *                   (griddepcontrol.wait), so results are unchanged; the
- *                   launch latency of a short call overlaps the previous
- *                   kernel instead of following it.  Useful for decode-size
- *                   calls in a chain; the previous kernel need not be ours.
+ *                   launch latency of a call overlaps the previous kernel
+ *                   instead of following it (measured on GB300: ~2 us per
+ *                   call in a chain of 4096 x 6656 sandwich calls, ~0.2 us
+ *                   per decode call in a CUDA graph).  The previous kernel
+ *                   need not be ours; a kernel launched after ours without
+ *                   the attribute is ordered as usual.
  * Unknown bits give MRN_ERR_INVALID_GEOMETRY.  Not on the pages: a launch
  * option of this library.
  */

@@ -297,11 +297,11 @@ def test_force_geometry_validation():
 
 
 def test_launch_options():
-    assert mrn.mrn_launch_options() == 0
+    assert mrn.mrn_launch_options() == mrn.MRN_LAUNCH_PDL          # the default
     assert mrn.mrn_set_launch_options(2) == mrn.MRN_ERR_INVALID_GEOMETRY
+    assert mrn.mrn_set_launch_options(0) == 0 and mrn.mrn_launch_options() == 0
     assert mrn.mrn_set_launch_options(mrn.MRN_LAUNCH_PDL) == 0
     assert mrn.mrn_launch_options() == mrn.MRN_LAUNCH_PDL
-    assert mrn.mrn_set_launch_options(0) == 0 and mrn.mrn_launch_options() == 0
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path):

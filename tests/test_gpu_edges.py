@@ -335,7 +335,7 @@ def test_programmatic_launch_chain_matches(rows, n):
             assert gu.call_sandwich(b, r, g1, g2, r, o, rows, n, 1e-8, 1e-5, "f32") == 0
             b, o = o, b
         torch.cuda.synchronize()
-        assert mrn.mrn_set_launch_options(0) == 0
+        assert mrn.mrn_set_launch_options(mrn.MRN_LAUNCH_PDL) == 0   # the default
         return b, r
 
     b0, r0 = chain(0)
