@@ -136,6 +136,47 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     g.vec = aligned16 ? natural_vec(dt) : 1;
     g.cluster = 1;
     const int64_t nvec = ceil_div(n, g.vec);
+    // RMSNorm + Q8_1 batches of aligned rows: whole 32-element blocks per
+    // thread (no shuffles; one reciprocal and one header per block).
+    // RMSNorm + Q8_1 batches of aligned rows use the whole-block kernels
+    // (measured on GB300, TB/s, rows >= 4096):
+    //   f32: staged (persistent, x bulk-copied two stages ahead) everywhere --
+    //        n = 1024: 4.2, 2048: 6.4, 4096: 6.3 (2 blocks per thread),
+    //        16384: 5.6 (one group: two do not fit in shared memory);
+    //   bf16: staged with 2 blocks per thread from n = 4096 (4.9 at 4096, 4.8
+    //        at 16384), one row per CTA at n = 2048 (4.9 vs 4.4 staged); below,
+    //        the lane-layout kernels (n = 1024: 4.0 vs 3.1).
+    const int64_t nblocks = n / mrn::kQ8Block;
+    const int64_t max_staged = static_cast<int64_t>(mrn::kQ8BlockMaxK) * mrn::kQ8TmaGroupThreads;
+    if (op == mrn::kRmsnormQ8 && aligned16 && rows >= sms && nblocks >= 32) {
+        g.kind = mrn::kQ8Blocks;
+        g.lanes = 0;
+        if ((dt == MRN_F32 || nblocks >= 128) && nblocks <= max_staged) {
+            g.k = nblocks >= 128 ? 2 : 1;
+            const int per = static_cast<int>(ceil_div(ceil_div(nblocks, g.k), 32) * 32);
+            for (int groups = 2; groups >= 1; --groups) {
+                if (mrn::q8_tma_shared_bytes(n, elem_bytes(dt), 2, groups) <= kTmaSharedBudget) {
+                    g.threads = groups * per;
+                    g.stages = 2;
+                    g.groups = groups;
+                    g.ctas = 0;
+                    g.rows_per_cta = groups;
+                    return g;
+                }
+            }
+        }
+        if (dt == MRN_BF16 && nblocks >= 64 &&
+            nblocks <= static_cast<int64_t>(mrn::kQ8BlockMaxK) * mrn::kQ8BlockMaxThreads) {
+            g.k = nblocks <= mrn::kQ8BlockMaxThreads ? 1 : 2;
+            g.threads = static_cast<int>(ceil_div(ceil_div(nblocks, g.k), 32) * 32);
+            g.stages = 0;
+            g.rows_per_cta = 1;
+            return g;
+        }
+        g = Geometry{};   // the lane-layout kernels below
+        g.vec = natural_vec(dt);
+        g.cluster = 1;
+    }
     if (nvec <= 32 * mrn::kMaxK) {
         // About four loads per thread (measured on GB300: per-head n = 128 rows
         // run ~15% faster with 4 slots x 4..8 lanes than with 1 slot x 16..32).
@@ -228,6 +269,15 @@ bool geometry_is_consistent(const Geometry &g) {
     if (g.kind == mrn::kStream) {
         return g.threads >= 32 && g.threads % 32 == 0 && g.threads <= mrn::kStreamMaxThreads;
     }
+    if (g.kind == mrn::kQ8Blocks) {
+        if (g.k < 1 || g.k > mrn::kQ8BlockMaxK || g.threads < 32 || g.threads % 32 != 0)
+            return false;
+        if (g.stages == 0) return g.threads <= mrn::kQ8BlockMaxThreads;
+        // staged: one stage per group per row, as for kTma
+        return g.groups >= 1 && g.groups <= 2 && g.threads % (32 * g.groups) == 0 &&
+               g.threads / g.groups <= mrn::kQ8TmaGroupThreads && g.stages >= g.groups &&
+               g.stages % g.groups == 0 && g.stages <= mrn::kTmaMaxStages && g.ctas >= 0;
+    }
     if (g.kind == mrn::kTma) {
         if (g.groups < 1 || g.groups > mrn::kTmaMaxGroups) return false;
         const int per_group = g.threads / g.groups;
@@ -246,7 +296,17 @@ bool resolve_forced(Geometry g, mrn::Op op, int64_t n, mrn_dtype dt, bool aligne
     if (g.vec == 0) g.vec = aligned16 ? natural_vec(dt) : 1;
     if (g.vec != 1 && !(g.vec == natural_vec(dt) && aligned16)) return false;
     const int64_t nvec = ceil_div(n, g.vec);
-    if (g.kind == mrn::kTma) {
+    if (g.kind == mrn::kQ8Blocks) {
+        if (op != mrn::kRmsnormQ8 || !aligned16 || g.vec != natural_vec(dt)) return false;
+        const int per = g.stages > 0 ? g.threads / g.groups : g.threads;
+        if (static_cast<int64_t>(per) * g.k * mrn::kQ8Block < n) return false;
+        if (g.stages > 0 &&
+            mrn::q8_tma_shared_bytes(n, elem_bytes(dt), g.stages, g.groups) > kTmaSharedBudget)
+            return false;
+        g.cluster = 1;
+        g.lanes = 0;
+        g.rows_per_cta = g.stages > 0 ? g.groups : 1;
+    } else if (g.kind == mrn::kTma) {
         if (!aligned16 || g.vec != natural_vec(dt)) return false;
         if (static_cast<int64_t>(g.threads / g.groups) * g.k < nvec) return false;
         if (mrn::tma_shared_bytes(op, n * elem_bytes(dt), g.stages) > kTmaSharedBudget)
@@ -639,9 +699,10 @@ mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtyp
     out->cluster = g.cluster;
     out->lanes_per_row = g.lanes;
     out->rows_per_cta = g.rows_per_cta;
-    out->stages = g.kind == mrn::kTma ? g.stages : 0;
-    out->ctas = g.kind == mrn::kTma ? g.ctas : 0;
-    out->groups = g.kind == mrn::kTma ? g.groups : 0;
+    const bool staged = g.kind == mrn::kTma || (g.kind == mrn::kQ8Blocks && g.stages > 0);
+    out->stages = staged ? g.stages : 0;
+    out->ctas = staged ? g.ctas : 0;
+    out->groups = staged ? g.groups : 0;
     return MRN_OK;
 }
 
@@ -660,7 +721,8 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry) {
     g.stages = geometry->stages;
     g.ctas = geometry->ctas;
     g.groups = geometry->groups;
-    if (g.kind == mrn::kTma && g.groups == 0) g.groups = 1;
+    if ((g.kind == mrn::kTma || (g.kind == mrn::kQ8Blocks && g.stages > 0)) && g.groups == 0)
+        g.groups = 1;
     if (g.kind == mrn::kRowsPerWarp && g.threads == 0) g.threads = mrn::kWarpKernelThreads;
     if (g.kind == mrn::kStream) g.k = 1;
     if (g.kind != mrn::kCta) g.cluster = 1;

@@ -47,7 +47,7 @@ MRN_HOST_DEVICE constexpr int op_gammas(int op) {
 // 16-bit gamma is read through L1 instead (its rows need not be a multiple
 // of 16 bytes when x is f32).
 MRN_HOST_DEVICE constexpr int op_staged_gammas(int op) { return op_is_seam(op) ? 0 : op_gammas(op); }
-enum Kind : int { kAuto = 0, kRowsPerWarp = 1, kCta = 2, kStream = 3, kTma = 4 };
+enum Kind : int { kAuto = 0, kRowsPerWarp = 1, kCta = 2, kStream = 3, kTma = 4, kQ8Blocks = 5 };
 
 // Launch-time view of one call.  Pointers are device pointers; row operands
 // are [rows x n] row-major.  For the sandwich, x = block_out, res = residual,
@@ -97,6 +97,23 @@ constexpr int kSharedBytesPerCta = 232448;    // 227 KB opt-in limit on sm_100 /
 constexpr int cta_max_threads(int k) { return k <= 2 ? 1024 : (k <= 4 ? 512 : 256); }
 // Staged kernel: threads per warp group, and per CTA for 1 or 2 groups.
 constexpr int kTmaMaxGroups = 2;
+// RMSNorm + Q8_1 with whole blocks per thread (kQ8Blocks): k = 1 or 2 blocks
+// per thread, at most this many threads per CTA (one row per CTA); with
+// stages > 0 the staged form: 1 or 2 warp groups of at most
+// kQ8TmaGroupThreads threads, persistent CTAs.
+constexpr int kQ8BlockMaxThreads = 512;
+constexpr int kQ8BlockMaxK = 2;
+constexpr int kQ8TmaGroupThreads = 256;
+// A row's Q8_1 blocks in shared memory, rounded up to 16 bytes.
+MRN_HOST_DEVICE constexpr int64_t q8_out_stride(int64_t blocks) {
+    return (blocks * 36 + 15) / 16 * 16;
+}
+// Dynamic shared memory of the staged Q8_1 kernel: gamma and `stages` rows of
+// x, plus one block buffer per group.
+MRN_HOST_DEVICE constexpr int64_t q8_tma_shared_bytes(int64_t n, int elem_bytes, int stages,
+                                                      int groups) {
+    return n * elem_bytes * (1 + stages) + groups * q8_out_stride(n / 32);
+}
 constexpr int tma_group_max_threads(int k) { return k <= 2 ? 512 : (k <= 4 ? 416 : 256); }
 constexpr int tma_max_threads(int k, int groups) {
     return groups == 1 ? cta_max_threads(k) : groups * tma_group_max_threads(k);

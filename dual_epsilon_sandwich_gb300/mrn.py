@@ -38,6 +38,7 @@ MRN_GEOM_ROWS_PER_WARP = 1
 MRN_GEOM_CTA = 2
 MRN_GEOM_STREAM = 3
 MRN_GEOM_TMA = 4
+MRN_GEOM_Q8_BLOCKS = 5
 
 MRN_LAUNCH_PDL = 1
 

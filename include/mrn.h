@@ -244,10 +244,13 @@ typedef enum mrn_geometry_kind {
                                    `cluster` CTAs with a DSMEM reduction; row held
                                    in registers */
     MRN_GEOM_STREAM = 3,        /* one row per CTA, looped over the row: any n */
-    MRN_GEOM_TMA = 4            /* persistent CTAs; `stages` future rows are copied
+    MRN_GEOM_TMA = 4,           /* persistent CTAs; `stages` future rows are copied
                                    into shared memory by cp.async.bulk while the
                                    current one is reduced; gammas kept in shared
                                    memory; needs 16-byte aligned rows */
+    MRN_GEOM_Q8_BLOCKS = 5      /* RMSNorm + Q8_1 only: one row per CTA, `k` (1 or 2)
+                                   whole 32-element blocks per thread, `threads` <= 512;
+                                   needs 16-byte aligned rows */
 } mrn_geometry_kind;
 
 typedef struct mrn_geometry {

@@ -239,6 +239,17 @@ def test_geometry_covers_every_row_width():
                             assert g["threads"] % 32 == 0 and 1 <= g["cluster"] <= 16
                             cap = 1024 if g["k"] <= 2 else (512 if g["k"] <= 4 else 256)
                             assert g["threads"] <= cap
+                        elif g["kind"] == mrn.MRN_GEOM_Q8_BLOCKS:
+                            assert op == 5 and a16 and rows >= 152 and g["k"] in (1, 2)
+                            if g["stages"]:                    # staged, two groups
+                                per = g["threads"] // g["groups"]
+                                assert per * g["k"] * 32 >= n and per <= 256 and per % 32 == 0
+                                assert g["stages"] % g["groups"] == 0
+                                assert (n * e * (1 + g["stages"]) +
+                                        g["groups"] * ((n // 32 * 36 + 15) // 16 * 16)) <= 232448 - 1024
+                            else:
+                                assert g["threads"] * g["k"] * 32 >= n and g["threads"] <= 512
+                                assert g["threads"] % 32 == 0
                         elif g["kind"] == mrn.MRN_GEOM_TMA:
                             assert a16 and rows >= 152
                             per_group = g["threads"] // g["groups"]
@@ -272,6 +283,12 @@ def test_force_geometry_validation():
         {"kind": 4, "k": 4, "threads": 800, "stages": 2, "groups": 2},     # 400 not a warp multiple
         {"kind": 4, "k": 8, "threads": 1024, "stages": 2, "groups": 2},    # 512 > 256 per group
         {"kind": 9},
+        {"kind": 5, "k": 3, "threads": 128},
+        {"kind": 5, "k": 1, "threads": 1024},
+        {"kind": 5, "k": 1, "threads": 100},
+        {"kind": 5, "k": 1, "threads": 1024, "stages": 2, "groups": 2},    # 512 > 256 per group
+        {"kind": 5, "k": 1, "threads": 256, "stages": 3, "groups": 2},     # stages % groups
+        {"kind": 5, "k": 1, "threads": 96, "stages": 2, "groups": 2},      # 48 per group
     ]
     for g in bad:
         assert mrn.mrn_force_geometry(g) == mrn.MRN_ERR_INVALID_GEOMETRY, g

@@ -39,14 +39,19 @@ def test_batch_and_zero_blocks(dtype):
     x[9, 100] = 1e-30
     x = wl.to_f32(x) if dtype == "f32" else wl.to_bf16_bits(x)
     gamma = wl.random_rows(32, 1, n, dtype)["gamma"]
-    assert mrn.mrn_query_geometry(5, rows, n, gu.code(dtype), True)["kind"] == mrn.MRN_GEOM_CTA
+    assert mrn.mrn_query_geometry(5, rows, n, gu.code(dtype), True)["kind"] == \
+        mrn.MRN_GEOM_Q8_BLOCKS
     off, ties = gu.parity_q8_1(x, gamma, 1e-6, dtype,
                                rows_sample=gu.sample_rows(rows, 200, 3, must=(5, 9)))
     print(f"q8 {dtype}: {off} codes one off, all within {ties} near-tie codes")
 
 
+@pytest.mark.parametrize("geom", [None, {"kind": 5, "k": 1, "threads": 32},
+                                  {"kind": 5, "k": 1, "threads": 64, "stages": 2, "groups": 2,
+                                   "ctas": 2}],
+                         ids=["auto", "blocks", "staged blocks"])
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_extreme_block_magnitudes(dtype):
+def test_extreme_block_magnitudes(dtype, geom):
     """Blocks whose amax is far from 1: tiny (normed values near 1e-34),
     products that fall below the smallest normal f32, and huge ones (gamma
     1e33, so d overflows f16 to infinity) -- the codes of such blocks are
@@ -64,7 +69,8 @@ def test_extreme_block_magnitudes(dtype):
     gamma[160:192] *= 1e-30
     x = wl.to_f32(x) if dtype == "f32" else wl.to_bf16_bits(x)
     gamma = wl.to_f32(gamma) if dtype == "f32" else wl.to_bf16_bits(gamma)
-    gu.parity_q8_1(x, gamma, 1e-6, dtype, what=f"q8 extreme magnitudes {dtype}")
+    assert mrn.mrn_force_geometry(geom) == 0
+    gu.parity_q8_1(x, gamma, 1e-6, dtype, what=f"q8 extreme magnitudes {dtype} {geom}")
 
 
 GEOMS = [   # (geometry, n for f32, n for bf16); 0 = not coverable
@@ -75,6 +81,14 @@ GEOMS = [   # (geometry, n for f32, n for bf16); 0 = not coverable
     ({"kind": 3, "threads": 96}, 2560, 2560),
     ({"kind": 4, "k": 1, "threads": 128, "stages": 2, "groups": 2, "ctas": 5}, 256, 512),
     ({"kind": 4, "k": 4, "threads": 256, "stages": 2, "groups": 2}, 2048, 4096),
+    ({"kind": 5, "k": 1, "threads": 128}, 4096, 4096),
+    ({"kind": 5, "k": 2, "threads": 64}, 4000, 4000),
+    ({"kind": 5, "k": 2, "threads": 96}, 6144, 6112),
+    ({"kind": 5, "k": 1, "threads": 32}, 32, 1024),
+    ({"kind": 5, "k": 1, "threads": 256, "stages": 2, "groups": 2}, 4096, 4096),
+    ({"kind": 5, "k": 2, "threads": 128, "stages": 2, "groups": 2, "ctas": 5}, 4000, 4064),
+    ({"kind": 5, "k": 1, "threads": 96, "stages": 3, "groups": 1, "ctas": 3}, 3072, 2976),
+    ({"kind": 5, "k": 2, "threads": 64, "stages": 4, "groups": 2, "ctas": 1}, 2048, 1024),
 ]
 
 
