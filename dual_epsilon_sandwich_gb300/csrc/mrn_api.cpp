@@ -5,7 +5,7 @@
 // sandwich", section 12.1), post norm then residual add (Hesper "RMSNorm
 // Layer", rmsNormThenAddKernel), the dual-epsilon sandwich tail (section
 // 12.4.3), residual add then norm (Hesper residualAddRmsNormKernel), post
-// norm, add, broadcast scale (Hesper rmsNormThenAddThenBroadcastScaleKernel)
+// norm, add, broadcast scale (Hesper rmsNormThenAddThenBroadcastScaleKernel),
 // RMSNorm with Q8_1 quantisation (Hesper fusedRMSNormQ8_1Kernel) and the
 // split-norm seam (section 12.7: the weightless norm published in F16 or
 // bf16, the weight applied as a second operation in that format).  This layer

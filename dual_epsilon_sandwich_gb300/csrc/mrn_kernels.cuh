@@ -1,8 +1,11 @@
-// mrn_kernels.cuh -- sm_103a kernels for RMSNorm, post-norm-then-add and the
-// dual-epsilon sandwich tail.
+// mrn_kernels.cuh -- sm_103a kernels for RMSNorm, post-norm-then-add, the
+// dual-epsilon sandwich tail and the operations built on the same row
+// reduction (residual add + norm, then-add-scale, RMSNorm + Q8_1, the
+// split-norm seam).
 //
 // The computation ("Chapter 12 -- RMSNorm and the dual-epsilon sandwich",
-// sections 12.1 and 12.4.3; Hesper "RMSNorm Layer", rmsNormThenAddKernel):
+// sections 12.1, 12.4.3 and 12.7; Hesper "RMSNorm Layer", rmsNormThenAddKernel
+// and the kernels named at each operation below):
 //   inv = 1 / sqrt(sum_j v_j^2 / n + eps)            (f32, IEEE sqrt and divide)
 //   rmsnorm   y = (x * inv) * gamma
 //   then-add  out = fma(x * inv, gamma, residual)
@@ -11,8 +14,8 @@
 //
 // Design for a bandwidth-bound row reduction on GB300:
 //  * every operand element is read from HBM once and every output written
-//    once: the row (and the residual) stay in registers between the
-//    reduction and the output pass;
+//    once: the row (and the residual) stay in registers (or a shared-memory
+//    stage) between the reduction and the output pass;
 //  * 16-byte vector loads/stores (4 x f32 or 8 x bf16), consecutive lanes on
 //    consecutive vectors, so a warp moves 512 contiguous bytes per access;
 //    streaming operands bypass L1 (L1::no_allocate) and ask L2 for 256-byte
@@ -22,12 +25,16 @@
 //    thread-block cluster -- one DSMEM slot per CTA written into every peer
 //    and a release/acquire cluster barrier.  Every CTA sums the same partials
 //    in the same order, so all CTAs of a row use bit-identical inv;
-//  * three geometries: several rows per warp (small n), one row per CTA or
-//    per cluster (register resident, mid to large n), and a looped
-//    fallback for rows too wide for registers.
-// No kernel waits on a flag, a peer or an mbarrier; the only inter-CTA
-// synchronisation is the hardware cluster barrier, which every thread of
-// every CTA of the cluster reaches unconditionally.
+//  * geometries: several rows per warp (small n), one row per CTA or per
+//    cluster (register resident), a looped fallback for rows too wide for
+//    registers, persistent CTAs whose rows are bulk-copied (cp.async.bulk)
+//    into shared-memory stages ahead of use, and for RMSNorm + Q8_1 whole
+//    32-element blocks per thread;
+//  * every kernel starts with griddepcontrol.wait / launch_dependents, so a
+//    launch with programmatic stream serialisation changes no result.
+// The only waits are the hardware cluster barrier (reached unconditionally by
+// every thread of the cluster) and, in the staged kernels, mbarrier waits on
+// their own bulk copies, each bounded in time (see mbar_wait_bounded).
 #pragma once
 
 #include <atomic>

@@ -11,6 +11,10 @@
  *                           normed[r,j]     = out_stream[r,j] * inv(out_stream[r,:]; eps_pre)
  *                                             * gamma_pre[j]
  *   with inv(v; eps) = 1 / sqrt((1/n) sum_j v_j^2 + eps).
+ * Built on the same row reduction (declared further down, same conventions):
+ *   mrn_add_rmsnorm, mrn_rmsnorm_then_add_scale, mrn_rmsnorm_q8_1 (Hesper
+ *   "RMSNorm Layer" kernels) and the split-norm seam mrn_rmsnorm_seam,
+ *   mrn_rmsnorm_unweighted, mrn_seam_scale ("Chapter 12", section 12.7).
  *
  * Sources: "Chapter 12 -- RMSNorm and the dual-epsilon sandwich" section 12.1
  * (definition), 12.2 (two epsilons: 1e-8 for the post norms, 1e-5 for the pre
