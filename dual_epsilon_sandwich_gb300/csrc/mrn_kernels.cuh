@@ -1290,13 +1290,47 @@ __device__ __forceinline__ uint32_t pack4(uint32_t c0, uint32_t c1, uint32_t c2,
     return __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
 }
 
+// Code word of four normed values (two f32 pairs) by IEEE division and
+// clamps: the path for a block whose amax is zero, tiny or huge.  Kept out of
+// line so that the common path's loop body stays small.
+static __device__ __noinline__ uint32_t q8_word_exact(uint64_t p0, uint64_t p1, float d) {
+    float v[4];
+    f2_unpack(p0, v[0], v[1]);
+    f2_unpack(p1, v[2], v[3]);
+    uint32_t c[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        c[i] = static_cast<uint32_t>(d > 0.0f ? min(127, max(-128, __float2int_rn(v[i] / d))) : 0);
+    return pack4(c[0], c[1], c[2], c[3]);
+}
+
+// Code words of one chunk slot (VEC elements = VEC / 2 f32 pairs), four codes
+// to a word: by the block reciprocal (fast) or by IEEE division and clamps.
+template <int VEC>
+__device__ __forceinline__ void q8_chunk_words(const uint64_t *xn, bool fast, uint64_t id2,
+                                               float d, uint32_t *w) {
+    constexpr float kRoundShift = 12582912.0f;   // 1.5 * 2^23
+    const uint64_t sh2 = f2_pack(kRoundShift, kRoundShift);
+#pragma unroll
+    for (int q = 0; q < VEC / 4; ++q) {
+        if (fast) {
+            float c0, c1, c2, c3;
+            f2_unpack(f2_fma(xn[2 * q], id2, sh2), c0, c1);
+            f2_unpack(f2_fma(xn[2 * q + 1], id2, sh2), c2, c3);
+            w[q] = pack4(__float_as_uint(c0), __float_as_uint(c1), __float_as_uint(c2),
+                         __float_as_uint(c3));
+        } else {
+            w[q] = q8_word_exact(xn[2 * q], xn[2 * q + 1], d);
+        }
+    }
+}
+
 template <class T, int KB>
 __global__ void __launch_bounds__(kQ8BlockMaxThreads)
 mrn_q8_block_kernel(const KernelArgs a) {
     constexpr int VEC = 16 / T::kBytes;       // elements per 16-byte chunk
     constexpr int CH = kQ8Block / VEC;        // chunks per block
     constexpr int NP = kQ8Block / 2;          // f32 pairs per block
-    constexpr float kRoundShift = 12582912.0f;   // 1.5 * 2^23
     extern __shared__ __align__(16) unsigned char q8_row[];   // the row's blocks
     __shared__ ReduceSlots slots;
     pdl_enter();
@@ -1319,7 +1353,9 @@ mrn_q8_block_kernel(const KernelArgs a) {
             }
         }
     }
-    uint64_t acc = f2_pack(0.0f, 0.0f);
+    // four independent accumulators (short dependency chains)
+    uint64_t acc[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
+                       f2_pack(0.0f, 0.0f)};
 #pragma unroll
     for (int k = 0; k < KB; ++k)
 #pragma unroll
@@ -1327,11 +1363,15 @@ mrn_q8_block_kernel(const KernelArgs a) {
 #pragma unroll
             for (int p = 0; p < VEC / 2; ++p) {
                 const uint64_t xp = frag_pair(xv[k][c], p);
-                acc = f2_fma(xp, xp, acc);
+                const int j = (c * (VEC / 2) + p) & 3;
+                acc[j] = f2_fma(xp, xp, acc[j]);
             }
-    float acc_lo, acc_hi;
-    f2_unpack(acc, acc_lo, acc_hi);
-    const float inv = inv_rms(cta_allsum(acc_lo + acc_hi, slots, 1, 0, false), a.n, a.eps1);
+    float acc_lo[4], acc_hi[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f2_unpack(acc[j], acc_lo[j], acc_hi[j]);
+    const float part = ((acc_lo[0] + acc_hi[0]) + (acc_lo[1] + acc_hi[1])) +
+                       ((acc_lo[2] + acc_hi[2]) + (acc_lo[3] + acc_hi[3]));
+    const float inv = inv_rms(cta_allsum(part, slots, 1, 0, false), a.n, a.eps1);
     const uint64_t inv2 = f2_pack(inv, inv);
 
 #pragma unroll
@@ -1339,7 +1379,7 @@ mrn_q8_block_kernel(const KernelArgs a) {
         const int b = tid + k * static_cast<int>(blockDim.x);
         if (b >= nb) continue;
         uint64_t xn[NP];
-        float amax = 0.0f;
+        float m[NP];   // per-pair maxima, then a max tree (short chains)
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
             Frag<T, VEC> g;
@@ -1351,41 +1391,27 @@ mrn_q8_block_kernel(const KernelArgs a) {
                 xn[c * (VEC / 2) + p] = v;
                 float lo, hi;
                 f2_unpack(v, lo, hi);
-                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                m[c * (VEC / 2) + p] = fmaxf(fabsf(lo), fabsf(hi));
             }
         }
-        uint32_t words[1 + kQ8Block / 4];
-        words[0] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(amax / 127.0f)));
-        if (amax >= 0x1p-100f && amax <= 0x1p100f) {
-            const float id = __fdividef(127.0f, amax);
-            const uint64_t id2 = f2_pack(id, id);
-            const uint64_t sh2 = f2_pack(kRoundShift, kRoundShift);
 #pragma unroll
-            for (int q = 0; q < kQ8Block / 4; ++q) {
-                float c0, c1, c2, c3;
-                f2_unpack(f2_fma(xn[2 * q], id2, sh2), c0, c1);
-                f2_unpack(f2_fma(xn[2 * q + 1], id2, sh2), c2, c3);
-                words[1 + q] = pack4(__float_as_uint(c0), __float_as_uint(c1), __float_as_uint(c2),
-                                     __float_as_uint(c3));
-            }
-        } else {   // zero, tiny or huge amax: per-element IEEE division and clamps
-            const float d = amax / 127.0f;
+        for (int w = NP / 2; w > 0; w >>= 1)
 #pragma unroll
-            for (int q = 0; q < kQ8Block / 4; ++q) {
-                float v[4];
-                f2_unpack(xn[2 * q], v[0], v[1]);
-                f2_unpack(xn[2 * q + 1], v[2], v[3]);
-                uint32_t c[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    c[i] = static_cast<uint32_t>(
-                        d > 0.0f ? min(127, max(-128, __float2int_rn(v[i] / d))) : 0);
-                words[1 + q] = pack4(c[0], c[1], c[2], c[3]);
-            }
-        }
+            for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+        const float amax = m[0];
+        const bool fast = amax >= 0x1p-100f && amax <= 0x1p100f;
+        const float d = amax / 127.0f;
+        const float id = fast ? __fdividef(127.0f, amax) : 0.0f;
+        const uint64_t id2 = f2_pack(id, id);
         uint32_t *dst = reinterpret_cast<uint32_t *>(q8_row + b * kQ8BlockBytes);
+        dst[0] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(d)));
 #pragma unroll
-        for (int w = 0; w < 1 + kQ8Block / 4; ++w) dst[w] = words[w];
+        for (int c = 0; c < CH; ++c) {
+            uint32_t w[VEC / 4];
+            q8_chunk_words<VEC>(xn + c * (VEC / 2), fast, id2, d, w);
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q) dst[1 + c * (VEC / 4) + q] = w[q];
+        }
     }
     __syncthreads();
     // The row's blocks, shared -> global: 16-byte stores where the row allows.
@@ -1442,35 +1468,6 @@ cudaError_t launch_q8_blocks(const Geometry &g, KernelArgs a, int64_t rows, cuda
 // bank groups; register slot i then holds chunk (i + rot) % CH, and its codes
 // are written at that chunk's offset.  Each group assembles its row's blocks
 // in its own shared-memory buffer, then copies them out with coalesced stores.
-
-// Code words of one chunk slot (VEC elements = VEC / 2 f32 pairs), four codes
-// to a word: by the block reciprocal (fast) or by IEEE division and clamps.
-template <int VEC>
-__device__ __forceinline__ void q8_chunk_words(const uint64_t *xn, bool fast, uint64_t id2,
-                                               float d, uint32_t *w) {
-    constexpr float kRoundShift = 12582912.0f;   // 1.5 * 2^23
-    const uint64_t sh2 = f2_pack(kRoundShift, kRoundShift);
-#pragma unroll
-    for (int q = 0; q < VEC / 4; ++q) {
-        if (fast) {
-            float c0, c1, c2, c3;
-            f2_unpack(f2_fma(xn[2 * q], id2, sh2), c0, c1);
-            f2_unpack(f2_fma(xn[2 * q + 1], id2, sh2), c2, c3);
-            w[q] = pack4(__float_as_uint(c0), __float_as_uint(c1), __float_as_uint(c2),
-                         __float_as_uint(c3));
-        } else {
-            float v[4];
-            f2_unpack(xn[2 * q], v[0], v[1]);
-            f2_unpack(xn[2 * q + 1], v[2], v[3]);
-            uint32_t c[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                c[i] = static_cast<uint32_t>(
-                    d > 0.0f ? min(127, max(-128, __float2int_rn(v[i] / d))) : 0);
-            w[q] = pack4(c[0], c[1], c[2], c[3]);
-        }
-    }
-}
 
 template <class T, int KB, int G>
 __global__ void __launch_bounds__(G * kQ8TmaGroupThreads, 1)
@@ -1549,7 +1546,9 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
                 }
             }
         }
-        uint64_t acc = f2_pack(0.0f, 0.0f);
+        // four independent accumulators (short dependency chains)
+        uint64_t acc[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
+                           f2_pack(0.0f, 0.0f)};
 #pragma unroll
         for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
@@ -1557,12 +1556,16 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
 #pragma unroll
                 for (int p = 0; p < VEC / 2; ++p) {
                     const uint64_t xp = frag_pair(xv[kb][i], p);
-                    acc = f2_fma(xp, xp, acc);
+                    const int j = (i * (VEC / 2) + p) & 3;
+                    acc[j] = f2_fma(xp, xp, acc[j]);
                 }
-        float acc_lo, acc_hi;
-        f2_unpack(acc, acc_lo, acc_hi);
+        float acc_lo[4], acc_hi[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f2_unpack(acc[j], acc_lo[j], acc_hi[j]);
+        const float part = ((acc_lo[0] + acc_hi[0]) + (acc_lo[1] + acc_hi[1])) +
+                           ((acc_lo[2] + acc_hi[2]) + (acc_lo[3] + acc_hi[3]));
         int any_failed;
-        const float tot = wg_allsum<true>(acc_lo + acc_hi, slots[grp], bar_id, gsize, gtid,
+        const float tot = wg_allsum<true>(part, slots[grp], bar_id, gsize, gtid,
                                           failed | abort_flag, &any_failed);
         if (any_failed) {
             if (gtid == 0) abort_flag = 1;
@@ -1586,7 +1589,7 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
             const int b = gtid + kb * gsize;
             if (b >= nb) continue;
             uint64_t xn[NP];
-            float amax = 0.0f;
+            float m[NP];   // per-pair maxima, then a max tree (short chains)
 #pragma unroll
             for (int i = 0; i < CH; ++i) {
                 const int cc = (i + rot) & (CH - 1);
@@ -1600,9 +1603,14 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
                     xn[i * (VEC / 2) + p] = v;
                     float lo, hi;
                     f2_unpack(v, lo, hi);
-                    amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                    m[i * (VEC / 2) + p] = fmaxf(fabsf(lo), fabsf(hi));
                 }
             }
+#pragma unroll
+            for (int w = NP / 2; w > 0; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+            const float amax = m[0];
             const bool fast = amax >= 0x1p-100f && amax <= 0x1p100f;
             const float d = amax / 127.0f;
             const float id = fast ? __fdividef(127.0f, amax) : 0.0f;
