@@ -116,6 +116,34 @@ template <> struct Frag<BF16, 1> {
     }
 };
 
+// Two f32 lanes per instruction (mul.rn.f32x2 / fma.rn.f32x2: each half
+// rounded exactly as the scalar instruction would), on register pairs.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+// Elements 2p and 2p + 1 of a 16-byte fragment as an f32 pair.
+__device__ __forceinline__ uint64_t frag_pair(const Frag<BF16, 8> &f, int p) {
+    const uint32_t w = f.w[p];
+    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint64_t frag_pair(const Frag<F32, 4> &f, int p) {
+    return f2_pack(__uint_as_float(f.w[2 * p]), __uint_as_float(f.w[2 * p + 1]));
+}
 // ---------------------------------------------------------------------------
 // Global memory access.  `stream` = operand read once (bypass L1, 256-byte L2
 // prefetch); `ro` = read-only, cached (gamma); `st` = plain store; `ld` =
@@ -544,12 +572,16 @@ __device__ __forceinline__ void seam_output(const Frag<T, VEC> &x, float inv, co
                                             void *y, int64_t e) {
     constexpr bool BF = op_seam_bf16(OP);
     H16<VEC> u;
-    if (VEC == 1) {
+    if constexpr (VEC == 1) {
         u.w[0] = seam_pack1<BF>(x.get(0) * inv);
     } else {
+        const uint64_t inv2 = f2_pack(inv, inv);
 #pragma unroll
-        for (int i = 0; i < VEC / 2; ++i)
-            u.w[i] = seam_pack2<BF>(x.get(2 * i) * inv, x.get(2 * i + 1) * inv);
+        for (int i = 0; i < VEC / 2; ++i) {
+            float lo, hi;
+            f2_unpack(f2_mul(frag_pair(x, i), inv2), lo, hi);   // x * inv, two lanes at once
+            u.w[i] = seam_pack2<BF>(lo, hi);
+        }
     }
     void *p = static_cast<char *>(y) + e * 2;
     if (op_seam_weighted(OP)) {
@@ -1259,32 +1291,6 @@ constexpr int64_t kRowsPerLaunch = int64_t(1) << 26;
 // the row's blocks to global memory with coalesced 16-byte stores.  Needs
 // 16-byte aligned rows; n = 32 * (number of blocks).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-// Elements 2p and 2p + 1 of a 16-byte fragment as an f32 pair.
-__device__ __forceinline__ uint64_t frag_pair(const Frag<BF16, 8> &f, int p) {
-    const uint32_t w = f.w[p];
-    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-__device__ __forceinline__ uint64_t frag_pair(const Frag<F32, 4> &f, int p) {
-    return f2_pack(__uint_as_float(f.w[2 * p]), __uint_as_float(f.w[2 * p + 1]));
-}
 // Low bytes of four codes (each in the low byte of a word) packed in order.
 __device__ __forceinline__ uint32_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
     return __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
