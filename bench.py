@@ -198,15 +198,16 @@ class OracleRunner:
     """The oracle's sandwich tail over row blocks, one block per host thread
     (ctypes releases the GIL, so the blocks run in parallel)."""
 
-    def __init__(self, arrays64, n):
+    def __init__(self, arrays64, n, threads=None):
         import numpy as np
 
         import oracle
         self.np = np
         self.orc = oracle.default()
+        self.arrays64 = arrays64
         self.b, self.r, self.gp, self.gq = arrays64
         self.n = n
-        self.threads = os.cpu_count() or 1
+        self.threads = threads or os.cpu_count() or 1
         self.pool = ThreadPoolExecutor(max_workers=self.threads)
         self.eps_post = float(np.float32(1e-8))
         self.eps_pre = float(np.float32(1e-5))
@@ -233,6 +234,66 @@ class OracleRunner:
             passes += 1
         return (sandwich_bytes(rows, self.n) * passes / elapsed / 1e9, rows * passes / elapsed,
                 passes, elapsed)
+
+
+def oracle_configs(threads: int, seconds_each: float = 1.0):
+    """The oracle, as it stands, on the other workloads' inputs (bounded
+    samples, each timed for about `seconds_each`): single-threaded, and with
+    rows split over `threads` host threads where a workload has enough rows.
+    Units follow the GPU lines they sit beside (us per call for the decode
+    workloads, GB/s of algorithmic bytes for the batched ones)."""
+    import numpy as np
+
+    import oracle
+    from dual_epsilon_sandwich_gb300 import workloads as wl
+    orc = oracle.default()
+    pool = ThreadPoolExecutor(max_workers=threads)
+
+    def timed(fn):
+        fn()                                      # untimed first call (first touch)
+        calls, elapsed = 0, 0.0
+        while calls == 0 or elapsed < seconds_each:
+            t0 = time.perf_counter()
+            fn()
+            elapsed += time.perf_counter() - t0
+            calls += 1
+        return elapsed / calls
+
+    def split(fn, rows):
+        bounds = np.linspace(0, rows, threads + 1).astype(int)
+        return lambda: list(pool.map(lambda i: fn(int(bounds[i]), int(bounds[i + 1])),
+                                     range(threads)))
+
+    out = {}
+    w = wl.plain_decode_rows()
+    x, g = w.arrays["x"].astype(np.float64), w.arrays["gamma"].astype(np.float64)
+    e = float(np.float32(w.eps))
+    out[w.name] = {"us_per_call_1_thread": 1e6 * timed(lambda: orc.rmsnorm(x, g, e))}
+    w = wl.sandwich_decode()
+    b, r, gp, gq = (w.arrays[k].astype(np.float64) for k in
+                    ("block_out", "residual", "gamma_post", "gamma_pre"))
+    e1, e2 = float(np.float32(1e-8)), float(np.float32(1e-5))
+    out[w.name] = {"us_per_call_1_thread": 1e6 * timed(
+        lambda: orc.norm_residual_norm(b, r, gp, gq, e1, e2))}
+    rows = 1024                                   # a sample drawn as the 16384 rows are
+    w = wl.llama_bf16(rows=rows)
+    x = orc.double_from_bf16(w.arrays["x"])
+    res = orc.double_from_bf16(w.arrays["residual"])
+    g = orc.double_from_bf16(w.arrays["gamma"])
+    e = float(np.float32(w.eps))
+    n = w.n
+    for name, nbytes, one in (
+            ("rmsnorm_bf16_rows16384_n4096", (2 * rows * n + n) * 2,
+             lambda lo, hi: orc.rmsnorm(x[lo:hi], g, e)),
+            ("then_add_bf16_rows16384_n4096", (3 * rows * n + n) * 2,
+             lambda lo, hi: orc.rmsnorm_then_add(x[lo:hi], g, res[lo:hi], e))):
+        t1 = timed(lambda: one(0, rows))
+        tn = timed(split(one, rows))
+        out[name] = {"GB_per_s_1_thread": nbytes / t1 / 1e9,
+                     f"GB_per_s_{threads}_threads": nbytes / tn / 1e9,
+                     "sample": f"{rows} rows drawn as the workload's 16384 are"}
+    pool.shutdown()
+    return out
 
 
 def run_reference(args):
@@ -463,11 +524,19 @@ def run_mrn(args):
         runner = OracleRunner([a[k].astype(np.float64) for k in ("block_out", "residual",
                                                                  "gamma_post", "gamma_pre")], n)
         gbs, rps, passes, elapsed = runner.rate(rows, args.cpu_seconds)
+        single = OracleRunner(runner.arrays64, n, threads=1)
+        sample = min(rows, 256)
+        gbs1, _, passes1, elapsed1 = single.rate(sample, max(0.5, args.cpu_seconds / 5))
         line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": runner.threads,
                                 "kind": "oracle",
                                 "sample": f"all {rows} rows x {passes} passes ({elapsed:.1f} s), "
                                           f"rows split over {runner.threads} host threads",
-                                "rows_per_s": rps}
+                                "rows_per_s": rps,
+                                "single_thread": {"value": gbs1, "unit": UNIT,
+                                                  "sample": f"the first {sample} rows x "
+                                                            f"{passes1} passes ({elapsed1:.1f} s)"},
+                                "configs": oracle_configs(runner.threads,
+                                                          max(0.2, args.cpu_seconds / 10))}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
