@@ -48,7 +48,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("mrn", "reference"), default="mrn")
     p.add_argument("--rows", type=int, default=4096)
     p.add_argument("--n", type=int, default=6656)
-    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--decode-calls", type=int, default=2000)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -697,6 +697,7 @@ def secondary_workloads(dev, stream):
     torch.cuda.empty_cache()
     out.update(more_ops(dev, stream))
     out.update(seam_ops(dev, stream))
+    out["sweep_large_f32"] = sweep_large(dev, stream)
 
     w = wl.plain_decode_rows()
     nsets = 512
@@ -841,6 +842,55 @@ def profile_other(args, dev):
     print(json.dumps({"profile_op": args.profile_op, "rows": rows, "n": n,
                       "profile_launches": args.profile_launches, "geometry": geometry}))
     return 0
+
+
+def sweep_large(dev, stream):
+    """The sweep workload's shapes with rows x n >= 2^26 (f32, plain and
+    then-add, eps 1e-5): GB/s of algorithmic bytes, one buffer set (every
+    operand exceeds L2), seeded device-side random inputs."""
+    import torch
+
+    from dual_epsilon_sandwich_gb300 import mrn
+    sh = stream.cuda_stream
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20261205)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {}
+    for rows, n in ((65536, 2048), (65536, 5120), (65536, 6656), (65536, 8192),
+                    (65536, 16384), (4096, 16384), (4096, 65536)):
+        x = torch.randn(rows, n, device=dev, generator=gen)
+        r = torch.randn(rows, n, device=dev, generator=gen)
+        g = 1 + 0.1 * torch.randn(n, device=dev, generator=gen)
+        y = torch.empty_like(x)
+        entry = {}
+        for op, nbytes in (("rmsnorm", (2 * rows * n + n) * 4),
+                           ("then_add", (3 * rows * n + n) * 4)):
+            def call():
+                if op == "rmsnorm":
+                    st = mrn.mrn_rmsnorm(x.data_ptr(), g.data_ptr(), y.data_ptr(), rows, n, 1e-5,
+                                         mrn.MRN_F32, sh)
+                else:
+                    st = mrn.mrn_rmsnorm_then_add(x.data_ptr(), g.data_ptr(), r.data_ptr(),
+                                                  y.data_ptr(), rows, n, 1e-5, mrn.MRN_F32, sh)
+                if st != 0:
+                    raise mrn.MrnError(st, f"sweep {rows}x{n} {op}")
+            iters = max(5, min(200, int(2e9 // nbytes)))
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(iters):
+                call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / iters
+            entry[op] = {"GB_per_s": nbytes / (us * 1e-6) / 1e9, "us_per_call": us}
+        entry["geometry"] = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM, rows, n, mrn.MRN_F32,
+                                                   True)
+        out[f"rows{rows}_n{n}"] = entry
+        del x, r, y
+        torch.cuda.empty_cache()
+    return out
 
 
 def seam_ops(dev, stream):

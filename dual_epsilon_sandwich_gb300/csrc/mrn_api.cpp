@@ -228,6 +228,12 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     }
     constexpr int64_t kCtaLoads = 2048;
     int64_t cl = ceil_div(nvec, kCtaLoads);
+    // Batches of wide f32 rows: half the loads per CTA (four register slots),
+    // up to clusters of 8 (measured on GB300: 65536 x 16384 plain 5.28 vs 4.94
+    // TB/s, then-add 5.91 vs 5.47; 8192 x 32768 plain 4.91 vs 4.68).  bf16
+    // rows were faster with the full 2048 loads per CTA.
+    if (dt == MRN_F32 && rows >= sms && cl >= 2 && ceil_div(nvec, kCtaLoads / 2) <= 8)
+        cl = ceil_div(nvec, kCtaLoads / 2);
     if (cl > mrn::kMaxCluster) {
         g.kind = mrn::kStream;
         g.threads = mrn::kStreamMaxThreads;
