@@ -226,6 +226,25 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
             return g;
         }
     }
+    // Batches of rows of 2049..4096 loads: a cluster of two CTAs per row, each
+    // staging its half two rows ahead (measured on GB300 against the register
+    // cluster kernel: f32 n = 16384 plain 6.01 vs 5.28 TB/s, then-add-scale
+    // 5.67 vs 5.43, then-add even; bf16 n = 32768 plain 5.84 vs 4.73, then-add
+    // 5.53 vs 4.06, sandwich 4.53 vs 3.51).  The f32 sandwich ran slower staged
+    // (4.29 vs 4.70) and keeps the register cluster kernel.
+    if (mrn::op_has_cluster_staging(op) && aligned16 && rows >= sms && nvec > 2048 &&
+        nvec <= 4096 && (op != mrn::kSandwich || dt == MRN_BF16) && row_bytes % 32 == 0 &&
+        (mrn::op_gammas(op) + 2 * mrn::op_row_inputs(op)) * (row_bytes / 2) <= kTmaSharedBudget) {
+        g.kind = mrn::kTma;
+        g.cluster = 2;
+        g.groups = 1;
+        g.stages = 2;
+        g.ctas = 0;
+        pick_threads(ceil_div(nvec, 2), &g.k, &g.threads);
+        g.lanes = 0;
+        g.rows_per_cta = 1;
+        return g;
+    }
     constexpr int64_t kCtaLoads = 2048;
     int64_t cl = ceil_div(nvec, kCtaLoads);
     // Batches of wide f32 rows: half the loads per CTA (four register slots),
@@ -286,6 +305,8 @@ bool geometry_is_consistent(const Geometry &g) {
     }
     if (g.kind == mrn::kTma) {
         if (g.groups < 1 || g.groups > mrn::kTmaMaxGroups) return false;
+        if (g.cluster < 1 || g.cluster > mrn::kMaxCluster) return false;
+        if (g.cluster > 1 && g.groups != 1) return false;   // one group per CTA of a cluster
         const int per_group = g.threads / g.groups;
         return g.k >= 1 && g.k <= mrn::kMaxK && g.threads % (32 * g.groups) == 0 &&
                per_group >= 32 && g.threads <= mrn::tma_max_threads(g.k, g.groups) &&
@@ -312,6 +333,18 @@ bool resolve_forced(Geometry g, mrn::Op op, int64_t n, mrn_dtype dt, bool aligne
         g.cluster = 1;
         g.lanes = 0;
         g.rows_per_cta = g.stages > 0 ? g.groups : 1;
+    } else if (g.kind == mrn::kTma && g.cluster > 1) {
+        // a cluster per row: each CTA stages a 16-byte-aligned slice
+        if (!mrn::op_has_cluster_staging(op)) return false;
+        if (!aligned16 || g.vec != natural_vec(dt)) return false;
+        const int64_t row_bytes = n * elem_bytes(dt);
+        if (row_bytes % (16 * g.cluster) != 0) return false;
+        if (static_cast<int64_t>(g.threads) * g.k < nvec / g.cluster) return false;
+        if ((mrn::op_gammas(op) + g.stages * mrn::op_row_inputs(op)) * (row_bytes / g.cluster) >
+            kTmaSharedBudget)
+            return false;
+        g.lanes = 0;
+        g.rows_per_cta = 1;
     } else if (g.kind == mrn::kTma) {
         if (!aligned16 || g.vec != natural_vec(dt)) return false;
         if (static_cast<int64_t>(g.threads / g.groups) * g.k < nvec) return false;
@@ -731,7 +764,8 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry) {
         g.groups = 1;
     if (g.kind == mrn::kRowsPerWarp && g.threads == 0) g.threads = mrn::kWarpKernelThreads;
     if (g.kind == mrn::kStream) g.k = 1;
-    if (g.kind != mrn::kCta) g.cluster = 1;
+    if (g.kind == mrn::kTma && g.cluster == 0) g.cluster = 1;
+    if (g.kind != mrn::kCta && g.kind != mrn::kTma) g.cluster = 1;
     if (!geometry_is_consistent(g) || g.vec < 0) return MRN_ERR_INVALID_GEOMETRY;
     t_forced_geometry = g;
     t_forced = true;

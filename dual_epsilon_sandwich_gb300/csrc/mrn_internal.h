@@ -149,6 +149,11 @@ cudaError_t launch_seam_scale(bool seam_bf16, const void *u, const void *gamma, 
 constexpr int64_t tma_shared_bytes(int op, int64_t row_bytes, int stages) {
     return row_bytes * (op_staged_gammas(op) + stages * op_row_inputs(op));
 }
+// The staged kernel with a cluster of `cluster` CTAs per row (each stages a
+// slice of row_bytes / cluster): plain, then-add, then-add-scale, sandwich.
+MRN_HOST_DEVICE constexpr bool op_has_cluster_staging(int op) {
+    return op == kRmsnorm || op == kThenAdd || op == kSandwich || op == kThenAddScale;
+}
 
 // Number of bounded waits that ran out since the last call (and reset them).
 int take_wait_timeouts_rmsnorm();

@@ -241,6 +241,11 @@ __device__ __forceinline__ unsigned cluster_index_x() {
     asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
     return r;
 }
+__device__ __forceinline__ unsigned cluster_count_x() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
@@ -256,6 +261,14 @@ __device__ __forceinline__ void st_cluster_f32(float *local, unsigned rank, floa
     unsigned remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
     asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(remote), "f"(v) : "memory");
+}
+
+// Store v into the shared-memory word `local` of CTA `rank` of this cluster.
+__device__ __forceinline__ void st_cluster_u32(int *local, unsigned rank, int v) {
+    const unsigned a = static_cast<unsigned>(__cvta_generic_to_shared(local));
+    unsigned remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(remote), "r"(v) : "memory");
 }
 
 struct ReduceSlots {
@@ -1250,6 +1263,211 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Staged kernel for rows too wide for one CTA's registers: a thread-block
+// cluster of C CTAs handles one row at a time, CTA `crank` owning slice
+// [crank * S, (crank + 1) * S) of it (S = n / C elements, a multiple of 16
+// bytes).  Persistent: cluster c takes rows c, c + (number of clusters), ...
+// Each CTA bulk-copies its slice of a future row (and of the residual) into
+// a shared-memory stage, `stages` rows ahead, and its slice of the gammas
+// once.  A row's sum is the CTA sums exchanged through distributed shared
+// memory: each CTA writes its partial (and its failure flag) into slot
+// [parity][crank] of every peer, then a release/acquire cluster barrier,
+// then every CTA adds the C partials in rank order (all CTAs get the same
+// bits).  The slots alternate with the row's parity: a CTA writes row j+1's
+// partials only after row j's barrier, and reaches row j+1's barrier only
+// after reading row j's slots, so a slot is never overwritten while a peer
+// may still read it.  Every thread of every CTA reaches every cluster barrier
+// (all CTAs of a cluster walk the same rows); a failed (bounded) stage wait
+// is voted on in the same exchange, so the whole cluster stops at one row,
+// then each CTA drains its own copies.  Operations: plain, then-add,
+// then-add-scale and the sandwich.
+// ---------------------------------------------------------------------------
+struct ClusterSlots {
+    float warp[32];
+    float cta[2][kMaxCluster];   // [row parity][rank of the writing CTA]
+    int fail[2][kMaxCluster];
+};
+
+// Sum of v over the cluster (every thread of every CTA calls it), with the
+// OR of `flag` over the cluster in *any_fail.  `first` completes the arrive
+// issued at kernel start (every peer is running before its memory is written).
+__device__ __forceinline__ float cluster_row_sum(float v, ClusterSlots &s, unsigned cl,
+                                                 unsigned crank, int parity, int flag,
+                                                 int *any_fail, bool first) {
+    v = warp_allsum(v);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    if (lane == 0) s.warp[warp] = v;
+    __syncthreads();
+    const float t = warp_allsum(lane < nwarps ? s.warp[lane] : 0.0f);
+    const int f = __syncthreads_or(flag);
+    if (first) cluster_wait_acquire();
+    if (threadIdx.x < cl) {
+        st_cluster_f32(&s.cta[parity][crank], threadIdx.x, t);
+        st_cluster_u32(&s.fail[parity][crank], threadIdx.x, f);
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();
+    const bool mine = lane < static_cast<int>(cl);
+    *any_fail = __any_sync(0xFFFFFFFFu, mine && s.fail[parity][lane] != 0);
+    return warp_allsum(mine ? s.cta[parity][lane] : 0.0f);
+}
+
+template <int OP, class T, int K>
+__global__ void __launch_bounds__(cta_max_threads(K), 1)
+mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
+    constexpr int VEC = 16 / T::kBytes;
+    using Fr = Frag<T, VEC>;
+    constexpr int NS = op_row_inputs(OP);   // row operands staged per row
+    constexpr int NG = op_gammas(OP);       // gamma slices kept in shared memory
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ ClusterSlots slots1;
+    __shared__ ClusterSlots slots2;
+    __shared__ __align__(8) uint64_t bars[kTmaMaxStages + 1];   // [stages] = the gammas
+    __shared__ int issued[kTmaMaxStages];
+    __shared__ int consumed[kTmaMaxStages];
+    pdl_enter();
+    const unsigned cl = cluster_nctarank();
+    const unsigned crank = cluster_ctarank();
+    cluster_arrive_relaxed();
+    const int64_t slice = a.n / cl;                    // elements of a row per CTA
+    const uint32_t sb = static_cast<uint32_t>(slice * T::kBytes);
+    const int64_t svec = slice / VEC;
+    unsigned char *const gsm = smem;
+    unsigned char *const stage0 = smem + NG * sb;
+    const int tid = threadIdx.x;
+    const int nt = blockDim.x;
+    const int64_t first = a.row0 + cluster_index_x();
+    const int64_t step = cluster_count_x();
+    const int64_t my_rows = first < a.rows_end ? (a.rows_end - first + step - 1) / step : 0;
+    const int64_t row_bytes = a.n * T::kBytes;
+    const int64_t soff = static_cast<int64_t>(crank) * sb;   // this CTA's slice in a row
+    const char *const xg = static_cast<const char *>(a.x) + soff;
+    const char *const rg = static_cast<const char *>(a.res) + soff;
+    const bool bad_stages = stages < 1 || stages > kTmaMaxStages;
+
+    if (tid == 0) {
+        for (int st = 0; st <= stages && st <= kTmaMaxStages; ++st) mbar_init(&bars[st], 1);
+        for (int st = 0; st < kTmaMaxStages; ++st) issued[st] = consumed[st] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0 && my_rows > 0 && !bad_stages) {
+        mbar_arrive_expect_tx(&bars[stages], NG * sb);
+        bulk_to_shared(gsm, static_cast<const char *>(a.g1) + soff, sb, &bars[stages]);
+        if (NG == 2) bulk_to_shared(gsm + sb, static_cast<const char *>(a.g2) + soff, sb,
+                                    &bars[stages]);
+        for (int st = 0; st < stages && st < my_rows; ++st) {
+            stage_row<NS>(stage0 + st * NS * sb, xg, rg, (first + st * step) * row_bytes, sb,
+                          &bars[st]);
+            issued[st] = 1;
+        }
+    }
+    // (the host never launches bad_stages; the kernel then only votes to stop)
+    int failed = bad_stages ? 1 : ((my_rows > 0 && !mbar_wait_bounded(&bars[stages], 0)) ? 1 : 0);
+    const float sc = load_out_scale<OP, T>(a.scale);
+    bool first_sum = true;
+    int stopped = 0;
+
+    for (int64_t it = 0; it < my_rows; ++it) {
+        const int s = bad_stages ? 0 : static_cast<int>(it % stages);
+        const uint32_t parity = bad_stages ? 0u : static_cast<uint32_t>((it / stages) & 1);
+        const int64_t row = first + it * step;
+        const int slot = static_cast<int>(it & 1);
+        if (!failed && !mbar_wait_bounded(&bars[s], parity)) failed = 1;
+
+        Fr xv[K];
+        Fr rv[K];
+        const unsigned char *sp = stage0 + s * NS * sb;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int64_t v = tid + static_cast<int64_t>(k) * nt;
+            if (v < svec && !failed) {
+                ld_shared(xv[k], sp + v * 16);
+                if (NS == 2) ld_shared(rv[k], sp + sb + v * 16);
+            } else {
+                xv[k].zero();
+                rv[k].zero();
+            }
+        }
+        float ss = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) ss += frag_sum_sq(xv[k]);
+        int any_failed;
+        const float tot = cluster_row_sum(ss, slots1, cl, crank, slot, failed, &any_failed,
+                                          first_sum);
+        first_sum = false;
+        if (any_failed) {
+            stopped = 1;
+            break;
+        }
+        // Every thread holds its part of the stage now (the barrier above): refill it.
+        if (tid == 0) {
+            consumed[s] += 1;
+            if (it + stages < my_rows) {
+                fence_proxy_async_smem();
+                stage_row<NS>(stage0 + s * NS * sb, xg, rg,
+                              (first + (it + stages) * step) * row_bytes, sb, &bars[s]);
+                issued[s] += 1;
+            }
+        }
+        const float inv1 = inv_rms(tot, a.n, a.eps1);
+        const int64_t row_elem = row * a.n + static_cast<int64_t>(crank) * slice;
+        if (OP != kSandwich) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int64_t v = tid + static_cast<int64_t>(k) * nt;
+                if (v >= svec) continue;
+                Fr g;
+                ld_shared(g, gsm + v * 16);
+                st_global(elem_ptr<T>(a.y, row_elem + v * VEC),
+                          single_norm_output<OP>(xv[k], inv1, g, rv[k], sc));
+            }
+            continue;
+        }
+        float ss2 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int64_t v = tid + static_cast<int64_t>(k) * nt;
+            if (v >= svec) continue;
+            Fr g;
+            ld_shared(g, gsm + v * 16);
+            rv[k] = apply_norm_add(xv[k], inv1, g, rv[k]);
+            st_global(elem_ptr<T>(a.y, row_elem + v * VEC), rv[k]);
+            ss2 += frag_sum_sq(rv[k]);
+        }
+        int unused;
+        const float inv2 = inv_rms(cluster_row_sum(ss2, slots2, cl, crank, slot, 0, &unused,
+                                                   false),
+                                   a.n, a.eps2);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int64_t v = tid + static_cast<int64_t>(k) * nt;
+            if (v >= svec) continue;
+            Fr g;
+            ld_shared(g, gsm + sb + v * 16);
+            st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(rv[k], inv2, g));
+        }
+    }
+    if (first_sum) cluster_wait_acquire();   // (no row: complete the start-up arrive)
+
+    // Exit: after a stop, wait (bounded) for this CTA's copies still in flight
+    // before it leaves its shared memory.
+    __syncthreads();
+    if (tid == 0 && my_rows > 0 && stopped) {
+        if (failed) atomicAdd(&g_wait_timeouts, 1u);
+        if (!bad_stages) {
+            (void)mbar_wait_bounded(&bars[stages], 0);
+            for (int st = 0; st < stages; ++st) {
+                if (issued[st] > consumed[st])
+                    (void)mbar_wait_bounded(&bars[st], static_cast<uint32_t>(consumed[st] & 1));
+            }
+        }
+    }
+}
+
 // Persistent grid of the staged kernel: as many CTAs as fit on the device
 // (SM count x CTAs per SM), at most one per row.  Occupancy answers are
 // cached per (kernel, threads, shared bytes); the SM count per device.
@@ -1822,6 +2040,84 @@ cudaError_t launch_tma(const Geometry &g, KernelArgs a, int64_t rows, cudaStream
     return cudaSuccess;
 }
 
+template <int OP, class T> struct TmaClusterTable {
+    static constexpr WarpKernelFn fn[kMaxK] = {
+        mrn_tma_cluster_kernel<OP, T, 1>, mrn_tma_cluster_kernel<OP, T, 2>,
+        mrn_tma_cluster_kernel<OP, T, 3>, mrn_tma_cluster_kernel<OP, T, 4>,
+        mrn_tma_cluster_kernel<OP, T, 5>, mrn_tma_cluster_kernel<OP, T, 6>,
+        mrn_tma_cluster_kernel<OP, T, 7>, mrn_tma_cluster_kernel<OP, T, 8>};
+};
+
+// Persistent grid of clusters: as many clusters as can be resident at once
+// (cudaOccupancyMaxActiveClusters), at most one per row.
+template <int OP, class T>
+cudaError_t launch_tma_cluster(const Geometry &g, KernelArgs a, int64_t rows, cudaStream_t stream,
+                               uint64_t *launches) {
+    static TmaLaunchCache cache[kMaxCachedDevices][kMaxK];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    TmaLaunchCache uncached;
+    TmaLaunchCache &c = (dev >= 0 && dev < kMaxCachedDevices) ? cache[dev][g.k - 1] : uncached;
+    const WarpKernelFn fn = TmaClusterTable<OP, T>::fn[g.k - 1];
+    const int64_t slice_bytes = a.n / g.cluster * T::kBytes;
+    const int64_t shared = slice_bytes * (op_gammas(OP) + g.stages * op_row_inputs(OP));
+    cudaError_t err;
+    if (c.shared_opened.load(std::memory_order_relaxed) < shared) {
+        err = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(shared));
+        if (err != cudaSuccess) return err;
+        c.shared_opened.store(shared, std::memory_order_relaxed);
+    }
+    if (g.cluster > 8) {   // (independent of the shared-memory size opened above)
+        err = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
+                                   cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    cfg.blockDim = dim3(g.threads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(shared);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(g.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    int64_t clusters = g.ctas > 0 ? g.ctas / g.cluster : 0;
+    if (clusters <= 0) {
+        const int64_t key = shared * 4096 + g.threads * 16 + g.cluster;
+        int resident = c.occ_key.load(std::memory_order_relaxed) == key
+                           ? c.occ_per_sm.load(std::memory_order_relaxed) : 0;
+        if (resident == 0) {
+            cfg.gridDim = dim3(static_cast<unsigned>(g.cluster), 1, 1);
+            err = cudaOccupancyMaxActiveClusters(&resident, fn, &cfg);
+            if (err != cudaSuccess) return err;
+            if (resident < 1) return cudaErrorInvalidConfiguration;
+            c.occ_per_sm.store(resident, std::memory_order_relaxed);
+            c.occ_key.store(key, std::memory_order_relaxed);
+        }
+        clusters = resident;
+    }
+    if (g.pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
+    for (int64_t r0 = 0; r0 < rows; r0 += kRowsPerLaunch) {
+        const int64_t nrows = rows - r0 < kRowsPerLaunch ? rows - r0 : kRowsPerLaunch;
+        a.row0 = r0;
+        a.rows_end = r0 + nrows;
+        const int64_t nclusters = clusters < nrows ? clusters : nrows;
+        cfg.gridDim = dim3(static_cast<unsigned>(nclusters * g.cluster), 1, 1);
+        err = cudaLaunchKernelEx(&cfg, fn, a, g.stages);
+        if (err != cudaSuccess) return err;
+        ++*launches;
+    }
+    return cudaSuccess;
+}
+
 template <int OP> int take_wait_timeouts() {
     unsigned int count = 0, zero = 0;
     if (cudaMemcpyFromSymbol(&count, g_wait_timeouts, sizeof(count)) != cudaSuccess) return -1;
@@ -1894,6 +2190,13 @@ cudaError_t launch_op(bool bf16, const Geometry &g, const KernelArgs &a, int64_t
             return bf16 ? launch_q8_blocks<BF16>(g, a, rows, stream, launches)
                         : launch_q8_blocks<F32>(g, a, rows, stream, launches);
         }
+    }
+    if (g.kind == kTma && g.cluster > 1) {
+        if constexpr (op_has_cluster_staging(OP)) {
+            return bf16 ? launch_tma_cluster<OP, BF16>(g, a, rows, stream, launches)
+                        : launch_tma_cluster<OP, F32>(g, a, rows, stream, launches);
+        }
+        return cudaErrorInvalidConfiguration;
     }
     if (g.kind == kTma) {
         return bf16 ? launch_tma<OP, BF16>(g, a, rows, stream, launches)

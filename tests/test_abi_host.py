@@ -252,13 +252,16 @@ def test_geometry_covers_every_row_width():
                                 assert g["threads"] % 32 == 0
                         elif g["kind"] == mrn.MRN_GEOM_TMA:
                             assert a16 and rows >= 152
+                            cl = g["cluster"]
                             per_group = g["threads"] // g["groups"]
-                            assert per_group * g["k"] >= nvec and per_group % 32 == 0
+                            assert per_group * g["k"] * cl >= nvec and per_group % 32 == 0
                             assert 2 <= g["stages"] <= 4 and g["ctas"] == 0
                             assert g["groups"] in (1, 2) and g["stages"] % g["groups"] == 0
+                            assert cl == 1 or (g["groups"] == 1 and op in (0, 1, 2, 4) and
+                                               (n * e) % (16 * cl) == 0)
                             ng = 2 if op == 2 else (0 if op in (6, 7) else 1)
                             ns = 1 if op in (0, 5, 6, 7) else 2
-                            assert (ng + g["stages"] * ns) * n * e <= 232448 - 1024
+                            assert (ng + g["stages"] * ns) * n * e // cl <= 232448 - 1024
                         else:
                             assert g["kind"] == mrn.MRN_GEOM_STREAM
                             assert nvec > 16 * 2048

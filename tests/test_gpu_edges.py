@@ -291,6 +291,11 @@ FORCED_TMA = [
     ({"kind": 4, "k": 4, "threads": 256, "stages": 4, "groups": 2, "ctas": 19}, 250, 500),
     ({"kind": 4, "k": 2, "threads": 192, "stages": 2, "groups": 2, "ctas": 3}, 190, 101),
     ({"kind": 4, "k": 1, "threads": 64, "stages": 4, "groups": 2, "ctas": 1}, 20, 9),
+    # a cluster per row, each CTA staging a slice of it
+    ({"kind": 4, "k": 2, "threads": 128, "stages": 2, "cluster": 4}, 1024, 300),
+    ({"kind": 4, "k": 1, "threads": 64, "stages": 3, "cluster": 2, "ctas": 6}, 128, 101),
+    ({"kind": 4, "k": 4, "threads": 256, "stages": 2, "cluster": 8}, 8192, 64),
+    ({"kind": 4, "k": 2, "threads": 64, "stages": 1, "cluster": 16}, 2048, 40),
 ]
 
 
