@@ -59,9 +59,11 @@ def parse_args(argv=None):
                    help="skip the bf16 16384x4096 and f32 4x6656 secondary measurements")
     p.add_argument("--profile-launches", type=int, default=0,
                    help="only run --warmup + this many launches of the timed call (for ncu)")
-    p.add_argument("--profile-op", choices=("sandwich", "seam_f16", "q8_1"), default="sandwich",
+    p.add_argument("--profile-op", choices=("sandwich", "seam_f16", "q8_1", "wide_f32"),
+                   default="sandwich",
                    help="with --profile-launches: the call to launch -- the timed sandwich, the "
-                        "fused f16 seam at the same shape, or RMSNorm + Q8_1 at 16384 x 4096 bf16")
+                        "fused f16 seam at the same shape, RMSNorm + Q8_1 at 16384 x 4096 bf16, "
+                        "or plain f32 RMSNorm at 1024 x 65536")
     return p.parse_args(argv)
 
 
@@ -823,6 +825,17 @@ def profile_other(args, dev):
             return mrn.mrn_rmsnorm_seam(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), rows,
                                         n, 1e-5, mrn.MRN_F32, mrn.MRN_F16, sh)
         geometry = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM_SEAM, rows, n, mrn.MRN_F32, True)
+    elif args.profile_op == "wide_f32":
+        # plain f32 RMSNorm of 256 KB rows (the cluster-staged kernel, 8 CTAs a row)
+        rows, n = 1024, 65536
+        sets = [(torch.randn(rows, n, device=dev, generator=gen),
+                 1 + 0.1 * torch.randn(n, device=dev, generator=gen),
+                 torch.empty(rows, n, device=dev)) for _ in range(2)]
+
+        def call(t):
+            return mrn.mrn_rmsnorm(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), rows, n,
+                                   1e-5, mrn.MRN_F32, sh)
+        geometry = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM, rows, n, mrn.MRN_F32, True)
     else:
         rows, n = 16384, 4096
         sets = [(torch.randn(rows, n, device=dev, generator=gen).bfloat16(),

@@ -126,6 +126,9 @@ constexpr int64_t kTmaSharedBudget = mrn::kSharedBytesPerCta - 1024;
 //  * at least one row per SM, 16-byte aligned rows, nvec <= 2048, and two
 //    rows' operands fit in shared memory: the persistent TMA-staged kernel,
 //    two warp groups, one stage each;
+//  * at least one row per SM, 16-byte aligned slices, 2048 < nvec <= 16 *
+//    2048 (plain, then-add, then-add-scale, sandwich): the persistent
+//    cluster-staged kernel, a cluster of 2..16 CTAs per row;
 //  * nvec <= 16 * 2048: the row in registers of one CTA or of a cluster of up
 //    to 16 CTAs (2048 loads per CTA at most).  Few rows (decode) are spread
 //    over up to 8 CTAs of a cluster so that more SMs pull the row in.
@@ -226,24 +229,44 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
             return g;
         }
     }
-    // Batches of rows of 2049..4096 loads: a cluster of two CTAs per row, each
-    // staging its half two rows ahead (measured on GB300 against the register
-    // cluster kernel: f32 n = 16384 plain 6.01 vs 5.28 TB/s, then-add-scale
-    // 5.67 vs 5.43, then-add even; bf16 n = 32768 plain 5.84 vs 4.73, then-add
-    // 5.53 vs 4.06, sandwich 4.53 vs 3.51).  The f32 sandwich ran slower staged
-    // (4.29 vs 4.70) and keeps the register cluster kernel.
+    // Batches of rows wider than 2048 loads: a cluster of C CTAs per row (C the
+    // smallest power of two giving slices of at most 2048 loads = 32 KB), each
+    // staging its slice of future rows in shared memory, the partial sums sent
+    // as st.async messages.  Stages: plain 3 at C = 2, else 2; then-add (and
+    // -scale) 2 up to C = 4, then 3; sandwich 2, with C doubled from 8 so two
+    // CTAs fit per SM.  Measured on GB300 (TB/s; staged vs the register
+    // cluster kernel it replaces): f32 4096 x 16384 plain 6.41 vs 5.06,
+    // then-add 6.62 vs 5.52; 65536 x 16384 plain 6.79 vs 5.28; 8192 x 32768
+    // plain 6.43 vs 4.91, then-add 6.77 vs 5.14; 4096 x 65536 plain 6.64 vs
+    // 4.31, then-add 6.88 vs 4.93, sandwich 5.94 vs 3.03; sandwich 16384 x
+    // 16384 6.55 vs 4.65; bf16 8192 x 32768 plain 6.27 vs 4.73, then-add 6.72
+    // vs 4.06.  (The other stage counts lost 5-20 %: with one CTA per SM a
+    // cluster of 8 packs the GPCs less well, and deeper staging of two
+    // operands overfilled the SM.)
     if (mrn::op_has_cluster_staging(op) && aligned16 && rows >= sms && nvec > 2048 &&
-        nvec <= 4096 && (op != mrn::kSandwich || dt == MRN_BF16) && row_bytes % 32 == 0 &&
-        (mrn::op_gammas(op) + 2 * mrn::op_row_inputs(op)) * (row_bytes / 2) <= kTmaSharedBudget) {
-        g.kind = mrn::kTma;
-        g.cluster = 2;
-        g.groups = 1;
-        g.stages = 2;
-        g.ctas = 0;
-        pick_threads(ceil_div(nvec, 2), &g.k, &g.threads);
-        g.lanes = 0;
-        g.rows_per_cta = 1;
-        return g;
+        nvec <= static_cast<int64_t>(mrn::kMaxCluster) * 2048) {
+        int64_t ccl = 2;
+        while (ccl * 2048 < nvec) ccl *= 2;
+        if (op == mrn::kSandwich && ccl >= 8 && ccl < mrn::kMaxCluster) ccl *= 2;
+        int stages = 2;
+        if (op == mrn::kRmsnorm && ccl == 2) stages = 3;
+        if ((op == mrn::kThenAdd || op == mrn::kThenAddScale) && ccl >= 8) stages = 3;
+        const int64_t slice = row_bytes / ccl;
+        auto fits = [&](int st) {
+            return (mrn::op_gammas(op) + st * mrn::op_row_inputs(op)) * slice <= kTmaSharedBudget;
+        };
+        if (!fits(stages)) stages = 2;
+        if (row_bytes % (16 * ccl) == 0 && fits(stages)) {
+            g.kind = mrn::kTma;
+            g.cluster = static_cast<int>(ccl);
+            g.groups = 1;
+            g.stages = stages;
+            g.ctas = 0;
+            pick_threads(nvec / ccl, &g.k, &g.threads);
+            g.lanes = 0;
+            g.rows_per_cta = 1;
+            return g;
+        }
     }
     constexpr int64_t kCtaLoads = 2048;
     int64_t cl = ceil_div(nvec, kCtaLoads);

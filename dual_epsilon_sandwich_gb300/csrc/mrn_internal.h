@@ -92,7 +92,7 @@ constexpr int kMaxK = 8;
 constexpr int kWarpKernelThreads = 256;
 constexpr int kStreamMaxThreads = 512;
 constexpr int kMaxCluster = 16;
-constexpr int kTmaMaxStages = 4;
+constexpr int kTmaMaxStages = 8;
 constexpr int kSharedBytesPerCta = 232448;    // 227 KB opt-in limit on sm_100 / sm_103
 constexpr int cta_max_threads(int k) { return k <= 2 ? 1024 : (k <= 4 ? 512 : 256); }
 // Staged kernel: threads per warp group, and per CTA for 1 or 2 groups.

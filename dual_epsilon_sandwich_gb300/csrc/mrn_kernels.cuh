@@ -1270,49 +1270,91 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
 // bytes).  Persistent: cluster c takes rows c, c + (number of clusters), ...
 // Each CTA bulk-copies its slice of a future row (and of the residual) into
 // a shared-memory stage, `stages` rows ahead, and its slice of the gammas
-// once.  A row's sum is the CTA sums exchanged through distributed shared
-// memory: each CTA writes its partial (and its failure flag) into slot
-// [parity][crank] of every peer, then a release/acquire cluster barrier,
-// then every CTA adds the C partials in rank order (all CTAs get the same
-// bits).  The slots alternate with the row's parity: a CTA writes row j+1's
-// partials only after row j's barrier, and reaches row j+1's barrier only
-// after reading row j's slots, so a slot is never overwritten while a peer
-// may still read it.  Every thread of every CTA reaches every cluster barrier
-// (all CTAs of a cluster walk the same rows); a failed (bounded) stage wait
-// is voted on in the same exchange, so the whole cluster stops at one row,
-// then each CTA drains its own copies.  Operations: plain, then-add,
-// then-add-scale and the sandwich.
+// once.  A row's sum is the CTA sums exchanged as messages: each CTA sends
+// {partial, stop vote} to every peer with st.async, which lands in the
+// peer's mailbox [row parity][sender rank] and completes the peer's
+// mailbox mbarrier for that parity (armed by the peer for (C - 1) * 8
+// bytes); a CTA waits (bounded) on its own mbarrier, then every CTA adds the
+// C partials in rank order, its own from registers (all CTAs get the same
+// bits).  No cluster-wide barrier per row, so no row waits for the previous
+// row's output stores to drain.  Mailboxes alternate with the row's parity:
+// a CTA sends row j + 2's message only after it has received every peer's
+// row j + 1 message, and a peer sends that only after it has read its row j
+// mailbox, so a mailbox is never overwritten while it may still be read and
+// no message lands in a later phase of the mbarrier than the one awaited.
+// All CTAs of a cluster walk the same rows; a failed (bounded) stage wait is
+// the stop vote, so the whole cluster stops at one row, then each CTA
+// drains its own copies.  A cluster barrier at start (after the mbarriers
+// are initialised) and one at exit (no CTA leaves while a message may still
+// be addressed to it) are the only cluster-wide barriers.  Operations:
+// plain, then-add, then-add-scale and the sandwich.
 // ---------------------------------------------------------------------------
-struct ClusterSlots {
+struct ClusterMail {
     float warp[32];
-    float cta[2][kMaxCluster];   // [row parity][rank of the writing CTA]
-    int fail[2][kMaxCluster];
+    uint2 box[2][kMaxCluster];   // [row parity][sender rank] = {partial bits, stop vote}
+    uint64_t bar[2];             // [row parity]: every peer's message for that row landed
 };
 
-// Sum of v over the cluster (every thread of every CTA calls it), with the
-// OR of `flag` over the cluster in *any_fail.  `first` completes the arrive
-// issued at kernel start (every peer is running before its memory is written).
-__device__ __forceinline__ float cluster_row_sum(float v, ClusterSlots &s, unsigned cl,
-                                                 unsigned crank, int parity, int flag,
-                                                 int *any_fail, bool first) {
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return done != 0;
+}
+// Bounded like mbar_wait_bounded, for mbarriers completed by peers' messages.
+__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1; i < (1u << 28); ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) break;
+    }
+    return false;
+}
+// Store {x, y} into `box` of CTA `rank` of this cluster, completing 8 bytes
+// of the transaction count of that CTA's `bar`.
+__device__ __forceinline__ void send_pair(uint2 *box, uint64_t *bar, unsigned rank, uint32_t x,
+                                          uint32_t y) {
+    uint32_t rbox, rbar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbox) : "r"(smem_addr(box)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(smem_addr(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];"
+                 :: "r"(rbox), "r"(x), "r"(y), "r"(rbar) : "memory");
+}
+
+// Sum of v over the cluster for row `it` of this CTA (every thread of every
+// CTA calls it).  *stop is set (uniformly over the CTA) when any CTA voted
+// `flag` or a message did not arrive in time; *timed_out when the latter
+// happened to this thread.  `first` completes the cluster arrive issued at
+// start, after which every peer's mailboxes are initialised.
+__device__ __forceinline__ float cluster_row_sum(float v, ClusterMail &m, unsigned cl,
+                                                 unsigned crank, int64_t it, int flag, int *stop,
+                                                 int *timed_out, bool first) {
     v = warp_allsum(v);
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    if (lane == 0) s.warp[warp] = v;
+    if (lane == 0) m.warp[warp] = v;
     __syncthreads();
-    const float t = warp_allsum(lane < nwarps ? s.warp[lane] : 0.0f);
-    const int f = __syncthreads_or(flag);
+    const float t = warp_allsum(lane < nwarps ? m.warp[lane] : 0.0f);
+    const int f = __syncthreads_or(flag);   // (also: every thread has read m.warp)
+    const int p = static_cast<int>(it & 1);
     if (first) cluster_wait_acquire();
-    if (threadIdx.x < cl) {
-        st_cluster_f32(&s.cta[parity][crank], threadIdx.x, t);
-        st_cluster_u32(&s.fail[parity][crank], threadIdx.x, f);
-    }
-    cluster_arrive_release();
-    cluster_wait_acquire();
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&m.bar[p], (cl - 1) * 8u);
+    if (threadIdx.x < cl && threadIdx.x != crank)
+        send_pair(&m.box[p][crank], &m.bar[p], threadIdx.x, __float_as_uint(t),
+                  static_cast<uint32_t>(f));
+    const bool ok = mbar_wait_bounded_cluster(&m.bar[p], static_cast<uint32_t>((it >> 1) & 1));
+    if (!ok) *timed_out = 1;
     const bool mine = lane < static_cast<int>(cl);
-    *any_fail = __any_sync(0xFFFFFFFFu, mine && s.fail[parity][lane] != 0);
-    return warp_allsum(mine ? s.cta[parity][lane] : 0.0f);
+    uint2 got = make_uint2(0u, 0u);
+    if (mine) got = lane == static_cast<int>(crank)
+                        ? make_uint2(__float_as_uint(t), static_cast<uint32_t>(f))
+                        : m.box[p][lane];
+    *stop = __syncthreads_or(!ok || (mine && got.y != 0u));
+    return warp_allsum(mine ? __uint_as_float(got.x) : 0.0f);
 }
 
 template <int OP, class T, int K>
@@ -1323,15 +1365,14 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
     constexpr int NS = op_row_inputs(OP);   // row operands staged per row
     constexpr int NG = op_gammas(OP);       // gamma slices kept in shared memory
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ ClusterSlots slots1;
-    __shared__ ClusterSlots slots2;
+    __shared__ __align__(8) ClusterMail mail1;
+    __shared__ __align__(8) ClusterMail mail2;
     __shared__ __align__(8) uint64_t bars[kTmaMaxStages + 1];   // [stages] = the gammas
     __shared__ int issued[kTmaMaxStages];
     __shared__ int consumed[kTmaMaxStages];
     pdl_enter();
     const unsigned cl = cluster_nctarank();
     const unsigned crank = cluster_ctarank();
-    cluster_arrive_relaxed();
     const int64_t slice = a.n / cl;                    // elements of a row per CTA
     const uint32_t sb = static_cast<uint32_t>(slice * T::kBytes);
     const int64_t svec = slice / VEC;
@@ -1351,9 +1392,14 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
     if (tid == 0) {
         for (int st = 0; st <= stages && st <= kTmaMaxStages; ++st) mbar_init(&bars[st], 1);
         for (int st = 0; st < kTmaMaxStages; ++st) issued[st] = consumed[st] = 0;
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&mail1.bar[q], 1);
+            mbar_init(&mail2.bar[q], 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
+    cluster_arrive_relaxed();   // (thread 0: after its initialisation and fence)
     if (tid == 0 && my_rows > 0 && !bad_stages) {
         mbar_arrive_expect_tx(&bars[stages], NG * sb);
         bulk_to_shared(gsm, static_cast<const char *>(a.g1) + soff, sb, &bars[stages]);
@@ -1369,13 +1415,13 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
     int failed = bad_stages ? 1 : ((my_rows > 0 && !mbar_wait_bounded(&bars[stages], 0)) ? 1 : 0);
     const float sc = load_out_scale<OP, T>(a.scale);
     bool first_sum = true;
-    int stopped = 0;
+    int stopped = 0;           // 1 / 2: stopped at the first / second exchange of row stop_it
+    int64_t stop_it = 0;
 
     for (int64_t it = 0; it < my_rows; ++it) {
         const int s = bad_stages ? 0 : static_cast<int>(it % stages);
         const uint32_t parity = bad_stages ? 0u : static_cast<uint32_t>((it / stages) & 1);
         const int64_t row = first + it * step;
-        const int slot = static_cast<int>(it & 1);
         if (!failed && !mbar_wait_bounded(&bars[s], parity)) failed = 1;
 
         Fr xv[K];
@@ -1395,12 +1441,13 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
         float ss = 0.0f;
 #pragma unroll
         for (int k = 0; k < K; ++k) ss += frag_sum_sq(xv[k]);
-        int any_failed;
-        const float tot = cluster_row_sum(ss, slots1, cl, crank, slot, failed, &any_failed,
+        int stop;
+        const float tot = cluster_row_sum(ss, mail1, cl, crank, it, failed, &stop, &failed,
                                           first_sum);
         first_sum = false;
-        if (any_failed) {
+        if (stop) {
             stopped = 1;
+            stop_it = it;
             break;
         }
         // Every thread holds its part of the stage now (the barrier above): refill it.
@@ -1438,10 +1485,14 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
             st_global(elem_ptr<T>(a.y, row_elem + v * VEC), rv[k]);
             ss2 += frag_sum_sq(rv[k]);
         }
-        int unused;
-        const float inv2 = inv_rms(cluster_row_sum(ss2, slots2, cl, crank, slot, 0, &unused,
-                                                   false),
-                                   a.n, a.eps2);
+        int stop2;
+        const float tot2 = cluster_row_sum(ss2, mail2, cl, crank, it, 0, &stop2, &failed, false);
+        if (stop2) {
+            stopped = 2;
+            stop_it = it;
+            break;
+        }
+        const float inv2 = inv_rms(tot2, a.n, a.eps2);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const int64_t v = tid + static_cast<int64_t>(k) * nt;
@@ -1454,10 +1505,13 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
     if (first_sum) cluster_wait_acquire();   // (no row: complete the start-up arrive)
 
     // Exit: after a stop, wait (bounded) for this CTA's copies still in flight
-    // before it leaves its shared memory.
-    __syncthreads();
+    // before it leaves its shared memory.  Then one cluster barrier: every
+    // peer has issued all its messages once it is past it.  After a timed-out
+    // message wait, the late message may still be landing: wait (bounded) for
+    // that mailbox phase once more before leaving.
+    const int any_timeout = __syncthreads_or(failed);
     if (tid == 0 && my_rows > 0 && stopped) {
-        if (failed) atomicAdd(&g_wait_timeouts, 1u);
+        if (any_timeout) atomicAdd(&g_wait_timeouts, 1u);
         if (!bad_stages) {
             (void)mbar_wait_bounded(&bars[stages], 0);
             for (int st = 0; st < stages; ++st) {
@@ -1465,6 +1519,13 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
                     (void)mbar_wait_bounded(&bars[st], static_cast<uint32_t>(consumed[st] & 1));
             }
         }
+    }
+    cluster_arrive_relaxed();
+    cluster_wait_acquire();
+    if (tid == 0 && stopped && any_timeout) {
+        ClusterMail &m = stopped == 1 ? mail1 : mail2;
+        (void)mbar_wait_bounded_cluster(&m.bar[stop_it & 1],
+                                        static_cast<uint32_t>((stop_it >> 1) & 1));
     }
 }
 

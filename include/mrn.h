@@ -265,7 +265,7 @@ typedef struct mrn_geometry {
     int32_t cluster;       /* CTAs per row (1 unless MRN_GEOM_CTA is split) */
     int32_t lanes_per_row; /* threads per row for MRN_GEOM_ROWS_PER_WARP */
     int32_t rows_per_cta;  /* rows one CTA handles at a time */
-    int32_t stages;        /* MRN_GEOM_TMA: rows staged in shared memory (1..4) */
+    int32_t stages;        /* MRN_GEOM_TMA: rows staged in shared memory (1..8) */
     int32_t ctas;          /* MRN_GEOM_TMA: persistent CTAs (0 = fill the device) */
     int32_t groups;        /* MRN_GEOM_TMA: warp groups per CTA (1 or 2), each
                               reducing its own rows; threads is the CTA total */

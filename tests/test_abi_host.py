@@ -277,7 +277,7 @@ def test_force_geometry_validation():
         {"kind": 2, "k": 1, "threads": 128, "cluster": 17},
         {"kind": 3, "threads": 1024},
         {"kind": 4, "k": 4, "threads": 416, "stages": 0},
-        {"kind": 4, "k": 4, "threads": 416, "stages": 5},
+        {"kind": 4, "k": 4, "threads": 416, "stages": 9},
         {"kind": 4, "k": 8, "threads": 512, "stages": 2},
         {"kind": 4, "k": 2, "threads": 96, "stages": 2, "ctas": -1},
         {"kind": 4, "k": 4, "threads": 832, "stages": 3, "groups": 3},

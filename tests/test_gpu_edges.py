@@ -296,6 +296,9 @@ FORCED_TMA = [
     ({"kind": 4, "k": 1, "threads": 64, "stages": 3, "cluster": 2, "ctas": 6}, 128, 101),
     ({"kind": 4, "k": 4, "threads": 256, "stages": 2, "cluster": 8}, 8192, 64),
     ({"kind": 4, "k": 2, "threads": 64, "stages": 1, "cluster": 16}, 2048, 40),
+    ({"kind": 4, "k": 8, "threads": 128, "stages": 3, "cluster": 8}, 8192, 200),
+    ({"kind": 4, "k": 4, "threads": 256, "stages": 6, "cluster": 4}, 4096, 77),
+    ({"kind": 4, "k": 8, "threads": 32, "stages": 8, "cluster": 16}, 4096, 300),
 ]
 
 
