@@ -301,11 +301,13 @@ __device__ __forceinline__ float cta_allsum(float v, ReduceSlots &s, unsigned cl
     return t;
 }
 
-// Programmatic dependent launch.  Every kernel starts by waiting for the
-// grid it depends on (the previous kernel on the stream) to complete and
-// publish its memory -- a no-op unless the launch allowed programmatic
-// serialisation -- and then lets its own dependent grid be scheduled, so that
-// the next launch's set-up overlaps this kernel instead of following it.
+// Programmatic dependent launch.  Every kernel waits for the grid it depends
+// on (the previous kernel on the stream) to complete and publish its memory --
+// a no-op unless the launch allowed programmatic serialisation -- before its
+// first global memory access, and then lets its own dependent grid be
+// scheduled, so that the next launch's set-up overlaps this kernel instead of
+// following it.  The staged kernels initialise their shared memory and
+// mbarriers before the wait.
 __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1066,7 +1068,6 @@ __global__ void __launch_bounds__(tma_max_threads(K, G), 1)
 mrn_tma_kernel(const KernelArgs a, const int stages) {
     constexpr int VEC = 16 / T::kBytes;
     using Fr = Frag<T, VEC>;
-    pdl_enter();
     constexpr int NS = op_row_inputs(OP);   // row operands staged per row
     constexpr int NG = op_staged_gammas(OP);   // gammas kept in shared memory
     extern __shared__ __align__(128) unsigned char smem[];
@@ -1104,6 +1105,7 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_enter();   // (the shared-memory set-up above overlapped the previous grid)
     if (tid == 0 && my_rows > 0) {
         mbar_arrive_expect_tx(&bars[stages], NG * rb);   // (NG == 0: completes at once)
         if (NG >= 1) bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
@@ -1370,7 +1372,6 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
     __shared__ __align__(8) uint64_t bars[kTmaMaxStages + 1];   // [stages] = the gammas
     __shared__ int issued[kTmaMaxStages];
     __shared__ int consumed[kTmaMaxStages];
-    pdl_enter();
     const unsigned cl = cluster_nctarank();
     const unsigned crank = cluster_ctarank();
     const int64_t slice = a.n / cl;                    // elements of a row per CTA
@@ -1400,6 +1401,7 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
     }
     __syncthreads();
     cluster_arrive_relaxed();   // (thread 0: after its initialisation and fence)
+    pdl_enter();   // (the shared-memory set-up above overlapped the previous grid)
     if (tid == 0 && my_rows > 0 && !bad_stages) {
         mbar_arrive_expect_tx(&bars[stages], NG * sb);
         bulk_to_shared(gsm, static_cast<const char *>(a.g1) + soff, sb, &bars[stages]);
@@ -1761,7 +1763,6 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
     constexpr int CH = kQ8Block / VEC;    // chunks per block: 4 or 8
     constexpr int NP = kQ8Block / 2;      // f32 pairs per block
     using Fr = Frag<T, VEC>;
-    pdl_enter();
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ ReduceSlots slots[G];
     __shared__ __align__(8) uint64_t bars[kTmaMaxStages + 1];   // [stages] = gamma
@@ -1799,6 +1800,7 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_enter();   // (the shared-memory set-up above overlapped the previous grid)
     if (tid == 0 && my_rows > 0) {
         mbar_arrive_expect_tx(&bars[stages], rb);
         bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
