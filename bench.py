@@ -447,7 +447,7 @@ def run_mrn(args):
     h2d = sum(t.numel() * 4 for t in pin.values())
     d2h = 2 * rows * n * 4
 
-    def e2e_step(i):
+    def e2e_step(i, call=True):
         st = e2e_streams[i % 2]
         b, r, gp, gq, s, o = sets[i % 2]
         host_s, host_o = host_out[i % 2]
@@ -456,11 +456,12 @@ def run_mrn(args):
             r.copy_(pin["residual"], non_blocking=True)
             gp.copy_(pin["gamma_post"], non_blocking=True)
             gq.copy_(pin["gamma_pre"], non_blocking=True)
-            stc = mrn.mrn_norm_residual_norm(b.data_ptr(), r.data_ptr(), gp.data_ptr(),
-                                             gq.data_ptr(), s.data_ptr(), o.data_ptr(), rows, n,
-                                             1e-8, 1e-5, mrn.MRN_F32, st.cuda_stream)
-            if stc != 0:
-                raise mrn.MrnError(stc, "mrn_norm_residual_norm")
+            if call:
+                stc = mrn.mrn_norm_residual_norm(b.data_ptr(), r.data_ptr(), gp.data_ptr(),
+                                                 gq.data_ptr(), s.data_ptr(), o.data_ptr(), rows,
+                                                 n, 1e-8, 1e-5, mrn.MRN_F32, st.cuda_stream)
+                if stc != 0:
+                    raise mrn.MrnError(stc, "mrn_norm_residual_norm")
             host_s.copy_(s, non_blocking=True)
             host_o.copy_(o, non_blocking=True)
 
@@ -486,6 +487,14 @@ def run_mrn(args):
     e2e_s = (time.perf_counter() - t0) / args.e2e_steps
     e2e_s = max_over_ranks(e2e_s, pg, dev)
     e2e_value = world * step_bytes / e2e_s / 1e9
+    # The same steps without the call: the host link's own ceiling for this
+    # traffic on this machine, in the same unit.
+    t0 = time.perf_counter()
+    for i in range(args.e2e_steps):
+        e2e_step(i, call=False)
+    e2e_drain()
+    link_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, pg, dev)
+    link_value = world * step_bytes / link_s / 1e9
 
     # -- decode latency: rows=1, n=6656 ---------------------------------------
     decode = decode_latency(args, dev, stream)
@@ -516,9 +525,11 @@ def run_mrn(args):
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
+                "copies_only": link_value,
                 "note": "pinned host buffers; every step copies its inputs H2D, runs the call "
                         "and copies both outputs D2H; steps alternate over two streams and "
-                        "two device buffer sets"},
+                        "two device buffer sets; copies_only = the same steps without the "
+                        "call (the host link's ceiling)"},
         "decode": decode,
         "secondary": secondary,
     }

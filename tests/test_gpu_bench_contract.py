@@ -35,6 +35,7 @@ def test_bench_line_contract():
     e2e = line["e2e"]
     assert e2e["unit"] == "GB/s" and 0 < e2e["value"] < line["value"]
     assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] == 2 * 4096 * 6656 * 4
+    assert e2e["copies_only"] > 0   # the same steps without the call
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
     assert line["clocks"]["sm_max_mhz"] > 0
