@@ -898,7 +898,7 @@ def sweep_large(dev, stream):
                                                   y.data_ptr(), rows, n, 1e-5, mrn.MRN_F32, sh)
                 if st != 0:
                     raise mrn.MrnError(st, f"sweep {rows}x{n} {op}")
-            iters = max(5, min(200, int(2e9 // nbytes)))
+            iters = max(20, min(200, int(2e10 // nbytes)))
             for _ in range(3):
                 call()
             torch.cuda.synchronize()

@@ -195,6 +195,26 @@ def test_wide_rows_use_the_looped_fallback(dtype, n):
     all_ops(rows_data(n, 3, n, dtype), dtype, f"wide n={n}")
 
 
+@pytest.mark.parametrize("dtype,n,cluster", [("f32", 16384, 2), ("f32", 32768, 4),
+                                             ("f32", 65536, 8), ("f32", 131072, 16),
+                                             ("bf16", 65536, 4), ("bf16", 262144, 16)])
+def test_wide_row_batches_use_the_cluster_staged_kernel(dtype, n, cluster):
+    """Batches (rows >= the SM count) of rows of 2049 .. 16 x 2048 loads take the
+    cluster-staged kernel, a cluster of 2 .. 16 CTAs per row, for the plain,
+    then-add, then-add-scale and sandwich operations (the sandwich's cluster is
+    doubled from 8); every output matches the oracle."""
+    rows = 160
+    for op in (0, 1, 2, 4):
+        g = mrn.mrn_query_geometry(op, rows, n, gu.code(dtype), True)
+        want = cluster * 2 if op == 2 and cluster == 8 else cluster
+        assert (g["kind"], g["cluster"], g["groups"]) == (mrn.MRN_GEOM_TMA, want, 1), (op, g)
+    d = rows_data(n + 11, rows, n, dtype)
+    all_ops(d, dtype, f"cluster-staged {rows}x{n}")
+    gu.parity_then_add_scale(d["x"], d["gamma"], d["residual"], 0.75, 1e-5, dtype,
+                             what=f"cluster-staged {rows}x{n} then_add_scale")
+    assert mrn.mrn_wait_timeouts() == 0
+
+
 def test_epsilon_routing_is_visible():
     """Block output of mean square 1e-8 and a stream of mean square ~1e-6:
     eps_post = 1e-8 and eps_pre = 1e-5 both move the outputs, and an oracle with
