@@ -741,24 +741,6 @@ mrn_rows_per_warp_kernel(const KernelArgs a, const int lanes) {
     row_body<OP, T, VEC, K>(a, row, row < a.rows_end, lane_in_row, lanes, reduce, reduce);
 }
 
-// One row per CTA, or per cluster of cl CTAs (launched with a cluster
-// dimension); CTA `rank` covers loads [rank*threads*K, (rank+1)*threads*K).
-template <int OP, class T, int VEC, int K>
-__global__ void __launch_bounds__(cta_max_threads(K))
-mrn_cta_kernel(const KernelArgs a) {
-    __shared__ ReduceSlots slots1;
-    __shared__ ReduceSlots slots2;
-    pdl_enter();
-    const unsigned cl = cluster_nctarank();
-    const unsigned crank = cluster_ctarank();
-    if (cl > 1) cluster_arrive_relaxed();
-    const int64_t row = a.row0 + cluster_index_x();
-    const int64_t first = static_cast<int64_t>(crank) * blockDim.x * K + threadIdx.x;
-    auto reduce1 = [&](float v) { return cta_allsum(v, slots1, cl, crank, true); };
-    auto reduce2 = [&](float v) { return cta_allsum(v, slots2, cl, crank, false); };
-    row_body<OP, T, VEC, K>(a, row, true, first, blockDim.x, reduce1, reduce2);
-}
-
 // Looped fallback for rows wider than the register-resident geometries
 // hold: one row per CTA, the row is read once for the sum and once more for
 // the output (the second read is usually served by L2).  The sandwich's pre
@@ -1357,6 +1339,98 @@ __device__ __forceinline__ float cluster_row_sum(float v, ClusterMail &m, unsign
                         : m.box[p][lane];
     *stop = __syncthreads_or(!ok || (mine && got.y != 0u));
     return warp_allsum(mine ? __uint_as_float(got.x) : 0.0f);
+}
+
+// ---------------------------------------------------------------------------
+// Register kernel: one row per CTA, or per cluster of cl CTAs (launched with
+// a cluster dimension); CTA `rank` covers loads [rank*threads*K,
+// (rank+1)*threads*K).  In a cluster each reduction is one exchange of
+// messages: every CTA sends its partial to every peer with st.async into the
+// peer's mailbox for that reduction, completing the peer's mailbox mbarrier
+// (armed for (cl - 1) * 4 bytes), and adds the cl partials in rank order, its
+// own from registers (all CTAs get the same bits).  A cluster barrier at
+// start, after the mailboxes are initialised, is the only cluster-wide
+// barrier: nothing ties a reduction to the stores before it (the sandwich's
+// second reduction does not wait for the stream's stores), and every message
+// a CTA receives is one it waits for before it leaves.
+// ---------------------------------------------------------------------------
+struct RowMail {
+    float warp[32];
+    float box[kMaxCluster];   // [sender rank]
+    uint64_t bar;             // every peer's partial landed
+};
+
+// Store v into `box` of CTA `rank` of this cluster, completing 4 bytes of the
+// transaction count of that CTA's `bar`.
+__device__ __forceinline__ void send_f32(float *box, uint64_t *bar, unsigned rank, float v) {
+    uint32_t rbox, rbar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbox) : "r"(smem_addr(box)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(smem_addr(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 :: "r"(rbox), "r"(__float_as_uint(v)), "r"(rbar) : "memory");
+}
+
+// Sum of v over the CTA and its cluster (cl > 1); every thread of every CTA
+// calls it once per mailbox.  `first` completes the cluster arrive issued at
+// start.  A message wait that runs out (bounded, about one second) sets
+// *timed_out: the row's outputs are then unspecified and the kernel counts it.
+__device__ __forceinline__ float cluster_mail_sum(float v, RowMail &m, unsigned cl,
+                                                  unsigned crank, bool first, int *timed_out) {
+    v = warp_allsum(v);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    if (lane == 0) m.warp[warp] = v;
+    __syncthreads();
+    const float t = warp_allsum(lane < nwarps ? m.warp[lane] : 0.0f);
+    if (first) cluster_wait_acquire();
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&m.bar, (cl - 1) * 4u);
+    if (threadIdx.x < cl && threadIdx.x != crank) send_f32(&m.box[crank], &m.bar, threadIdx.x, t);
+    if (!mbar_wait_bounded_cluster(&m.bar, 0)) *timed_out = 1;
+    const bool mine = lane < static_cast<int>(cl);
+    return warp_allsum(mine ? (lane == static_cast<int>(crank) ? t : m.box[lane]) : 0.0f);
+}
+
+template <int OP, class T, int VEC, int K>
+__global__ void __launch_bounds__(cta_max_threads(K))
+mrn_cta_kernel(const KernelArgs a) {
+    __shared__ ReduceSlots slots1;
+    __shared__ ReduceSlots slots2;
+    __shared__ __align__(8) RowMail mail1;
+    __shared__ __align__(8) RowMail mail2;
+    const unsigned cl = cluster_nctarank();
+    const unsigned crank = cluster_ctarank();
+    if (cl > 1) {
+        if (threadIdx.x == 0) {
+            mbar_init(&mail1.bar, 1);
+            mbar_init(&mail2.bar, 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        cluster_arrive_relaxed();   // (thread 0: after its initialisation and fence)
+    }
+    pdl_enter();
+    const int64_t row = a.row0 + cluster_index_x();
+    const int64_t first = static_cast<int64_t>(crank) * blockDim.x * K + threadIdx.x;
+    int timed_out = 0;
+    auto reduce1 = [&](float v) {
+        return cl > 1 ? cluster_mail_sum(v, mail1, cl, crank, true, &timed_out)
+                      : cta_allsum(v, slots1, 1, 0, false);
+    };
+    auto reduce2 = [&](float v) {
+        return cl > 1 ? cluster_mail_sum(v, mail2, cl, crank, false, &timed_out)
+                      : cta_allsum(v, slots2, 1, 0, false);
+    };
+    row_body<OP, T, VEC, K>(a, row, true, first, blockDim.x, reduce1, reduce2);
+    if (timed_out) {
+        // A late message may still be landing in this CTA: wait once more
+        // (bounded) before leaving; count the timeout once per warp.
+        (void)mbar_wait_bounded_cluster(&mail1.bar, 0);
+        if (OP == kSandwich) (void)mbar_wait_bounded_cluster(&mail2.bar, 0);
+        const unsigned lanes = __activemask();
+        if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(lanes) - 1))
+            atomicAdd(&g_wait_timeouts, 1u);
+    }
 }
 
 template <int OP, class T, int K>
