@@ -1144,9 +1144,16 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
 #pragma unroll
             for (int k = 0; k < K; ++k) ss += frag_sum_sq(xv[k]);
         }
+        // One barrier per reduction: a warp may start the next row's reduction
+        // while another still reads this one's warp sums.  Single-reduction
+        // operations therefore alternate the two slot sets by row (a set is
+        // rewritten only after the next row's barrier, which every reader
+        // passes after its read); the sandwich's second reduction separates
+        // the uses of each set.
+        ReduceSlots &rs1 = (OP != kSandwich && ((it / G) & 1)) ? slots2[grp] : slots1[grp];
         int any_failed;
-        const float tot = wg_allsum<true>(ss, slots1[grp], bar_id, gsize, gtid,
-                                             failed | abort_flag, &any_failed);
+        const float tot = wg_allsum<true>(ss, rs1, bar_id, gsize, gtid, failed | abort_flag,
+                                             &any_failed);
         if (any_failed) {
             if (gtid == 0) abort_flag = 1;
             break;
