@@ -441,6 +441,7 @@ mrn_status launch(const Call &c, bool aligned16, cudaStream_t stream) {
     }
     g.pdl = (t_launch_options & MRN_LAUNCH_PDL) ? 1 : 0;
     KernelArgs a = c.args;
+    a.stall_bytes = (t_launch_options & MRN_LAUNCH_TEST_WAIT_TIMEOUT) ? 16u : 0u;
     a.n = c.n;
     a.nvec = ceil_div(c.n, g.vec);
     const bool bf16 = c.dt == MRN_BF16;
@@ -798,7 +799,8 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry) {
 uint64_t mrn_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
 mrn_status mrn_set_launch_options(uint32_t options) {
-    if (options & ~static_cast<uint32_t>(MRN_LAUNCH_PDL)) return MRN_ERR_INVALID_GEOMETRY;
+    if (options & ~static_cast<uint32_t>(MRN_LAUNCH_PDL | MRN_LAUNCH_TEST_WAIT_TIMEOUT))
+        return MRN_ERR_INVALID_GEOMETRY;
     t_launch_options = options;
     return MRN_OK;
 }

@@ -70,6 +70,8 @@ struct KernelArgs {
     int64_t rows_end;  // one past the last row of this launch
     float eps1;        // eps (rmsnorm, then-add) or eps_post (sandwich)
     float eps2;        // eps_pre (sandwich)
+    uint32_t stall_bytes;   // test hook: bytes a CTA's first wait expects beyond its
+                            // copies or messages (0 in use; see MRN_LAUNCH_TEST_WAIT_TIMEOUT)
 };
 
 struct Geometry {

@@ -1089,7 +1089,8 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
     __syncthreads();
     pdl_enter();   // (the shared-memory set-up above overlapped the previous grid)
     if (tid == 0 && my_rows > 0) {
-        mbar_arrive_expect_tx(&bars[stages], NG * rb);   // (NG == 0: completes at once)
+        // (NG == 0: completes at once; stall_bytes is a test hook, 0 in use)
+        mbar_arrive_expect_tx(&bars[stages], NG * rb + a.stall_bytes);
         if (NG >= 1) bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
         if (NG == 2) bulk_to_shared(gsm + rb, a.g2, rb, &bars[stages]);
         for (int s = 0; s < stages && s < my_rows; ++s) {
@@ -1382,7 +1383,8 @@ __device__ __forceinline__ void send_f32(float *box, uint64_t *bar, unsigned ran
 // start.  A message wait that runs out (bounded, about one second) sets
 // *timed_out: the row's outputs are then unspecified and the kernel counts it.
 __device__ __forceinline__ float cluster_mail_sum(float v, RowMail &m, unsigned cl,
-                                                  unsigned crank, bool first, int *timed_out) {
+                                                  unsigned crank, bool first, uint32_t stall,
+                                                  int *timed_out) {
     v = warp_allsum(v);
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -1391,7 +1393,7 @@ __device__ __forceinline__ float cluster_mail_sum(float v, RowMail &m, unsigned 
     __syncthreads();
     const float t = warp_allsum(lane < nwarps ? m.warp[lane] : 0.0f);
     if (first) cluster_wait_acquire();
-    if (threadIdx.x == 0) mbar_arrive_expect_tx(&m.bar, (cl - 1) * 4u);
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&m.bar, (cl - 1) * 4u + stall);   // (test hook: 0)
     if (threadIdx.x < cl && threadIdx.x != crank) send_f32(&m.box[crank], &m.bar, threadIdx.x, t);
     if (!mbar_wait_bounded_cluster(&m.bar, 0)) *timed_out = 1;
     const bool mine = lane < static_cast<int>(cl);
@@ -1421,11 +1423,11 @@ mrn_cta_kernel(const KernelArgs a) {
     const int64_t first = static_cast<int64_t>(crank) * blockDim.x * K + threadIdx.x;
     int timed_out = 0;
     auto reduce1 = [&](float v) {
-        return cl > 1 ? cluster_mail_sum(v, mail1, cl, crank, true, &timed_out)
+        return cl > 1 ? cluster_mail_sum(v, mail1, cl, crank, true, a.stall_bytes, &timed_out)
                       : cta_allsum(v, slots1, 1, 0, false);
     };
     auto reduce2 = [&](float v) {
-        return cl > 1 ? cluster_mail_sum(v, mail2, cl, crank, false, &timed_out)
+        return cl > 1 ? cluster_mail_sum(v, mail2, cl, crank, false, 0u, &timed_out)
                       : cta_allsum(v, slots2, 1, 0, false);
     };
     row_body<OP, T, VEC, K>(a, row, true, first, blockDim.x, reduce1, reduce2);
@@ -1484,7 +1486,7 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
     cluster_arrive_relaxed();   // (thread 0: after its initialisation and fence)
     pdl_enter();   // (the shared-memory set-up above overlapped the previous grid)
     if (tid == 0 && my_rows > 0 && !bad_stages) {
-        mbar_arrive_expect_tx(&bars[stages], NG * sb);
+        mbar_arrive_expect_tx(&bars[stages], NG * sb + a.stall_bytes);   // (test hook: 0)
         bulk_to_shared(gsm, static_cast<const char *>(a.g1) + soff, sb, &bars[stages]);
         if (NG == 2) bulk_to_shared(gsm + sb, static_cast<const char *>(a.g2) + soff, sb,
                                     &bars[stages]);
@@ -1883,7 +1885,7 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
     __syncthreads();
     pdl_enter();   // (the shared-memory set-up above overlapped the previous grid)
     if (tid == 0 && my_rows > 0) {
-        mbar_arrive_expect_tx(&bars[stages], rb);
+        mbar_arrive_expect_tx(&bars[stages], rb + a.stall_bytes);   // (test hook: 0)
         bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
         for (int s = 0; s < stages && s < my_rows; ++s) {
             stage_row<1>(stage0 + s * rb, xg, nullptr, (first + s * step) * row_bytes, rb,

@@ -41,6 +41,7 @@ MRN_GEOM_TMA = 4
 MRN_GEOM_Q8_BLOCKS = 5
 
 MRN_LAUNCH_PDL = 1
+MRN_LAUNCH_TEST_WAIT_TIMEOUT = 0x80000000   # test hook (see include/mrn.h)
 
 STATUS = {
     0: "MRN_OK",
@@ -216,7 +217,8 @@ def mrn_launch_count() -> int:
 
 
 def mrn_set_launch_options(options: int) -> int:
-    """Launch options of the calling thread (MRN_LAUNCH_PDL or 0)."""
+    """Launch options of the calling thread (MRN_LAUNCH_PDL or 0; MRN_LAUNCH_TEST_WAIT_TIMEOUT
+    is a test hook)."""
     return lib().mrn_set_launch_options(options)
 
 

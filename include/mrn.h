@@ -306,19 +306,31 @@ uint64_t mrn_launch_count(void);
  *                   per decode call in a CUDA graph).  The previous kernel
  *                   need not be ours; a kernel launched after ours without
  *                   the attribute is ordered as usual.
+ *   MRN_LAUNCH_TEST_WAIT_TIMEOUT
+ *                   test hook, never for use: the first wait of every CTA
+ *                   of the staged kernels (MRN_GEOM_TMA, staged
+ *                   MRN_GEOM_Q8_BLOCKS: its gamma copy) and of cluster
+ *                   reductions in MRN_GEOM_CTA (its first message exchange)
+ *                   expects 16 bytes more than ever arrive, so it runs out
+ *                   after about one second.  The staged kernels then write
+ *                   nothing; the register kernel's outputs are unspecified.
+ *                   mrn_wait_timeouts() reports the waits; the context stays
+ *                   usable.  Lets a test drive the timeout path with no fault.
  * Unknown bits give MRN_ERR_INVALID_GEOMETRY.  Not on the pages: a launch
  * option of this library.
  */
 #define MRN_LAUNCH_PDL 1u
+#define MRN_LAUNCH_TEST_WAIT_TIMEOUT 0x80000000u
 mrn_status mrn_set_launch_options(uint32_t options);
 uint32_t mrn_launch_options(void);
 
 /*
- * Number of bounded waits (on the shared-memory copy barriers of the
- * MRN_GEOM_TMA kernels) that ran out on the current device since the previous
- * call, which resets the count; -1 if the count could not be read.  Every
- * wait gives up after about one second; the CTA then drains its copies and
- * returns without writing its remaining rows, so the context stays usable.
+ * Number of bounded waits (on the shared-memory copy barriers of the staged
+ * kernels and the message barriers of cluster reductions) that ran out on the
+ * current device since the previous call, which resets the count; -1 if the
+ * count could not be read.  Every wait gives up after about one second; a
+ * staged CTA then drains its copies and returns without writing its remaining
+ * rows, so the context stays usable.
  * Synchronises the device.  Not on the pages: a diagnostic of this library.
  */
 int mrn_wait_timeouts(void);

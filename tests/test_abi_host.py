@@ -321,6 +321,9 @@ def test_launch_options():
     assert mrn.mrn_set_launch_options(2) == mrn.MRN_ERR_INVALID_GEOMETRY
     assert mrn.mrn_set_launch_options(0) == 0 and mrn.mrn_launch_options() == 0
     assert mrn.mrn_set_launch_options(mrn.MRN_LAUNCH_PDL) == 0
+    both = mrn.MRN_LAUNCH_PDL | mrn.MRN_LAUNCH_TEST_WAIT_TIMEOUT   # the test hook is a known bit
+    assert mrn.mrn_set_launch_options(both) == 0 and mrn.mrn_launch_options() == both
+    assert mrn.mrn_set_launch_options(mrn.MRN_LAUNCH_PDL) == 0
     assert mrn.mrn_launch_options() == mrn.MRN_LAUNCH_PDL
 
 
