@@ -47,6 +47,29 @@ def test_exports_every_declared_symbol(library):
         assert re.search(rf"\bT {name}$", nm, flags=re.M), name
 
 
+def header_constants():
+    """Every enum value and #define of the header: name -> integer."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    found = {}
+    for name, value in re.findall(r"\b(MRN_[A-Z0-9_]+)\s*=\s*(0x[0-9A-Fa-f]+|\d+)", text):
+        found[name] = int(value, 0)
+    for name, value in re.findall(r"#define\s+(MRN_[A-Z0-9_]+)\s+(0x[0-9A-Fa-f]+|\d+)u?", text):
+        found[name] = int(value, 0)
+    return found
+
+
+def test_binding_constants_match_the_header():
+    """The binding restates the header's constants; they must agree, and every
+    enum value and option bit of the header must be there."""
+    consts = header_constants()
+    statuses = {v: k for k, v in consts.items() if k == "MRN_OK" or k.startswith("MRN_ERR_")}
+    assert mrn.STATUS == statuses
+    for name, value in consts.items():
+        if name == "MRN_OK" or name.startswith("MRN_ERR_"):
+            continue
+        assert getattr(mrn, name) == value, name
+
+
 def test_status_strings():
     for code in range(10):
         assert mrn.mrn_status_string(code)
