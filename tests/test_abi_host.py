@@ -290,6 +290,42 @@ def test_geometry_covers_every_row_width():
                             assert nvec > 16 * 2048
 
 
+# (op, rows, n, dtype) -> (cluster, stages, threads, k) of the cluster-staged kernel,
+# as measured best on GB300: slices of at most 2048 loads; plain 3 stages at C = 2,
+# else 2; then-add (and -scale) 3 stages from C = 8; the sandwich doubles C from 8.
+CLUSTER_STAGED = [
+    ((0, 4096, 16384, 0), (2, 3, 256, 8)),
+    ((1, 4096, 16384, 0), (2, 2, 256, 8)),
+    ((2, 16384, 16384, 0), (2, 2, 256, 8)),
+    ((0, 8192, 32768, 0), (4, 2, 256, 8)),
+    ((1, 8192, 32768, 0), (4, 2, 256, 8)),
+    ((0, 4096, 65536, 0), (8, 2, 256, 8)),
+    ((1, 4096, 65536, 0), (8, 3, 256, 8)),
+    ((4, 4096, 65536, 0), (8, 3, 256, 8)),
+    ((2, 4096, 65536, 0), (16, 2, 256, 4)),
+    ((0, 8192, 32768, 1), (2, 3, 256, 8)),
+    ((2, 8192, 32768, 1), (2, 2, 256, 8)),
+    ((0, 4096, 131072, 0), (16, 2, 256, 8)),
+]
+
+
+@pytest.mark.parametrize("call,want", CLUSTER_STAGED, ids=[str(c) for c, _ in CLUSTER_STAGED])
+def test_cluster_staged_geometry_choice(call, want):
+    op, rows, n, dt = call
+    g = mrn.mrn_query_geometry(op, rows, n, dt, True, 152)
+    assert g["kind"] == mrn.MRN_GEOM_TMA and g["groups"] == 1
+    assert (g["cluster"], g["stages"], g["threads"], g["k"]) == want
+
+
+def test_cluster_staged_kernel_is_not_chosen_outside_its_range():
+    # fewer rows than SMs, slices that are not 16-byte multiples, too wide, or an
+    # operation it does not serve: other kernels
+    for op, rows, n, dt in ((0, 100, 65536, 0), (1, 4096, 16388, 0), (0, 4096, 262144, 0),
+                            (3, 4096, 16384, 0), (6, 4096, 16384, 0)):
+        g = mrn.mrn_query_geometry(op, rows, n, dt, True, 152)
+        assert not (g["kind"] == mrn.MRN_GEOM_TMA and g["cluster"] > 1), (op, rows, n, g)
+
+
 def test_force_geometry_validation():
     bad = [
         {"kind": 1, "lanes_per_row": 3, "k": 1},
