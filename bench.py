@@ -59,11 +59,14 @@ def parse_args(argv=None):
                    help="skip the bf16 16384x4096 and f32 4x6656 secondary measurements")
     p.add_argument("--profile-launches", type=int, default=0,
                    help="only run --warmup + this many launches of the timed call (for ncu)")
-    p.add_argument("--profile-op", choices=("sandwich", "seam_f16", "q8_1", "wide_f32"),
+    p.add_argument("--profile-op", choices=("sandwich", "seam_f16", "q8_1", "wide_f32",
+                                            "decode", "qk_norm", "add_rmsnorm", "widest_f32"),
                    default="sandwich",
                    help="with --profile-launches: the call to launch -- the timed sandwich, the "
                         "fused f16 seam at the same shape, RMSNorm + Q8_1 at 16384 x 4096 bf16, "
-                        "or plain f32 RMSNorm at 1024 x 65536")
+                        "plain f32 RMSNorm at 1024 x 65536, the decode sandwich (1 x 6656 f32), "
+                        "QK-norm (163840 x 128 bf16), residual add + norm (4096 x 6656 f32), or "
+                        "plain f32 RMSNorm at 256 x 262144 (the looped kernel)")
     return p.parse_args(argv)
 
 
@@ -836,6 +839,49 @@ def profile_other(args, dev):
             return mrn.mrn_rmsnorm_seam(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), rows,
                                         n, 1e-5, mrn.MRN_F32, mrn.MRN_F16, sh)
         geometry = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM_SEAM, rows, n, mrn.MRN_F32, True)
+    elif args.profile_op in ("decode", "add_rmsnorm"):
+        # the decode sandwich tail (1 x 6656 f32, a cluster of 8 CTAs), or the
+        # residual add + norm at the prefill shape (the register batch kernel)
+        rows, n = (1, 6656) if args.profile_op == "decode" else (4096, 6656)
+        sets = [tuple(torch.randn(rows, n, device=dev, generator=gen) for _ in range(2)) +
+                tuple(1 + 0.1 * torch.randn(n, device=dev, generator=gen) for _ in range(2)) +
+                tuple(torch.empty(rows, n, device=dev) for _ in range(2)) for _ in range(2)]
+        if args.profile_op == "decode":
+            def call(t):
+                return mrn.mrn_norm_residual_norm(t[0].data_ptr(), t[1].data_ptr(),
+                                                  t[2].data_ptr(), t[3].data_ptr(),
+                                                  t[4].data_ptr(), t[5].data_ptr(), rows, n,
+                                                  1e-8, 1e-5, mrn.MRN_F32, sh)
+            geometry = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, rows, n, mrn.MRN_F32, True)
+        else:
+            def call(t):
+                return mrn.mrn_add_rmsnorm(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(),
+                                           t[4].data_ptr(), t[5].data_ptr(), rows, n, 1e-5,
+                                           mrn.MRN_F32, sh)
+            geometry = mrn.mrn_query_geometry(mrn.MRN_OP_ADD_RMSNORM, rows, n, mrn.MRN_F32,
+                                              True)
+    elif args.profile_op == "qk_norm":
+        # per-head QK-norm: 163840 rows of 128 bf16 (the rows-per-warp kernel)
+        rows, n = 163840, 128
+        sets = [(torch.randn(rows, n, device=dev, generator=gen).bfloat16(),
+                 (1 + 0.1 * torch.randn(n, device=dev, generator=gen)).bfloat16(),
+                 torch.empty(rows, n, dtype=torch.bfloat16, device=dev)) for _ in range(2)]
+
+        def call(t):
+            return mrn.mrn_rmsnorm(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), rows, n,
+                                   1e-6, mrn.MRN_BF16, sh)
+        geometry = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM, rows, n, mrn.MRN_BF16, True)
+    elif args.profile_op == "widest_f32":
+        # rows past the cluster kernels' reach (1 MB each): the looped kernel
+        rows, n = 256, 262144
+        sets = [(torch.randn(rows, n, device=dev, generator=gen),
+                 1 + 0.1 * torch.randn(n, device=dev, generator=gen),
+                 torch.empty(rows, n, device=dev)) for _ in range(2)]
+
+        def call(t):
+            return mrn.mrn_rmsnorm(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), rows, n,
+                                   1e-5, mrn.MRN_F32, sh)
+        geometry = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM, rows, n, mrn.MRN_F32, True)
     elif args.profile_op == "wide_f32":
         # plain f32 RMSNorm of 256 KB rows (the cluster-staged kernel, 8 CTAs a row)
         rows, n = 1024, 65536
