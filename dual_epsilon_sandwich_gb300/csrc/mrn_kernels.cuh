@@ -743,7 +743,8 @@ mrn_rows_per_warp_kernel(const KernelArgs a, const int lanes) {
 
 // Looped fallback for rows wider than the register-resident geometries
 // hold: one row per CTA, the row is read once for the sum and once more for
-// the output (the second read is usually served by L2).  The sandwich's pre
+// the output (the second read comes from L2 while the rows in flight fit in
+// it; 256 rows of 1 MB do not, and read DRAM twice).  The sandwich's pre
 // norm re-reads the stream values this same thread stored.  Each iteration
 // handles kStreamUnroll loads per operand so that several are in flight.
 constexpr int kStreamUnroll = 4;
