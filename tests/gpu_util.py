@@ -397,7 +397,17 @@ def parity_q8_1(x, gamma, eps, dtype, rows_sample=None, what="q8_1", x_offset=0)
     torch.cuda.synchronize()
     host = raw.cpu().numpy()
     assert np.all(host[:guard] == 0xA5) and np.all(host[-guard:] == 0xA5), what + ": guard bands"
-    d_bits, s_bits, q = decode_q8_1(host[guard:-guard].reshape(rows, nb, 36))
+    return check_q8_1_blocks(host[guard:-guard], x, gamma, eps, dtype, rows_sample, what)
+
+
+def check_q8_1_blocks(host_blocks, x, gamma, eps, dtype, rows_sample=None, what="q8_1"):
+    """The checks of parity_q8_1 on the blocks as bytes on the host (rows x n/32
+    blocks of 36 bytes): s == 0, d within one f16 ulp of the oracle's, zero
+    blocks zero, codes equal except one off within Q8_TIE_MARGIN of a tie.
+    Returns (codes one off, elements near a tie)."""
+    rows, n = x.shape
+    nb = n // 32
+    d_bits, s_bits, q = decode_q8_1(np.asarray(host_blocks).reshape(rows, nb, 36))
     sel = slice(None) if rows_sample is None else rows_sample
     d64, qreal, q64 = oracle.rmsnorm_q8_1(widen(x[sel], dtype), widen(gamma, dtype),
                                           float(np.float32(eps)))
