@@ -245,13 +245,18 @@ typedef enum mrn_geometry_kind {
     MRN_GEOM_ROWS_PER_WARP = 1, /* lanes_per_row (1..32) lanes per row, several rows
                                    per CTA, shuffle-only reduction */
     MRN_GEOM_CTA = 2,           /* one row per CTA, or per thread-block cluster of
-                                   `cluster` CTAs with a DSMEM reduction; row held
-                                   in registers */
+                                   `cluster` CTAs whose partial sums travel as
+                                   st.async messages to the peers' shared memory;
+                                   row held in registers */
     MRN_GEOM_STREAM = 3,        /* one row per CTA, looped over the row: any n */
     MRN_GEOM_TMA = 4,           /* persistent CTAs; `stages` future rows are copied
                                    into shared memory by cp.async.bulk while the
                                    current one is reduced; gammas kept in shared
-                                   memory; needs 16-byte aligned rows */
+                                   memory; needs 16-byte aligned rows.  cluster > 1
+                                   (groups 1; plain, then-add, then-add-scale and
+                                   the sandwich): a cluster per row, each CTA
+                                   staging a 16-byte-multiple slice, the partial
+                                   sums exchanged as st.async messages */
     MRN_GEOM_Q8_BLOCKS = 5      /* RMSNorm + Q8_1 only: one row per CTA, `k` (1 or 2)
                                    whole 32-element blocks per thread, `threads` <= 512;
                                    needs 16-byte aligned rows */
@@ -262,7 +267,7 @@ typedef struct mrn_geometry {
     int32_t vec;           /* elements per load: 16 / element size, or 1 */
     int32_t k;             /* loads per operand per thread (register slots) */
     int32_t threads;       /* threads per CTA */
-    int32_t cluster;       /* CTAs per row (1 unless MRN_GEOM_CTA is split) */
+    int32_t cluster;       /* CTAs per row, 1..16 (MRN_GEOM_CTA or MRN_GEOM_TMA) */
     int32_t lanes_per_row; /* threads per row for MRN_GEOM_ROWS_PER_WARP */
     int32_t rows_per_cta;  /* rows one CTA handles at a time */
     int32_t stages;        /* MRN_GEOM_TMA: rows staged in shared memory (1..8) */
