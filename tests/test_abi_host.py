@@ -3,7 +3,6 @@
 Every call here fails validation before anything is enqueued, so the pointers
 are fake addresses that are never dereferenced.
 """
-import ctypes
 import os
 import re
 import subprocess

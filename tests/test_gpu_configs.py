@@ -2,7 +2,6 @@
 in the automatic geometry the benchmark times."""
 import numpy as np
 import pytest
-import torch
 
 import gpu_util as gu
 from dual_epsilon_sandwich_gb300 import mrn
