@@ -729,7 +729,6 @@ const char *mrn_status_string(mrn_status status) {
     case MRN_ERR_MISALIGNED: return "pointer not aligned to its element size";
     case MRN_ERR_CUDA: return "CUDA launch failed (see mrn_last_cuda_error)";
     case MRN_ERR_INVALID_GEOMETRY: return "forced geometry cannot cover this call";
-    case MRN_ERR_WAIT_TIMEOUT: return "a bounded wait in a kernel ran out (mrn_wait_timeouts)";
     }
     return "unknown status";
 }

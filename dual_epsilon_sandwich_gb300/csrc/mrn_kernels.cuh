@@ -39,6 +39,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -2265,12 +2266,22 @@ cudaError_t launch_tma_cluster(const Geometry &g, KernelArgs a, int64_t rows, cu
     return cudaSuccess;
 }
 
+// Timeouts counted by this translation unit's kernels on the current device
+// since the previous call.  The device counter is never reset (a reset
+// racing with a kernel's atomicAdd could lose a count); the last value
+// reported per device is kept on the host under a lock and the difference
+// (modulo 2^32) is returned.
 template <int OP> int take_wait_timeouts() {
-    unsigned int count = 0, zero = 0;
+    static std::mutex lock;
+    static unsigned int reported[kMaxCachedDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxCachedDevices) return -1;
+    std::lock_guard<std::mutex> guard(lock);
+    unsigned int count = 0;
     if (cudaMemcpyFromSymbol(&count, g_wait_timeouts, sizeof(count)) != cudaSuccess) return -1;
-    if (count != 0 && cudaMemcpyToSymbol(g_wait_timeouts, &zero, sizeof(zero)) != cudaSuccess)
-        return -1;
-    return static_cast<int>(count);
+    const unsigned int fresh = count - reported[dev];
+    reported[dev] = count;
+    return static_cast<int>(fresh & 0x7FFFFFFFu);
 }
 
 

@@ -53,7 +53,6 @@ STATUS = {
     6: "MRN_ERR_MISALIGNED",
     7: "MRN_ERR_CUDA",
     8: "MRN_ERR_INVALID_GEOMETRY",
-    9: "MRN_ERR_WAIT_TIMEOUT",
 }
 for _code, _name in STATUS.items():
     globals()[_name] = _code

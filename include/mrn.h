@@ -54,7 +54,13 @@
  * Errors     Argument errors are detected before anything is enqueued; nothing
  *            is written.  MRN_ERR_CUDA means the launch itself failed (see
  *            mrn_last_cuda_error).  Faults during execution surface at the
- *            caller's next synchronisation, as for any CUDA kernel.
+ *            caller's next synchronisation, as for any CUDA kernel.  Every
+ *            wait inside a kernel is bounded (about one second); one that runs
+ *            out is counted on the device and reported only by
+ *            mrn_wait_timeouts(), never as the status of the call that
+ *            enqueued the kernel (that call returned MRN_OK at enqueue time).
+ *            The affected rows' outputs are then not written (staged kernels)
+ *            or unspecified (cluster reductions of the register kernel).
  * Threads    All entry points are thread-safe.
  */
 #ifndef MRN_H
@@ -84,10 +90,9 @@ typedef enum mrn_status {
     MRN_ERR_ALIASING = 5,          /* a forbidden overlap between buffers */
     MRN_ERR_MISALIGNED = 6,        /* a pointer not aligned to its element size */
     MRN_ERR_CUDA = 7,              /* the CUDA runtime refused the launch */
-    MRN_ERR_INVALID_GEOMETRY = 8,  /* a forced geometry cannot cover the row */
-    MRN_ERR_WAIT_TIMEOUT = 9       /* a kernel's bounded wait ran out (see
-                                      mrn_wait_timeouts); outputs of the affected
-                                      rows were not written */
+    MRN_ERR_INVALID_GEOMETRY = 8   /* a forced geometry cannot cover the row */
+    /* A kernel whose bounded wait ran out is never reported as a call status
+       (the call has returned long before): only mrn_wait_timeouts() reports it. */
 } mrn_status;
 
 /*
@@ -332,11 +337,17 @@ uint32_t mrn_launch_options(void);
 /*
  * Number of bounded waits (on the shared-memory copy barriers of the staged
  * kernels and the message barriers of cluster reductions) that ran out on the
- * current device since the previous call, which resets the count; -1 if the
- * count could not be read.  Every wait gives up after about one second; a
- * staged CTA then drains its copies and returns without writing its remaining
- * rows, so the context stays usable.
- * Synchronises the device.  Not on the pages: a diagnostic of this library.
+ * current device since the previous mrn_wait_timeouts() call on that device;
+ * -1 if the count could not be read.  This is the only place a timeout is
+ * reported: no entry point returns a status for it.  The device-side counts
+ * only grow; the library keeps the last value it reported per device (under
+ * a lock), so a timeout counted while this function runs is reported by the
+ * next call, never lost.  Every wait gives up after about one second of wall
+ * time (%globaltimer, which also runs while the context is time-sliced out on
+ * a shared GPU); a staged CTA then drains its copies and returns without
+ * writing its remaining rows, so the context stays usable.
+ * Synchronises the device (it reads device memory with cudaMemcpyFromSymbol).
+ * Not on the pages: a diagnostic of this library.
  */
 int mrn_wait_timeouts(void);
 

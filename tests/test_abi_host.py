@@ -70,10 +70,26 @@ def test_binding_constants_match_the_header():
 
 
 def test_status_strings():
-    for code in range(10):
+    for code in range(9):
         assert mrn.mrn_status_string(code)
+        assert "unknown" not in mrn.mrn_status_string(code)
     assert "unknown" in mrn.mrn_status_string(99)
     assert mrn.mrn_last_cuda_error() == 0
+
+
+def test_a_wait_timeout_is_not_a_call_status():
+    """The contract: a kernel's bounded wait that runs out is reported only by
+    mrn_wait_timeouts(), never as the status of a call (the call returned at
+    enqueue time).  No status value stands for it, and the header says so
+    (the GPU side of the contract: tests/test_gpu_wait_timeouts.py checks that
+    every call whose kernel timed out returned MRN_OK)."""
+    consts = header_constants()
+    assert not any("TIMEOUT" in k for k in consts if k.startswith("MRN_ERR_")), consts
+    assert max(mrn.STATUS) == mrn.MRN_ERR_INVALID_GEOMETRY
+    assert "unknown" in mrn.mrn_status_string(mrn.MRN_ERR_INVALID_GEOMETRY + 1)
+    text = open(HEADER).read()
+    assert "reported only by\n *            mrn_wait_timeouts()" in text
+    assert "never as the status of the call" in text
 
 
 def rms(x=A, g=G, y=Y, rows=4, n=64, eps=1e-5, dt=mrn.MRN_F32):

@@ -90,6 +90,8 @@ def test_rows_not_16_byte_aligned(dtype):
     torch.cuda.synchronize()
     s.check("misaligned stream")
     o.check("misaligned normed")
+    gu.check_sandwich(s.host(), o.host(), d["x"], d["residual"], d["gamma"], d["gamma2"],
+                      1e-8, 1e-5, dtype, "misaligned sandwich")
     assert e in (2, 4)
 
 

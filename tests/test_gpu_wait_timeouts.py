@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 def _lib(gpu_lib):
     mrn.mrn_force_geometry(None)
     mrn.mrn_set_launch_options(mrn.MRN_LAUNCH_PDL)
-    mrn.mrn_wait_timeouts()          # (reads and clears the count)
+    mrn.mrn_wait_timeouts()          # (the count since the previous read)
     yield
     mrn.mrn_set_launch_options(mrn.MRN_LAUNCH_PDL)
     mrn.mrn_wait_timeouts()

@@ -95,7 +95,7 @@ def _q8_blocks(x, gamma, eps):
 
 def test_q8_1_gate():
     g = np.random.default_rng(6)
-    rows, n, eps = 8, 512, 1e-6
+    rows, n, eps = 64, 2048, 1e-6                            # ~16 codes within the tie margin
     x = g.standard_normal((rows, n)).astype(np.float32)
     x[0, :32] = 0.0                                          # one all-zero block
     gamma = (1 + 0.1 * g.standard_normal(n)).astype(np.float32)
@@ -144,3 +144,73 @@ def test_seam_gate():
     two.flat[far] = np.uint16(int(u.flat[far]) + 2)
     with pytest.raises(AssertionError):
         gu.check_seam_bits(two, u, alt, near, "two units off")
+
+
+def _sandwich_case():
+    from dual_epsilon_sandwich_gb300 import workloads as wl
+    w = wl.sandwich_decode()
+    a = w.arrays
+    args = (a["block_out"], a["residual"], a["gamma_post"], a["gamma_pre"], w.eps, w.eps_pre)
+    e1, e2 = float(np.float32(w.eps)), float(np.float32(w.eps_pre))
+    s, o = oracle.norm_residual_norm(*(a[k].astype(np.float64) for k in
+                                       ("block_out", "residual", "gamma_post", "gamma_pre")),
+                                     e1, e2)
+    return args, s, o
+
+
+def test_sandwich_strict_gate_on_normed():
+    """normed: a 2e-5 relative error on a well-conditioned element is red even
+    though the end-to-end (carried) bound would admit it; the same error on an
+    element whose stream cancels is admitted by the end-to-end bound and
+    counted as excused; the f32 rounding of the definition is green."""
+    args, s, o = _sandwich_case()
+    got_s, got_o = s.astype(np.float32), o.astype(np.float32)
+    _, _, rep = gu.check_sandwich(got_s, got_o, *args, "f32", "rounded definition")
+    assert rep["excused"] > 0 and rep["strict"] > 0.9 * o.size and rep["worst"] < 1e-7
+    b, r, gp, gq = (np.asarray(v, dtype=np.float64) for v in args[:4])
+    e1, e2 = float(np.float32(args[4])), float(np.float32(args[5]))
+    scale_s = np.abs(oracle.rmsnorm(b, gp, e1)) + np.abs(r)
+    kappa = gu.sandwich_normed_scale(s, gu.F32_TOL * scale_s, gq, e2) / gu.F32_TOL / np.abs(o)
+    well = int(np.argmin(kappa))
+    cancel = int(np.argmax(np.where(kappa < 1e3, kappa, 0.0)))
+    assert kappa.flat[well] <= gu.KAPPA_STRICT < kappa.flat[cancel]
+    bad = got_o.astype(np.float64)
+    bad.flat[well] *= 1 + 2e-5
+    with pytest.raises(AssertionError):
+        gu.check_sandwich(got_s, bad, *args, "f32", "2e-5 on a well-conditioned element")
+    ok = got_o.astype(np.float64)
+    ok.flat[cancel] *= 1 + 2e-5
+    _, _, rep2 = gu.check_sandwich(got_s, ok, *args, "f32", "2e-5 where the stream cancels")
+    assert rep2["excused"] == rep["excused"]
+
+
+def test_sandwich_strict_gate_bf16():
+    """bf16 normed: two units off on an element whose stream cannot flip is red."""
+    from dual_epsilon_sandwich_gb300 import workloads as wl
+    w = wl.llama_bf16(rows=4, n=512)
+    a = w.arrays
+    x, r, g = a["x"], a["residual"], a["gamma"]
+    X, R, G = gu.widen(x, "bf16"), gu.widen(r, "bf16"), gu.widen(g, "bf16")
+    e1, e2 = float(np.float32(1e-8)), float(np.float32(1e-5))
+    raw_s, _ = oracle.norm_residual_norm(X, R, G, G, e1, e2, stream_bf16=False)
+    _, want_o = oracle.norm_residual_norm(X, R, G, G, e1, e2, stream_bf16=True)
+    got_s, got_o = oracle.bf16_from_double(raw_s), oracle.bf16_from_double(want_o)
+    _, _, rep = gu.check_sandwich(got_s, got_o, x, r, g, g, 1e-8, 1e-5, "bf16", "exact")
+    assert rep["worst"] == 0 and rep["strict"] > 0.9 * want_o.size
+    well = np.flatnonzero((gu.bf16_tie_distance(raw_s) > 1e-3 * np.abs(raw_s)).ravel()
+                          & (np.abs(want_o) > 0.5).ravel())[0]
+    bad = got_o.copy()
+    bad.flat[well] = np.uint16(int(bad.flat[well]) + 2)
+    with pytest.raises(AssertionError):
+        gu.check_sandwich(got_s, bad, x, r, g, g, 1e-8, 1e-5, "bf16", "two units off")
+
+
+def test_bf16_tie_distance():
+    """Distance to the nearest bf16 rounding boundary: 0 on a midpoint, half a
+    unit on a representable value, and monotone between."""
+    one = 1.0
+    ulp = 2.0 ** -7
+    v = np.array([one, one + ulp / 2, one + ulp / 4, -one - ulp / 4, 0.0])
+    d = gu.bf16_tie_distance(v)
+    np.testing.assert_allclose(d[:4], [ulp / 2, 0.0, ulp / 4, ulp / 4])
+    assert d[4] > 0
