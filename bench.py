@@ -57,6 +57,11 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-secondary", action="store_true",
                    help="skip the bf16 16384x4096 and f32 4x6656 secondary measurements")
+    p.add_argument("--shard", action="store_true",
+                   help="N > 1: split one global batch of --rows rows into contiguous row "
+                        "blocks, one per rank (strong scaling; gammas replicated, no "
+                        "collective on the data path); default: every rank runs its own "
+                        "--rows batch (weak scaling)")
     p.add_argument("--profile-launches", type=int, default=0,
                    help="only run --warmup + this many launches of the timed call (for ncu)")
     p.add_argument("--profile-op", choices=("sandwich", "seam_f16", "q8_1", "wide_f32",
@@ -85,6 +90,25 @@ def shard_rows(total_rows: int, world: int, rank: int):
     base, extra = divmod(total_rows, world)
     start = rank * base + min(rank, extra)
     return start, start + base + (1 if rank < extra else 0)
+
+
+def shard_plan(total_rows: int, n: int, elem_bytes: int, world: int, rank: int) -> dict:
+    """What one rank runs in the row-sharded mode: rows [row0, row0 + rows) of
+    one global row-major [total_rows x n] batch, held in its own device copy.
+    byte_offset is where that block starts in the global tensor (row0 * n *
+    elem_bytes); the rank calls the library on its copy with `rows` rows, the
+    gammas replicated, and nothing crosses between ranks on the data path."""
+    lo, hi = shard_rows(total_rows, world, rank)
+    return {"row0": lo, "rows": hi - lo, "byte_offset": lo * n * elem_bytes,
+            "bytes": (hi - lo) * n * elem_bytes}
+
+
+def local_block(arrays: dict, plan: dict, row_keys=("block_out", "residual")) -> dict:
+    """This rank's inputs in the row-sharded mode: its row block of every row
+    operand (views of the global host arrays) and every other array (the
+    gammas) whole."""
+    lo, hi = plan["row0"], plan["row0"] + plan["rows"]
+    return {k: (v[lo:hi] if k in row_keys else v) for k, v in arrays.items()}
 
 
 def max_over_ranks(value: float, dist=None, device=None) -> float:
@@ -371,9 +395,15 @@ def run_mrn(args):
     if args.profile_launches and args.profile_op != "sandwich":
         return profile_other(args, dev)
 
-    rows, n = args.rows, args.n
-    w = wl.sandwich_prefill(rows=rows, n=n)
+    global_rows, n = args.rows, args.n
+    w = wl.sandwich_prefill(rows=global_rows, n=n)
     a = w.arrays
+    plan = None
+    if args.shard:
+        # row-sharded: this rank's contiguous block of the one global batch
+        plan = shard_plan(global_rows, n, 4, world, rank)
+        a = local_block(a, plan)
+    rows = plan["rows"] if plan else global_rows
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
 
@@ -431,9 +461,12 @@ def run_mrn(args):
     launches = mrn.mrn_launch_count() - launches0
     local_ms = t_begin.elapsed_time(t_end)
     total_ms = max_over_ranks(local_ms, pg, dev)
-    avg_kernel_ms = local_ms / launches
+    avg_kernel_ms = local_ms / max(1, launches)
     step_bytes = sandwich_bytes(rows, n)
-    value = world * step_bytes * K / (total_ms * 1e-3) / 1e9
+    # whole-job bytes per step: every rank's batch (weak) or the one global batch (sharded)
+    job_bytes = (4 * global_rows * n + 2 * n * world) * 4 if plan else world * step_bytes
+    job_rows = global_rows if plan else world * rows
+    value = job_bytes * K / (total_ms * 1e-3) / 1e9
     achieved = step_bytes / (avg_kernel_ms * 1e-3) / 1e9
 
     # -- end to end through the C ABI with host buffers --------------------
@@ -489,7 +522,7 @@ def run_mrn(args):
     e2e_drain()
     e2e_s = (time.perf_counter() - t0) / args.e2e_steps
     e2e_s = max_over_ranks(e2e_s, pg, dev)
-    e2e_value = world * step_bytes / e2e_s / 1e9
+    e2e_value = job_bytes / e2e_s / 1e9
     # The same steps without the call: the host link's own ceiling for this
     # traffic on this machine, in the same unit.
     t0 = time.perf_counter()
@@ -497,7 +530,7 @@ def run_mrn(args):
         e2e_step(i, call=False)
     e2e_drain()
     link_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, pg, dev)
-    link_value = world * step_bytes / link_s / 1e9
+    link_value = job_bytes / link_s / 1e9
 
     # -- decode latency: rows=1, n=6656 ---------------------------------------
     decode = decode_latency(args, dev, stream)
@@ -505,18 +538,22 @@ def run_mrn(args):
 
     peak, peak_kind = measured_peaks()
     traffic = profiled_traffic()
+    parallelism = (f"one global batch of {global_rows} rows in contiguous row blocks over "
+                   f"{world} ranks ({rows} here, from row {plan['row0']}); gammas replicated, "
+                   f"no exchange" if plan else f"rows x{world}, no exchange")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": total_ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "strong" if plan else "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
         "config": {"workload": w.name, "rows": rows, "n": n, "eps_post": 1e-8, "eps_pre": 1e-5,
-                   "global_batch": rows * world, "parallelism": f"rows x{world}, no exchange",
+                   "global_batch": job_rows, "parallelism": parallelism,
                    "l2": "inputs larger than L2: two resident buffer sets of 436 MB used "
                          "alternately", "geometry": geometry,
                    "launch": "programmatic dependent launch (the library's default; "
                              "mrn_set_launch_options(0) turns it off)"
                    if mrn.mrn_launch_options() & mrn.MRN_LAUNCH_PDL else "stream-ordered"},
-        "rows_per_s": world * rows * K / (total_ms * 1e-3),
+        "rows_per_s": job_rows * K / (total_ms * 1e-3),
         "pct_of_peak": 100.0 * value / (world * peak),
         "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -553,12 +590,55 @@ def run_mrn(args):
                                                             f"{passes1} passes ({elapsed1:.1f} s)"},
                                 "configs": oracle_configs(runner.threads,
                                                           max(0.2, args.cpu_seconds / 10))}
+    # Last in the line, short: every workload's headline figure, so that a
+    # reader who keeps only the end of the line still sees all of them.
+    line["workloads"] = workload_summary(line, peak)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.barrier()
         pg.destroy_process_group()
     return 0
+
+
+def workload_summary(line: dict, peak: float) -> dict:
+    """One compact entry per workload (rounded; the detailed figures are in
+    `decode`, `secondary` and the top-level keys of the same line)."""
+    def r(v, nd=1):
+        return None if v is None else round(float(v), nd)
+
+    dec = line.get("decode") or {}
+    sec = line.get("secondary") or {}
+    out = {
+        "1_rmsnorm_f32_rows4_n6656_us_per_call_graph":
+            r(sec.get("rmsnorm_f32_rows4_n6656", {}).get("us_per_call_graph"), 3),
+        "2_decode_sandwich_f32_rows1_n6656_us_per_call":
+            {"graph": r(dec.get("us_per_call_graph"), 3),
+             "graph_l2_hot": r(dec.get("us_per_call_graph_l2_hot"), 3),
+             "stream": r(dec.get("us_per_call_stream"), 3)} if dec else None,
+        "3_sandwich_f32_rows4096_n6656":
+            {"GB_per_s": r(line["value"]), "pct_of_copy": r(100 * line["value"] /
+                                                             (line["n_gpus"] * peak), 2),
+             "us_per_call": r(1e3 * line["ms_per_step"], 2)},
+    }
+    for key, name in (("4_rmsnorm_bf16_rows16384_n4096_GB_per_s", "rmsnorm_bf16_rows16384_n4096"),
+                      ("4_then_add_bf16_rows16384_n4096_GB_per_s",
+                       "then_add_bf16_rows16384_n4096")):
+        out[key] = r(sec.get(name, {}).get("GB_per_s"))
+    sweep = sec.get("sweep_large_f32") or {}
+    out["5_sweep_f32_GB_per_s_rmsnorm_then_add"] = {
+        shape: [r(e.get("rmsnorm", {}).get("GB_per_s"), 0), r(e.get("then_add", {}).get("GB_per_s"), 0)]
+        for shape, e in sweep.items()} or None
+    nxt = {}
+    for name in ("add_rmsnorm_f32_rows4096_n6656", "then_add_scale_bf16_rows16384_n4096",
+                 "rmsnorm_q8_1_bf16_rows16384_n4096", "qk_norm_bf16_rows163840_n128",
+                 "seam_f16_from_f32_rows4096_n6656", "seam_bf16_from_bf16_rows16384_n4096",
+                 "sandwich_f32_rows4096_n6655", "rmsnorm_f32_rows4096_n6655",
+                 "rmsnorm_f32_rows256_n262144"):
+        if name in sec:
+            nxt[name] = r(sec[name].get("GB_per_s"))
+    out["next_GB_per_s"] = nxt or None
+    return out
 
 
 def decode_latency(args, dev, stream):
@@ -751,7 +831,8 @@ def secondary_workloads(dev, stream):
 def more_ops(dev, stream):
     """The operations beyond the three of the benchmark spec, timed the same way
     (GB/s of algorithmic bytes, two rotating buffer sets larger than L2,
-    seeded torch inputs): residual add + norm at the benchmark's width,
+    seeded torch inputs): residual add + norm at the benchmark's width, the
+    sandwich and plain RMSNorm at one element less (rows not 16-byte aligned),
     then-add-scale and RMSNorm + Q8_1 at 16384 x 4096 bf16, and the per-head
     QK-norm shape (163840 rows of 128, bf16)."""
     import torch
@@ -802,6 +883,17 @@ def more_ops(dev, stream):
         lambda t: check(mrn.mrn_add_rmsnorm(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(),
                                             t[3].data_ptr(), t[4].data_ptr(), rows, n, 1e-5, F,
                                             sh), "add_rmsnorm"))
+    # the benchmark's width minus one: a row pitch of 26,620 bytes (not a multiple
+    # of 16), every row staged as the 16-byte granules that cover it
+    rows, n = 4096, 6655
+    run("sandwich_f32_rows4096_n6655", mrn.MRN_OP_SANDWICH, F, rows, n, (4 * rows * n + 2 * n) * 4,
+        lambda t: check(mrn.mrn_norm_residual_norm(t[0].data_ptr(), t[1].data_ptr(),
+                                                   t[2].data_ptr(), t[2].data_ptr(),
+                                                   t[3].data_ptr(), t[4].data_ptr(), rows, n,
+                                                   1e-8, 1e-5, F, sh), "sandwich n=6655"))
+    run("rmsnorm_f32_rows4096_n6655", mrn.MRN_OP_RMSNORM, F, rows, n, (2 * rows * n + n) * 4,
+        lambda t: check(mrn.mrn_rmsnorm(t[0].data_ptr(), t[2].data_ptr(), t[3].data_ptr(), rows,
+                                        n, 1e-5, F, sh), "rmsnorm n=6655"))
     rows, n = 16384, 4096
     run("then_add_scale_bf16_rows16384_n4096", mrn.MRN_OP_THEN_ADD_SCALE, B, rows, n,
         (3 * rows * n + n + 1) * 2,

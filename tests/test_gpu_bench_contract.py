@@ -40,3 +40,10 @@ def test_bench_line_contract():
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0
     assert line["clocks"]["sm_max_mhz"] > 0
     assert line["decode"]["us_per_call_graph"] > 0
+    # the compact per-workload summary closes the line (the end of the line is
+    # what survives when only a tail of the output is kept)
+    assert list(line)[-1] == "workloads"
+    wk = line["workloads"]
+    assert wk["3_sandwich_f32_rows4096_n6656"]["GB_per_s"] == round(line["value"], 1)
+    assert wk["2_decode_sandwich_f32_rows1_n6656_us_per_call"]["graph"] > 0
+    assert len(json.dumps(wk)) < 2000
