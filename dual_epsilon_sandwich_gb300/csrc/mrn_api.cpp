@@ -16,6 +16,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <initializer_list>
 #include <cmath>
 #include <cstdint>
 
@@ -134,11 +135,35 @@ constexpr int64_t kTmaSharedBudget = mrn::kSharedBytesPerCta - 1024;
 //    over up to 8 CTAs of a cluster so that more SMs pull the row in.
 //  * wider: the looped fallback.
 Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool aligned16,
-                         int sms) {
+                         int sms, bool same_offset = false) {
     Geometry g = {};
     g.vec = aligned16 ? natural_vec(dt) : 1;
     g.cluster = 1;
     const int64_t nvec = ceil_div(n, g.vec);
+    // Batches of rows that are not 16-byte aligned but whose row operands all
+    // sit at one offset within 16 bytes (a row pitch that is not a multiple of
+    // 16 bytes, or operands offset alike): the staged kernel on the 16-byte
+    // granules that cover each row, as for aligned rows (measured on GB300:
+    // see the edge-staged kernel's notes).
+    if (!aligned16 && same_offset && mrn::op_has_edge_staging(op) && rows >= sms) {
+        const int64_t stage = mrn::edge_stage_bytes(n * elem_bytes(dt));
+        const int64_t gran = mrn::edge_granules(n * elem_bytes(dt));
+        if (gran <= 2 * 1024 && nvec > 32 * mrn::kMaxK &&   // (shorter rows: rows per warp)
+            mrn::tma_shared_bytes(op, stage, 2) <= kTmaSharedBudget) {
+            g.kind = mrn::kTma;
+            g.vec = natural_vec(dt);
+            g.stages = 2;
+            g.ctas = 0;
+            g.groups = 2;
+            g.edge = 1;
+            int per_group = 0;
+            pick_threads(gran, &g.k, &per_group, tma_group_cap, 128.0);
+            g.threads = 2 * per_group;
+            g.lanes = 0;
+            g.rows_per_cta = 2;
+            return g;
+        }
+    }
     // RMSNorm + Q8_1 batches of aligned rows: whole 32-element blocks per
     // thread (no shuffles; one reciprocal and one header per block).
     // RMSNorm + Q8_1 batches of aligned rows use the whole-block kernels
@@ -305,6 +330,8 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
 }
 
 bool geometry_is_consistent(const Geometry &g) {
+    // the edge-staged kernel exists with two warp groups and no cluster only
+    if (g.edge && (g.kind != mrn::kTma || g.groups != 2 || g.cluster != 1)) return false;
     if (g.kind == mrn::kRowsPerWarp) {
         const bool pow2 = g.lanes >= 1 && g.lanes <= 32 && (g.lanes & (g.lanes - 1)) == 0;
         return pow2 && g.k >= 1 && g.k <= mrn::kMaxK && g.threads == mrn::kWarpKernelThreads;
@@ -342,7 +369,23 @@ bool geometry_is_consistent(const Geometry &g) {
 // Resolve the thread's forced geometry for one call; false if it cannot
 // cover the row or asks for vectors the pointers do not allow.
 bool resolve_forced(Geometry g, mrn::Op op, int64_t n, mrn_dtype dt, bool aligned16,
-                    Geometry *out) {
+                    Geometry *out, bool same_offset = false) {
+    if (g.edge) {
+        // the edge-staged kernel: 16-byte granules of rows at one offset
+        // (aligned rows are the case of offset 0)
+        if (!mrn::op_has_edge_staging(op) || !(aligned16 || same_offset)) return false;
+        if (g.vec == 0) g.vec = natural_vec(dt);
+        if (g.vec != natural_vec(dt)) return false;
+        const int64_t stage = mrn::edge_stage_bytes(n * elem_bytes(dt));
+        if (static_cast<int64_t>(g.threads / g.groups) * g.k < mrn::edge_granules(n * elem_bytes(dt)))
+            return false;
+        if (mrn::tma_shared_bytes(op, stage, g.stages) > kTmaSharedBudget) return false;
+        g.cluster = 1;
+        g.lanes = 0;
+        g.rows_per_cta = g.groups;
+        *out = g;
+        return true;
+    }
     if (g.vec == 0) g.vec = aligned16 ? natural_vec(dt) : 1;
     if (g.vec != 1 && !(g.vec == natural_vec(dt) && aligned16)) return false;
     const int64_t nvec = ceil_div(n, g.vec);
@@ -423,21 +466,32 @@ mrn_status check_common(int64_t rows, int64_t n, mrn_dtype dt, float eps1, float
 
 bool aligned_to(const void *p, int64_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
+// True when every given pointer sits at the same offset within 16 bytes (then
+// every row of the call starts at one offset in all its row operands).
+bool same_offset16(std::initializer_list<const void *> ptrs) {
+    const uintptr_t m = reinterpret_cast<uintptr_t>(*ptrs.begin()) & 15u;
+    for (const void *p : ptrs)
+        if ((reinterpret_cast<uintptr_t>(p) & 15u) != m) return false;
+    return true;
+}
+
 struct Call {
     mrn::Op op;
     mrn_dtype dt;
     int64_t rows;
     int64_t n;
     KernelArgs args;
+    bool same_offset;   // every row operand at one offset within 16 bytes
 };
 
 mrn_status launch(const Call &c, bool aligned16, cudaStream_t stream) {
     Geometry g;
     if (t_forced) {
-        if (!resolve_forced(t_forced_geometry, c.op, c.n, c.dt, aligned16, &g))
+        if (!resolve_forced(t_forced_geometry, c.op, c.n, c.dt, aligned16, &g, c.same_offset))
             return MRN_ERR_INVALID_GEOMETRY;
     } else {
-        g = choose_geometry(c.op, c.rows, c.n, c.dt, aligned16, sm_count_of_current_device());
+        g = choose_geometry(c.op, c.rows, c.n, c.dt, aligned16, sm_count_of_current_device(),
+                            c.same_offset);
     }
     g.pdl = (t_launch_options & MRN_LAUNCH_PDL) ? 1 : 0;
     KernelArgs a = c.args;
@@ -497,7 +551,7 @@ mrn_status seam_norm(bool weighted, const void *x, const void *gamma, void *y, i
     const bool bf = seam == MRN_BF16;
     const mrn::Op op = weighted ? (bf ? mrn::kSeamBF16 : mrn::kSeamF16)
                                 : (bf ? mrn::kUnweightedBF16 : mrn::kUnweightedF16);
-    Call c{op, dtype, rows, n, KernelArgs{}};
+    Call c{op, dtype, rows, n, KernelArgs{}, false};
     c.args.x = x;
     c.args.g1 = gamma;
     c.args.y = y;
@@ -523,7 +577,7 @@ mrn_status mrn_rmsnorm(const void *x, const void *gamma, void *y, int64_t rows, 
     if (!output_vs_row_input_ok(sy, sx) || overlaps(sy, sg)) return MRN_ERR_ALIASING;
     const bool a16 = (n * e) % 16 == 0 && aligned_to(x, 16) && aligned_to(gamma, 16) &&
                      aligned_to(y, 16);
-    Call c{mrn::kRmsnorm, dtype, rows, n, KernelArgs{}};
+    Call c{mrn::kRmsnorm, dtype, rows, n, KernelArgs{}, same_offset16({x, y})};
     c.args.x = x;
     c.args.g1 = gamma;
     c.args.y = y;
@@ -549,7 +603,7 @@ mrn_status mrn_rmsnorm_then_add(const void *x, const void *gamma, const void *re
         return MRN_ERR_ALIASING;
     const bool a16 = (n * e) % 16 == 0 && aligned_to(x, 16) && aligned_to(gamma, 16) &&
                      aligned_to(residual, 16) && aligned_to(out, 16);
-    Call c{mrn::kThenAdd, dtype, rows, n, KernelArgs{}};
+    Call c{mrn::kThenAdd, dtype, rows, n, KernelArgs{}, same_offset16({x, residual, out})};
     c.args.x = x;
     c.args.res = residual;
     c.args.g1 = gamma;
@@ -583,7 +637,8 @@ mrn_status mrn_norm_residual_norm(const void *block_out, const void *residual,
     const bool a16 = (n * e) % 16 == 0 && aligned_to(block_out, 16) && aligned_to(residual, 16) &&
                      aligned_to(gamma_post, 16) && aligned_to(gamma_pre, 16) &&
                      aligned_to(out_stream, 16) && aligned_to(normed, 16);
-    Call c{mrn::kSandwich, dtype, rows, n, KernelArgs{}};
+    Call c{mrn::kSandwich, dtype, rows, n, KernelArgs{},
+           same_offset16({block_out, residual, out_stream, normed})};
     c.args.x = block_out;
     c.args.res = residual;
     c.args.g1 = gamma_post;
@@ -616,7 +671,7 @@ mrn_status mrn_add_rmsnorm(const void *a, const void *b, const void *gamma, void
     const bool a16 = (n * e) % 16 == 0 && aligned_to(a, 16) && aligned_to(b, 16) &&
                      aligned_to(gamma, 16) && aligned_to(residual_out, 16) &&
                      aligned_to(normed, 16);
-    Call c{mrn::kAddRmsnorm, dtype, rows, n, KernelArgs{}};
+    Call c{mrn::kAddRmsnorm, dtype, rows, n, KernelArgs{}, false};
     c.args.x = a;
     c.args.res = b;
     c.args.g1 = gamma;
@@ -646,7 +701,7 @@ mrn_status mrn_rmsnorm_then_add_scale(const void *x, const void *gamma, const vo
         return MRN_ERR_ALIASING;
     const bool a16 = (n * e) % 16 == 0 && aligned_to(x, 16) && aligned_to(gamma, 16) &&
                      aligned_to(residual, 16) && aligned_to(out, 16);
-    Call c{mrn::kThenAddScale, dtype, rows, n, KernelArgs{}};
+    Call c{mrn::kThenAddScale, dtype, rows, n, KernelArgs{}, same_offset16({x, residual, out})};
     c.args.x = x;
     c.args.res = residual;
     c.args.g1 = gamma;
@@ -673,7 +728,7 @@ mrn_status mrn_rmsnorm_q8_1(const void *x, const void *gamma, void *blocks, int6
     const Span so = span_of(blocks, rows * (n / mrn::kQ8Block) * mrn::kQ8BlockBytes);
     if (overlaps(so, sx) || overlaps(so, sg)) return MRN_ERR_ALIASING;
     const bool a16 = (n * e) % 16 == 0 && aligned_to(x, 16) && aligned_to(gamma, 16);
-    Call c{mrn::kRmsnormQ8, dtype, rows, n, KernelArgs{}};
+    Call c{mrn::kRmsnormQ8, dtype, rows, n, KernelArgs{}, false};
     c.args.x = x;
     c.args.g1 = gamma;
     c.args.y = blocks;
@@ -741,18 +796,21 @@ mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtyp
     if (op < MRN_OP_RMSNORM || op > MRN_OP_RMSNORM_UNWEIGHTED) return MRN_ERR_INVALID_GEOMETRY;
     mrn_status st = check_common(rows, n, dtype, 1.0f, 1.0f);
     if (st != MRN_OK) return st;
-    const bool a16 = aligned16 != 0 && (n * elem_bytes(dtype)) % 16 == 0;
+    // aligned16: 1 = every pointer 16-byte aligned; 2 = the row operands at
+    // one offset within 16 bytes (not all aligned); 0 = neither
+    const bool a16 = aligned16 == 1 && (n * elem_bytes(dtype)) % 16 == 0;
+    const bool same = aligned16 == 2 || (aligned16 == 1 && !a16);
     // (the seam's geometry does not depend on its 16-bit format)
     const mrn::Op iop = op == MRN_OP_RMSNORM_SEAM         ? mrn::kSeamF16
                         : op == MRN_OP_RMSNORM_UNWEIGHTED ? mrn::kUnweightedF16
                                                           : static_cast<mrn::Op>(op);
     Geometry g;
     if (t_forced) {
-        if (!resolve_forced(t_forced_geometry, iop, n, dtype, a16, &g))
+        if (!resolve_forced(t_forced_geometry, iop, n, dtype, a16, &g, same))
             return MRN_ERR_INVALID_GEOMETRY;
     } else {
         g = choose_geometry(iop, rows, n, dtype, a16,
-                            sm_count > 0 ? sm_count : sm_count_of_current_device());
+                            sm_count > 0 ? sm_count : sm_count_of_current_device(), same);
     }
     out->kind = g.kind;
     out->vec = g.vec;
@@ -765,6 +823,7 @@ mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtyp
     out->stages = staged ? g.stages : 0;
     out->ctas = staged ? g.ctas : 0;
     out->groups = staged ? g.groups : 0;
+    out->edge = g.edge;
     return MRN_OK;
 }
 
@@ -783,6 +842,7 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry) {
     g.stages = geometry->stages;
     g.ctas = geometry->ctas;
     g.groups = geometry->groups;
+    g.edge = geometry->edge != 0 ? 1 : 0;
     if ((g.kind == mrn::kTma || (g.kind == mrn::kQ8Blocks && g.stages > 0)) && g.groups == 0)
         g.groups = 1;
     if (g.kind == mrn::kRowsPerWarp && g.threads == 0) g.threads = mrn::kWarpKernelThreads;

@@ -72,6 +72,8 @@ struct KernelArgs {
     float eps2;        // eps_pre (sandwich)
     uint32_t stall_bytes;   // test hook: bytes a CTA's first wait expects beyond its
                             // copies or messages (0 in use; see MRN_LAUNCH_TEST_WAIT_TIMEOUT)
+    uint32_t stage_bytes;   // staged kernel, rows not 16-byte aligned (Geometry::edge):
+                            // bytes between its shared-memory slots (edge_stage_bytes)
 };
 
 struct Geometry {
@@ -86,6 +88,8 @@ struct Geometry {
     int ctas;          // CTAs launched (kTma: persistent grid), 0 = from rows
     int groups;        // warp groups per CTA (kTma), each on its own rows
     int pdl;           // launch with programmatic stream serialisation
+    int edge;          // kTma: rows not 16-byte aligned, staged as the 16-byte granules
+                       // that cover them (every row operand at the same offset)
 };
 
 // Register-slot limits per thread count: the kernels are compiled with these
@@ -156,6 +160,22 @@ constexpr int64_t tma_shared_bytes(int op, int64_t row_bytes, int stages) {
 MRN_HOST_DEVICE constexpr bool op_has_cluster_staging(int op) {
     return op == kRmsnorm || op == kThenAdd || op == kSandwich || op == kThenAddScale;
 }
+// The staged kernel for rows that are not 16-byte aligned (Geometry::edge):
+// the same operations, whose outputs have the row operands' element size.
+MRN_HOST_DEVICE constexpr bool op_has_edge_staging(int op) { return op_has_cluster_staging(op); }
+// Bytes between the shared-memory slots of the edge-staged kernel: a row of
+// row_bytes starting anywhere within a 16-byte granule spans at most this
+// many bytes of granules.
+MRN_HOST_DEVICE constexpr int64_t edge_stage_bytes(int64_t row_bytes) {
+    return (row_bytes + 15) / 16 * 16 + 16;
+}
+// Granules (16-byte loads) of such a row at most.
+MRN_HOST_DEVICE constexpr int64_t edge_granules(int64_t row_bytes) {
+    return edge_stage_bytes(row_bytes) / 16;
+}
+// The edge-staged kernel's persistent grid is a multiple of this many CTAs:
+// rows that far apart start at the same offset within 16 bytes for any n.
+constexpr int kEdgeGridMultiple = 8;
 
 // Number of bounded waits that ran out since the last call (and reset them).
 int take_wait_timeouts_rmsnorm();

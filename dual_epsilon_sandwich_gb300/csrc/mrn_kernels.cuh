@@ -84,6 +84,11 @@ template <> struct Frag<F32, 4> {
 #pragma unroll
         for (int i = 0; i < 4; ++i) w[i] = __float_as_uint(f[i]);
     }
+    __device__ __forceinline__ void clear(int i) { w[i] = 0u; }
+    // element i stored alone at p
+    __device__ __forceinline__ void st_elem(char *p, int i) const {
+        asm volatile("st.global.u32 [%0], %1;" :: "l"(p), "r"(w[i]) : "memory");
+    }
 };
 
 template <> struct Frag<BF16, 8> {
@@ -96,6 +101,12 @@ template <> struct Frag<BF16, 8> {
     __device__ __forceinline__ void put(const float (&f)[8]) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) w[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+    }
+    __device__ __forceinline__ void clear(int i) { w[i >> 1] &= (i & 1) ? 0x0000FFFFu : 0xFFFF0000u; }
+    __device__ __forceinline__ void st_elem(char *p, int i) const {
+        const unsigned short h = static_cast<unsigned short>((i & 1) ? (w[i >> 1] >> 16)
+                                                                     : (w[i >> 1] & 0xFFFFu));
+        asm volatile("st.global.u16 [%0], %1;" :: "l"(p), "h"(h) : "memory");
     }
 };
 
@@ -995,13 +1006,54 @@ __device__ __forceinline__ void ld_shared(Frag<BF16, 8> &f, const void *p) {
                  : "memory");
 }
 
-// Copy one row of x (and of the residual when NS == 2) into a stage.
+// Copy `bytes` of one row of x (and of the residual when NS == 2, into the
+// slot `stride` bytes further on) into a stage.
 template <int NS>
 __device__ __forceinline__ void stage_row(unsigned char *dst, const char *x, const char *res,
-                                          int64_t offset, uint32_t rb, uint64_t *bar) {
-    mbar_arrive_expect_tx(bar, NS * rb);
-    bulk_to_shared(dst, x + offset, rb, bar);
-    if (NS == 2) bulk_to_shared(dst + rb, res + offset, rb, bar);
+                                          int64_t offset, uint32_t bytes, uint32_t stride,
+                                          uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, NS * bytes);
+    bulk_to_shared(dst, x + offset, bytes, bar);
+    if (NS == 2) bulk_to_shared(dst + stride, res + offset, bytes, bar);
+}
+
+// Rows that are not 16-byte aligned, in the staged kernel.  A row that starts
+// `mis` bytes past a 16-byte boundary is staged as the 16-byte granules that
+// cover it: granule v holds the row's bytes [16 v - mis, 16 v - mis + 16).
+// Bytes of a granule outside the row (the start of the first granule, the
+// end of the last) belong to the neighbouring rows or lie past the operand;
+// they are zeroed in registers before any arithmetic and never stored.  Every
+// granule lies in the same 16-byte-aligned memory as a byte of the operand,
+// so reading it cannot leave the operand's pages.
+// Byte range [lo, hi) of granule v that lies inside the row (span = granules).
+__device__ __forceinline__ void granule_bounds(int64_t v, int64_t ngran, uint32_t mis,
+                                               uint32_t rb, uint32_t *lo, uint32_t *hi) {
+    *lo = v == 0 ? mis : 0u;
+    *hi = v == ngran - 1 ? mis + rb - 16u * static_cast<uint32_t>(v) : 16u;
+}
+// Zero the elements of a granule outside [lo, hi).
+template <class T, int VEC>
+__device__ __forceinline__ void mask_granule(Frag<T, VEC> &f, uint32_t lo, uint32_t hi) {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const uint32_t b = static_cast<uint32_t>(i * T::kBytes);
+        if (b < lo || b >= hi) f.clear(i);
+    }
+}
+// Store the elements of granule f that lie in [lo, hi) at the 16-byte-aligned
+// address p: one vector store for a whole granule, else element by element.
+template <class T, int VEC>
+__device__ __forceinline__ void st_granule(char *p, const Frag<T, VEC> &f, uint32_t lo,
+                                           uint32_t hi) {
+    if (lo == 0u && hi == 16u) {
+        st_global(p, f);
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+        const uint32_t b = static_cast<uint32_t>(i * T::kBytes);
+        if (b >= lo && b < hi) f.st_elem(p + b, i);
+    }
 }
 
 // Named barrier `id` over `count` threads (a multiple of 32).
@@ -1047,13 +1099,28 @@ __device__ __forceinline__ float wg_allsum(float v, ReduceSlots &s, int id, int 
 // that sees it raises `abort`; every group stops at its next vote, all meet
 // at a CTA barrier, and thread 0 drains (bounded) every stage copy still in
 // flight before the CTA exits.
-template <int OP, class T, int K, int G>
+//
+// EDGE: rows that are not 16-byte aligned (a row pitch n * s that is not a
+// multiple of 16, or operands offset from a 16-byte boundary), for the plain,
+// then-add, then-add-scale and sandwich operations.  Every row operand and
+// output must sit at the same offset `mis` from a 16-byte boundary in a row,
+// and the host makes the persistent grid a multiple of 8 CTAs, so that all the
+// rows of one CTA share that offset (a CTA's rows are gridDim.x rows apart,
+// and 8 rows advance the offset by a multiple of 16 bytes for any n).  Each
+// row is staged as the granules that cover it (granule_bounds); the gammas are
+// copied element by element into shared memory at offset `mis` of zeroed
+// slots, so that granule v of a staged row and of a gamma slot hold the same
+// elements; edge granules are masked and stored element by element.  Stage
+// slots are a.stage_bytes apart (at least the row's bytes rounded up to 16,
+// plus 16).
+template <int OP, class T, int K, int G, bool EDGE>
 __global__ void __launch_bounds__(tma_max_threads(K, G), 1)
 mrn_tma_kernel(const KernelArgs a, const int stages) {
     constexpr int VEC = 16 / T::kBytes;
     using Fr = Frag<T, VEC>;
     constexpr int NS = op_row_inputs(OP);   // row operands staged per row
     constexpr int NG = op_staged_gammas(OP);   // gammas kept in shared memory
+    static_assert(!EDGE || op_has_edge_staging(OP), "edge staging: plain, then-add(-scale), sandwich");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ ReduceSlots slots1[G];
     __shared__ ReduceSlots slots2[G];
@@ -1063,8 +1130,9 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
     __shared__ volatile int abort_flag;
 
     const uint32_t rb = static_cast<uint32_t>(a.n * T::kBytes);
+    const uint32_t sb = EDGE ? a.stage_bytes : rb;        // bytes between shared-memory slots
     unsigned char *const gsm = smem;
-    unsigned char *const stage0 = smem + NG * rb;
+    unsigned char *const stage0 = smem + NG * sb;
     const int tid = threadIdx.x;
     const int gsize = blockDim.x / G;
     const int grp = tid / gsize;
@@ -1081,6 +1149,28 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
         if (tid == 0) atomicAdd(&g_wait_timeouts, 1u);
         return;
     }
+    // This CTA's rows: `mis` bytes past a 16-byte boundary, `span` bytes of
+    // granules per operand, `ngran` granules (EDGE); else whole 16-byte loads.
+    uint32_t mis = 0;
+    if (EDGE && my_rows > 0)
+        mis = static_cast<uint32_t>((reinterpret_cast<uintptr_t>(xg) + first * row_bytes) & 15u);
+    const uint32_t span = EDGE ? ((mis + rb + 15u) & ~15u) : rb;
+    const int64_t ngran = EDGE ? static_cast<int64_t>(span >> 4) : a.nvec;
+    if (EDGE && my_rows > 0) {
+        // Refuse what the host never launches: a span beyond a slot, rows of
+        // this CTA at different offsets, an operand at another offset (its
+        // bulk copy or vector stores would be misaligned).
+        const uintptr_t off = static_cast<uintptr_t>(first * row_bytes);
+        bool ok = span <= sb &&
+                  (my_rows == 1 || ((step * row_bytes) & 15) == 0) &&
+                  ((reinterpret_cast<uintptr_t>(a.y) + off) & 15u) == mis;
+        if (NS == 2) ok = ok && ((reinterpret_cast<uintptr_t>(rg) + off) & 15u) == mis;
+        if (OP == kSandwich) ok = ok && ((reinterpret_cast<uintptr_t>(a.y2) + off) & 15u) == mis;
+        if (!ok) {
+            if (tid == 0) atomicAdd(&g_wait_timeouts, 1u);
+            return;
+        }
+    }
 
     if (tid == 0) {
         for (int s = 0; s <= stages; ++s) mbar_init(&bars[s], 1);
@@ -1088,21 +1178,66 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
         abort_flag = 0;
         fence_mbar_init();
     }
+    if (EDGE && NG > 0 && my_rows > 0) {
+        for (uint32_t i = tid; i < NG * sb / 4u; i += blockDim.x)
+            reinterpret_cast<uint32_t *>(gsm)[i] = 0u;
+    }
     __syncthreads();
     pdl_enter();   // (the shared-memory set-up above overlapped the previous grid)
+    if (EDGE && NG > 0 && my_rows > 0) {
+        // gamma element j at byte mis + j * s of its (zeroed) slot
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+            const void *gq = q == 0 ? a.g1 : a.g2;
+            unsigned char *dst = gsm + q * sb + mis;
+            for (int64_t j = tid; j < a.n; j += blockDim.x) {
+                if (T::kBytes == 4) {
+                    reinterpret_cast<uint32_t *>(dst)[j] = __ldg(static_cast<const unsigned int *>(gq) + j);
+                } else {
+                    reinterpret_cast<unsigned short *>(dst)[j] =
+                        __ldg(static_cast<const unsigned short *>(gq) + j);
+                }
+            }
+        }
+        __syncthreads();
+    }
     if (tid == 0 && my_rows > 0) {
-        // (NG == 0: completes at once; stall_bytes is a test hook, 0 in use)
-        mbar_arrive_expect_tx(&bars[stages], NG * rb + a.stall_bytes);
-        if (NG >= 1) bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
-        if (NG == 2) bulk_to_shared(gsm + rb, a.g2, rb, &bars[stages]);
+        // The first rows' copies go out before the gammas', and the gammas are
+        // awaited only after a group's first reduction: their arrival overlaps
+        // that row's load and reduction instead of preceding it (measured on
+        // GB300: 4096 x 6656 sandwich 70.8 -> 70.2 us per call).
         for (int s = 0; s < stages && s < my_rows; ++s) {
-            stage_row<NS>(stage0 + s * NS * rb, xg, rg, (first + s * step) * row_bytes, rb,
-                          &bars[s]);
+            stage_row<NS>(stage0 + s * NS * sb, xg, rg, (first + s * step) * row_bytes - mis,
+                          span, sb, &bars[s]);
             issued[s] = 1;
         }
+        // (NG == 0 or EDGE: completes at once; stall_bytes is a test hook, 0 in use)
+        mbar_arrive_expect_tx(&bars[stages], (EDGE ? 0u : NG * rb) + a.stall_bytes);
+        if (!EDGE && NG >= 1) bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
+        if (!EDGE && NG == 2) bulk_to_shared(gsm + rb, a.g2, rb, &bars[stages]);
     }
-    int failed = (my_rows > 0 && !mbar_wait_bounded(&bars[stages], 0)) ? 1 : 0;
+    int failed = 0;
+    bool gammas_in = my_rows == 0;   // the gamma copy awaited (by this thread)
+    if (OP == kAddRmsnorm && my_rows > 0) {
+        // (its sums are stored before the first reduction: wait up front, so a
+        // timed-out copy still means nothing is written)
+        failed = mbar_wait_bounded(&bars[stages], 0) ? 0 : 1;
+        gammas_in = true;
+    }
     const float sc = load_out_scale<OP, T>(a.scale);
+
+    // Store granule v of an output row (out_base + row_byte0 is the row's
+    // first granule): whole vectors, element-wise at the edges (EDGE).
+    auto store = [&](void *out_base, int64_t row_byte0, int64_t v, const Fr &f) {
+        char *p = static_cast<char *>(out_base) + row_byte0 + v * 16;
+        if (EDGE) {
+            uint32_t lo, hi;
+            granule_bounds(v, ngran, mis, rb, &lo, &hi);
+            st_granule(p, f, lo, hi);
+        } else {
+            st_global(p, f);
+        }
+    };
 
     for (int64_t it = grp; it < my_rows; it += G) {
         const int s = static_cast<int>(it % stages);
@@ -1112,13 +1247,21 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
 
         Fr xv[K];
         Fr rv[K];
-        const unsigned char *sp = stage0 + s * NS * rb;
+        const unsigned char *sp = stage0 + s * NS * sb;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
-            if (v < a.nvec) {
+            if (v < ngran) {
                 ld_shared(xv[k], sp + v * 16);
-                if (NS == 2) ld_shared(rv[k], sp + rb + v * 16);
+                if (NS == 2) ld_shared(rv[k], sp + sb + v * 16);
+                if (EDGE) {
+                    uint32_t lo, hi;
+                    granule_bounds(v, ngran, mis, rb, &lo, &hi);
+                    if (lo != 0u || hi != 16u) {
+                        mask_granule(xv[k], lo, hi);
+                        if (NS == 2) mask_granule(rv[k], lo, hi);
+                    }
+                }
             } else {
                 xv[k].zero();
                 rv[k].zero();
@@ -1133,6 +1276,7 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             }
         }
         const int64_t row_elem = row * a.n;
+        const int64_t row_byte0 = row * row_bytes - mis;   // the row's first granule
         float ss = 0.0f;
         if (OP == kAddRmsnorm) {
 #pragma unroll
@@ -1166,9 +1310,21 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             consumed[s] += 1;
             if (it + stages < my_rows) {
                 fence_proxy_async_smem();
-                stage_row<NS>(stage0 + s * NS * rb, xg, rg,
-                              (first + (it + stages) * step) * row_bytes, rb, &bars[s]);
+                stage_row<NS>(stage0 + s * NS * sb, xg, rg,
+                              (first + (it + stages) * step) * row_bytes - mis, span, sb,
+                              &bars[s]);
                 issued[s] += 1;
+            }
+        }
+        if (!gammas_in) {
+            // First row of this group: the gammas must have landed before any
+            // output; the group agrees on a timed-out wait in one vote and stops
+            // before writing anything.
+            gammas_in = true;
+            const int late = (!failed && !mbar_wait_bounded(&bars[stages], 0)) ? 1 : failed;
+            if (group_sync_or(bar_id, gsize, late)) {
+                if (gtid == 0) abort_flag = 1;
+                break;
             }
         }
         const float inv1 = inv_rms(tot, a.n, a.eps1);
@@ -1211,11 +1367,10 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
-                if (v >= a.nvec) continue;
+                if (v >= ngran) continue;
                 Fr g;
                 ld_shared(g, gsm + v * 16);
-                st_global(elem_ptr<T>(a.y, row_elem + v * VEC),
-                          single_norm_output<OP>(xv[k], inv1, g, rv[k], sc));
+                store(a.y, row_byte0, v, single_norm_output<OP>(xv[k], inv1, g, rv[k], sc));
             }
             continue;
         }
@@ -1223,11 +1378,11 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
-            if (v >= a.nvec) continue;
+            if (v >= ngran) continue;
             Fr g;
             ld_shared(g, gsm + v * 16);
             rv[k] = apply_norm_add(xv[k], inv1, g, rv[k]);
-            st_global(elem_ptr<T>(a.y, row_elem + v * VEC), rv[k]);
+            store(a.y, row_byte0, v, rv[k]);
             ss2 += frag_sum_sq(rv[k]);
         }
         const float inv2 = inv_rms(wg_allsum<false>(ss2, slots2[grp], bar_id, gsize, gtid, 0,
@@ -1236,10 +1391,10 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
-            if (v >= a.nvec) continue;
+            if (v >= ngran) continue;
             Fr g;
-            ld_shared(g, gsm + rb + v * 16);
-            st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(rv[k], inv2, g));
+            ld_shared(g, gsm + sb + v * 16);
+            store(a.y2, row_byte0, v, apply_norm(rv[k], inv2, g));
         }
     }
 
@@ -1402,6 +1557,159 @@ __device__ __forceinline__ float cluster_mail_sum(float v, RowMail &m, unsigned 
     return warp_allsum(mine ? (lane == static_cast<int>(crank) ? t : m.box[lane]) : 0.0f);
 }
 
+// Four sums at once (the one-exchange sandwich below): each CTA's four
+// partials travel as one 16-byte st.async message per peer.
+struct Sums4 {
+    float v[4];
+};
+struct RowMail4 {
+    float4 warp[32];
+    float4 box[kMaxCluster];   // [sender rank]
+    uint64_t bar;              // every peer's partials landed
+};
+template <bool USED> struct RowMail4Slot {   // present only where the kernel uses it
+    RowMail4 m;
+};
+template <> struct RowMail4Slot<false> {};
+__device__ __forceinline__ Sums4 warp_allsum4(Sums4 s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s.v[i] += __shfl_xor_sync(0xFFFFFFFFu, s.v[i], o);
+    return s;
+}
+__device__ __forceinline__ void send_f32x4(float4 *box, uint64_t *bar, unsigned rank,
+                                           const Sums4 &t) {
+    uint32_t rbox, rbar;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbox) : "r"(smem_addr(box)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(smem_addr(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                 :: "r"(rbox), "r"(__float_as_uint(t.v[0])), "r"(__float_as_uint(t.v[1])),
+                    "r"(__float_as_uint(t.v[2])), "r"(__float_as_uint(t.v[3])), "r"(rbar)
+                 : "memory");
+}
+// Sums of four values over the CTA and, when cl > 1, over the cluster (every
+// thread of every CTA calls it, as the kernel's first cluster operation: it
+// completes the arrive issued at start).  Every CTA adds the cl partials in
+// rank order, so all get the same bits.  A timed-out message wait sets
+// *timed_out (the row's outputs are then unspecified).
+__device__ __forceinline__ Sums4 cluster_mail_sum4(Sums4 v, RowMail4 &m, unsigned cl,
+                                                   unsigned crank, uint32_t stall,
+                                                   int *timed_out) {
+    v = warp_allsum4(v);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    if (lane == 0) m.warp[warp] = make_float4(v.v[0], v.v[1], v.v[2], v.v[3]);
+    __syncthreads();
+    Sums4 t = {{0.0f, 0.0f, 0.0f, 0.0f}};
+    if (lane < nwarps) {
+        const float4 w = m.warp[lane];
+        t = Sums4{{w.x, w.y, w.z, w.w}};
+    }
+    t = warp_allsum4(t);
+    if (cl == 1) return t;
+    cluster_wait_acquire();
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&m.bar, (cl - 1) * 16u + stall);   // (test hook: 0)
+    if (threadIdx.x < cl && threadIdx.x != crank) send_f32x4(&m.box[crank], &m.bar, threadIdx.x, t);
+    if (!mbar_wait_bounded_cluster(&m.bar, 0)) *timed_out = 1;
+    Sums4 got = {{0.0f, 0.0f, 0.0f, 0.0f}};
+    if (lane < static_cast<int>(cl)) {
+        if (lane == static_cast<int>(crank)) {
+            got = t;
+        } else {
+            const float4 w = m.box[lane];
+            got = Sums4{{w.x, w.y, w.z, w.w}};
+        }
+    }
+    return warp_allsum4(got);
+}
+
+// The f32 sandwich with one reduction on the critical path (the register
+// kernel, for decode).  The stream s = (b * inv1) * g1 + r of the fused tail
+// ("Chapter 12", section 12.4.3) has, in exact arithmetic,
+//   sum s^2 = inv1^2 * sum (b g1)^2 + 2 inv1 * sum (b g1) r + sum r^2,
+// and the three sums on the right need no inv1: they are taken in the first
+// pass, beside sum b^2, and reduced together in one exchange.  Where the
+// terms do not cancel (their magnitudes sum to at most twice the result) the
+// f32 error of the result stays within a few units of 2^-24 per reduction
+// level, as for the direct sum of the stored stream; where they do, the row
+// takes the second reduction of the stored stream, as the general path does.
+// The decision depends only on the reduced sums, so every CTA of the cluster
+// takes the same one.
+template <class T, int VEC, int K, class Reduce4, class Reduce2>
+__device__ __forceinline__ void sandwich_one_exchange(const KernelArgs &a, int64_t row,
+                                                      int64_t first, int64_t stride,
+                                                      Reduce4 reduce4, Reduce2 reduce2,
+                                                      bool *second) {
+    using Fr = Frag<T, VEC>;
+    const int64_t row_elem = row * a.n;
+    Fr xv[K];
+    Fr rv[K];
+    Fr gv[K];
+    bool ok[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int64_t v = first + k * stride;
+        ok[k] = v < a.nvec;
+        const int64_t e = row_elem + v * VEC;
+        if (ok[k]) {
+            ld_stream(xv[k], elem_ptr<T>(a.x, e));
+            ld_stream(rv[k], elem_ptr<T>(a.res, e));
+        } else {
+            xv[k].zero();
+            rv[k].zero();
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (ok[k]) {
+            ld_ro(gv[k], elem_ptr<T>(a.g1, (first + k * stride) * VEC));
+        } else {
+            gv[k].zero();
+        }
+    }
+    Sums4 part = {{0.0f, 0.0f, 0.0f, 0.0f}};   // sum b^2, sum (b g1)^2, sum (b g1) r, sum r^2
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            const float b = xv[k].get(i), r = rv[k].get(i);
+            const float q = b * gv[k].get(i);
+            part.v[0] = fmaf(b, b, part.v[0]);
+            part.v[1] = fmaf(q, q, part.v[1]);
+            part.v[2] = fmaf(q, r, part.v[2]);
+            part.v[3] = fmaf(r, r, part.v[3]);
+        }
+    const Sums4 tot = reduce4(part);
+    const float inv1 = inv_rms(tot.v[0], a.n, a.eps1);
+    const float i2 = inv1 * inv1;
+    const float est = fmaf(i2, tot.v[1], fmaf(2.0f * inv1, tot.v[2], tot.v[3]));
+    const float mag = fmaf(i2, tot.v[1], fmaf(2.0f * inv1, fabsf(tot.v[2]), tot.v[3]));
+    const bool direct = !(est >= 0.5f * mag);   // (a NaN takes the direct sum too)
+    float ss2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (!ok[k]) continue;
+        const int64_t v = first + k * stride;
+        rv[k] = apply_norm_add(xv[k], inv1, gv[k], rv[k]);
+        st_global(elem_ptr<T>(a.y, row_elem + v * VEC), rv[k]);
+        if (direct) ss2 += frag_sum_sq(rv[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (ok[k]) ld_ro(gv[k], elem_ptr<T>(a.g2, (first + k * stride) * VEC));
+    }
+    *second = direct;
+    const float inv2 = inv_rms(direct ? reduce2(ss2) : est, a.n, a.eps2);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        if (!ok[k]) continue;
+        const int64_t v = first + k * stride;
+        st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(rv[k], inv2, gv[k]));
+    }
+}
+
 template <int OP, class T, int VEC, int K>
 __global__ void __launch_bounds__(cta_max_threads(K))
 mrn_cta_kernel(const KernelArgs a) {
@@ -1409,12 +1717,15 @@ mrn_cta_kernel(const KernelArgs a) {
     __shared__ ReduceSlots slots2;
     __shared__ __align__(8) RowMail mail1;
     __shared__ __align__(8) RowMail mail2;
+    constexpr bool kOneExchange = OP == kSandwich && T::kBytes == 4;   // f32 sandwich
+    __shared__ __align__(16) RowMail4Slot<kOneExchange> mail4;
     const unsigned cl = cluster_nctarank();
     const unsigned crank = cluster_ctarank();
     if (cl > 1) {
         if (threadIdx.x == 0) {
             mbar_init(&mail1.bar, 1);
             mbar_init(&mail2.bar, 1);
+            if constexpr (kOneExchange) mbar_init(&mail4.m.bar, 1);
             fence_mbar_init();
         }
         __syncthreads();
@@ -1424,6 +1735,27 @@ mrn_cta_kernel(const KernelArgs a) {
     const int64_t row = a.row0 + cluster_index_x();
     const int64_t first = static_cast<int64_t>(crank) * blockDim.x * K + threadIdx.x;
     int timed_out = 0;
+    if constexpr (kOneExchange) {
+        auto reduce4 = [&](Sums4 v) {
+            return cluster_mail_sum4(v, mail4.m, cl, crank, a.stall_bytes, &timed_out);
+        };
+        auto reduce2 = [&](float v) {
+            return cl > 1 ? cluster_mail_sum(v, mail2, cl, crank, false, 0u, &timed_out)
+                          : cta_allsum(v, slots2, 1, 0, false);
+        };
+        bool second = false;
+        sandwich_one_exchange<T, VEC, K>(a, row, first, blockDim.x, reduce4, reduce2, &second);
+        if (timed_out) {
+            // A late message may still be landing in this CTA: wait once more
+            // (bounded) before leaving; count the timeout once per warp.
+            (void)mbar_wait_bounded_cluster(&mail4.m.bar, 0);
+            if (second) (void)mbar_wait_bounded_cluster(&mail2.bar, 0);
+            const unsigned lanes = __activemask();
+            if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(lanes) - 1))
+                atomicAdd(&g_wait_timeouts, 1u);
+        }
+        return;
+    }
     auto reduce1 = [&](float v) {
         return cl > 1 ? cluster_mail_sum(v, mail1, cl, crank, true, a.stall_bytes, &timed_out)
                       : cta_allsum(v, slots1, 1, 0, false);
@@ -1493,7 +1825,7 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
         if (NG == 2) bulk_to_shared(gsm + sb, static_cast<const char *>(a.g2) + soff, sb,
                                     &bars[stages]);
         for (int st = 0; st < stages && st < my_rows; ++st) {
-            stage_row<NS>(stage0 + st * NS * sb, xg, rg, (first + st * step) * row_bytes, sb,
+            stage_row<NS>(stage0 + st * NS * sb, xg, rg, (first + st * step) * row_bytes, sb, sb,
                           &bars[st]);
             issued[st] = 1;
         }
@@ -1543,7 +1875,7 @@ mrn_tma_cluster_kernel(const KernelArgs a, const int stages) {
             if (it + stages < my_rows) {
                 fence_proxy_async_smem();
                 stage_row<NS>(stage0 + s * NS * sb, xg, rg,
-                              (first + (it + stages) * step) * row_bytes, sb, &bars[s]);
+                              (first + (it + stages) * step) * row_bytes, sb, sb, &bars[s]);
                 issued[s] += 1;
             }
         }
@@ -1890,7 +2222,7 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
         mbar_arrive_expect_tx(&bars[stages], rb + a.stall_bytes);   // (test hook: 0)
         bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
         for (int s = 0; s < stages && s < my_rows; ++s) {
-            stage_row<1>(stage0 + s * rb, xg, nullptr, (first + s * step) * row_bytes, rb,
+            stage_row<1>(stage0 + s * rb, xg, nullptr, (first + s * step) * row_bytes, rb, rb,
                          &bars[s]);
             issued[s] = 1;
         }
@@ -1949,7 +2281,7 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
             if (it + stages < my_rows) {
                 fence_proxy_async_smem();
                 stage_row<1>(stage0 + s * rb, xg, nullptr,
-                             (first + (it + stages) * step) * row_bytes, rb, &bars[s]);
+                             (first + (it + stages) * step) * row_bytes, rb, rb, &bars[s]);
                 issued[s] += 1;
             }
         }
@@ -2121,26 +2453,45 @@ template <int OP, class T, int VEC> struct KernelTable {
 
 template <int OP, class T> struct TmaTable {
     static constexpr WarpKernelFn fn[2][kMaxK] = {
-        {mrn_tma_kernel<OP, T, 1, 1>, mrn_tma_kernel<OP, T, 2, 1>, mrn_tma_kernel<OP, T, 3, 1>,
-         mrn_tma_kernel<OP, T, 4, 1>, mrn_tma_kernel<OP, T, 5, 1>, mrn_tma_kernel<OP, T, 6, 1>,
-         mrn_tma_kernel<OP, T, 7, 1>, mrn_tma_kernel<OP, T, 8, 1>},
-        {mrn_tma_kernel<OP, T, 1, 2>, mrn_tma_kernel<OP, T, 2, 2>, mrn_tma_kernel<OP, T, 3, 2>,
-         mrn_tma_kernel<OP, T, 4, 2>, mrn_tma_kernel<OP, T, 5, 2>, mrn_tma_kernel<OP, T, 6, 2>,
-         mrn_tma_kernel<OP, T, 7, 2>, mrn_tma_kernel<OP, T, 8, 2>}};
+        {mrn_tma_kernel<OP, T, 1, 1, false>, mrn_tma_kernel<OP, T, 2, 1, false>,
+         mrn_tma_kernel<OP, T, 3, 1, false>, mrn_tma_kernel<OP, T, 4, 1, false>,
+         mrn_tma_kernel<OP, T, 5, 1, false>, mrn_tma_kernel<OP, T, 6, 1, false>,
+         mrn_tma_kernel<OP, T, 7, 1, false>, mrn_tma_kernel<OP, T, 8, 1, false>},
+        {mrn_tma_kernel<OP, T, 1, 2, false>, mrn_tma_kernel<OP, T, 2, 2, false>,
+         mrn_tma_kernel<OP, T, 3, 2, false>, mrn_tma_kernel<OP, T, 4, 2, false>,
+         mrn_tma_kernel<OP, T, 5, 2, false>, mrn_tma_kernel<OP, T, 6, 2, false>,
+         mrn_tma_kernel<OP, T, 7, 2, false>, mrn_tma_kernel<OP, T, 8, 2, false>}};
+};
+// Rows that are not 16-byte aligned: two warp groups only.
+template <int OP, class T> struct TmaEdgeTable {
+    static constexpr WarpKernelFn fn[kMaxK] = {
+        mrn_tma_kernel<OP, T, 1, 2, true>, mrn_tma_kernel<OP, T, 2, 2, true>,
+        mrn_tma_kernel<OP, T, 3, 2, true>, mrn_tma_kernel<OP, T, 4, 2, true>,
+        mrn_tma_kernel<OP, T, 5, 2, true>, mrn_tma_kernel<OP, T, 6, 2, true>,
+        mrn_tma_kernel<OP, T, 7, 2, true>, mrn_tma_kernel<OP, T, 8, 2, true>};
 };
 
 template <int OP, class T>
 cudaError_t launch_tma(const Geometry &g, KernelArgs a, int64_t rows, cudaStream_t stream,
                        uint64_t *launches) {
-    static TmaLaunchCache cache[kMaxCachedDevices][2][kMaxK];
+    static TmaLaunchCache cache[kMaxCachedDevices][3][kMaxK];   // [groups - 1 | edge][k - 1]
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     TmaLaunchCache uncached;
-    const int gi = g.groups - 1;
+    const bool edge = g.edge != 0;
+    if (edge && (!op_has_edge_staging(OP) || g.groups != 2)) return cudaErrorInvalidConfiguration;
+    const int gi = edge ? 2 : g.groups - 1;
     TmaLaunchCache &c =
         (dev >= 0 && dev < kMaxCachedDevices) ? cache[dev][gi][g.k - 1] : uncached;
-    const WarpKernelFn fn = TmaTable<OP, T>::fn[gi][g.k - 1];
-    const int64_t shared = tma_shared_bytes(OP, a.n * T::kBytes, g.stages);
+    WarpKernelFn fn = nullptr;
+    if constexpr (op_has_edge_staging(OP)) {
+        fn = edge ? TmaEdgeTable<OP, T>::fn[g.k - 1] : TmaTable<OP, T>::fn[gi][g.k - 1];
+    } else {
+        fn = TmaTable<OP, T>::fn[gi][g.k - 1];
+    }
+    a.stage_bytes = edge ? static_cast<uint32_t>(edge_stage_bytes(a.n * T::kBytes)) : 0u;
+    const int64_t shared =
+        tma_shared_bytes(OP, edge ? edge_stage_bytes(a.n * T::kBytes) : a.n * T::kBytes, g.stages);
     cudaError_t err;
     if (c.shared_opened.load(std::memory_order_relaxed) < shared) {
         err = cudaFuncSetAttribute(reinterpret_cast<const void *>(fn),
@@ -2164,6 +2515,11 @@ cudaError_t launch_tma(const Geometry &g, KernelArgs a, int64_t rows, cudaStream
         }
         ctas = static_cast<int64_t>(device_sm_count()) * per_sm;
         if (ctas < 1) return cudaErrorInvalidDevice;
+    }
+    if (edge) {
+        // a CTA's rows all start at one offset within 16 bytes (see mrn_tma_kernel)
+        ctas = ctas / kEdgeGridMultiple * kEdgeGridMultiple;
+        if (ctas < kEdgeGridMultiple) ctas = kEdgeGridMultiple;
     }
     for (int64_t r0 = 0; r0 < rows; r0 += kRowsPerLaunch) {
         const int64_t nrows = rows - r0 < kRowsPerLaunch ? rows - r0 : kRowsPerLaunch;

@@ -80,7 +80,7 @@ class MrnGeometry(ctypes.Structure):
                 ("threads", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("lanes_per_row", ctypes.c_int32), ("rows_per_cta", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("ctas", ctypes.c_int32),
-                ("groups", ctypes.c_int32)]
+                ("groups", ctypes.c_int32), ("edge", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -195,9 +195,12 @@ def mrn_last_cuda_error() -> int:
 
 
 def mrn_query_geometry(op, rows, n, dtype, aligned16=True, sm_count=0) -> dict:
+    """aligned16: True / 1 (all pointers 16-byte aligned), 2 (the row operands at
+    one offset within 16 bytes) or False / 0."""
     g = MrnGeometry()
-    st = lib().mrn_query_geometry(op, rows, n, dtype, 1 if aligned16 else 0, sm_count,
-                                  ctypes.byref(g))
+    code = aligned16 if isinstance(aligned16, int) and not isinstance(aligned16, bool) \
+        else (1 if aligned16 else 0)
+    st = lib().mrn_query_geometry(op, rows, n, dtype, code, sm_count, ctypes.byref(g))
     if st != 0:
         raise MrnError(st, "mrn_query_geometry")
     return g.as_dict()

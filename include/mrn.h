@@ -42,7 +42,15 @@
  *            in int64.
  * Alignment  Each pointer must be aligned to its element size.  When every
  *            pointer is 16-byte aligned and n * element size is a multiple
- *            of 16, rows are moved in 16-byte vectors; otherwise element-wise.
+ *            of 16, rows are moved in 16-byte vectors.  Otherwise, batches of
+ *            the plain, then-add, then-add-scale and sandwich operations whose
+ *            row operands and outputs all sit at one offset within 16 bytes
+ *            (a row pitch that is not a multiple of 16 bytes on aligned
+ *            buffers, or buffers offset alike) are still read as 16-byte
+ *            granules: each row's granules are copied whole, including up to
+ *            15 bytes before its first and after its last element within the
+ *            same granules (never more), and its edge elements are written
+ *            one by one.  Everything else moves element-wise.
  * Aliasing   An output may be the very same buffer as a row input (same base
  *            pointer): y == x, out == x or out == residual, out_stream ==
  *            residual (the in-place residual update) or out_stream ==
@@ -279,13 +287,22 @@ typedef struct mrn_geometry {
     int32_t ctas;          /* MRN_GEOM_TMA: persistent CTAs (0 = fill the device) */
     int32_t groups;        /* MRN_GEOM_TMA: warp groups per CTA (1 or 2), each
                               reducing its own rows; threads is the CTA total */
+    int32_t edge;          /* MRN_GEOM_TMA, cluster 1, groups 2: rows that are not
+                              16-byte aligned (plain, then-add, then-add-scale,
+                              sandwich; every row operand and output at one offset
+                              within 16 bytes), each staged as the 16-byte granules
+                              that cover it, the edge elements masked and stored one
+                              by one; k * threads / 2 must cover
+                              (n * size + 15) / 16 + 1 granules */
 } mrn_geometry;
 
 /*
- * The geometry an operation would launch with.  aligned16 != 0 states that all
- * pointers would be 16-byte aligned.  sm_count 0 means: ask the current
- * device; a positive value is used as given (lets host-only tests query).
- * The thread's forced geometry, if any, is reported instead.
+ * The geometry an operation would launch with.  aligned16: 1 states that all
+ * pointers would be 16-byte aligned; 2 that they would not, but that every
+ * row operand and output would sit at one offset within 16 bytes; 0 neither.
+ * sm_count 0 means: ask the current device; a positive value is used as
+ * given (lets host-only tests query).  The thread's forced geometry, if any,
+ * is reported instead.
  */
 mrn_status mrn_query_geometry(mrn_op op, int64_t rows, int64_t n, mrn_dtype dtype,
                               int32_t aligned16, int32_t sm_count, mrn_geometry *out);

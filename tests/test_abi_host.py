@@ -265,6 +265,20 @@ def test_geometry_covers_every_row_width():
                             continue
                         g = mrn.mrn_query_geometry(op, rows, n, dt, a16, 152)
                         vec = g["vec"]
+                        if g["edge"]:
+                            # rows not 16-byte aligned, every row operand at one offset
+                            # (aligned buffers with a pitch that is not a multiple of 16)
+                            assert a16 and (n * e) % 16 != 0 and op in (0, 1, 2, 4)
+                            assert g["kind"] == mrn.MRN_GEOM_TMA and g["groups"] == 2
+                            assert vec == 16 // e and rows >= 152 and n > 256
+                            gran = (n * e + 15) // 16 + 1
+                            assert g["threads"] // 2 * g["k"] >= gran and g["cluster"] == 1
+                            assert g["threads"] // 2 % 32 == 0 and g["stages"] == 2
+                            stage = gran * 16
+                            ng = 2 if op == 2 else 1
+                            nin = 1 if op == 0 else 2
+                            assert stage * (ng + 2 * nin) <= 232448 - 1024
+                            continue
                         assert vec == (16 // e if a16 and (n * e) % 16 == 0 else 1)
                         nvec = -(-n // vec)
                         if g["kind"] == mrn.MRN_GEOM_ROWS_PER_WARP:
@@ -407,3 +421,42 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
             "    print('raised', e)\nelse:\n    raise SystemExit('no error')\n")
     res = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
     assert res.returncode == 0 and "raised" in res.stdout, res.stderr
+
+
+def test_unaligned_rows_query_and_force():
+    """Row operands at one offset within 16 bytes (aligned16 = 2) take the
+    edge-staged kernel for batches of the four operations it serves; the
+    others, few rows and short rows move element-wise; a forced edge geometry
+    must be a two-group staged one."""
+    g = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, 4096, 6656, mrn.MRN_F32, 2, 152)
+    assert g["edge"] == 1 and g["kind"] == mrn.MRN_GEOM_TMA and g["vec"] == 4
+    g = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM, 4096, 6655, mrn.MRN_F32, True, 152)
+    assert g["edge"] == 1 and g["threads"] // 2 * g["k"] >= 6655 * 4 // 16 + 2
+    for op in (mrn.MRN_OP_ADD_RMSNORM, mrn.MRN_OP_RMSNORM_SEAM):
+        g = mrn.mrn_query_geometry(op, 4096, 6655, mrn.MRN_F32, 2, 152)
+        assert g["edge"] == 0 and g["vec"] == 1
+    g = mrn.mrn_query_geometry(mrn.MRN_OP_THEN_ADD, 64, 6655, mrn.MRN_F32, 2, 152)
+    assert g["edge"] == 0 and g["vec"] == 1 and g["kind"] == mrn.MRN_GEOM_CTA
+    g = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM, 4096, 7, mrn.MRN_F32, 2, 152)
+    assert g["edge"] == 0 and g["kind"] == mrn.MRN_GEOM_ROWS_PER_WARP
+    g = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM, 4096, 5121, mrn.MRN_BF16, 0, 152)
+    assert g["edge"] == 0 and g["vec"] == 1
+    bad = [{"kind": 2, "k": 4, "threads": 256, "cluster": 1, "edge": 1},
+           {"kind": 4, "k": 4, "threads": 416, "stages": 2, "groups": 1, "edge": 1},
+           {"kind": 4, "k": 4, "threads": 256, "stages": 1, "groups": 1, "cluster": 2, "edge": 1}]
+    for geo in bad:
+        full = {"vec": 0, "lanes_per_row": 0, "stages": 0, "ctas": 0, "groups": 0, "cluster": 1}
+        full.update(geo)
+        assert mrn.mrn_force_geometry(full) == mrn.MRN_ERR_INVALID_GEOMETRY, geo
+    ok = {"kind": 4, "vec": 0, "k": 8, "threads": 448, "cluster": 1, "lanes_per_row": 0,
+          "stages": 2, "ctas": 0, "groups": 2, "edge": 1}
+    assert mrn.mrn_force_geometry(ok) == 0
+    try:
+        g = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, 4096, 6655, mrn.MRN_F32, 2, 152)
+        assert g["edge"] == 1 and g["threads"] == 448
+        with pytest.raises(mrn.MrnError):      # add + norm has no edge-staged form
+            mrn.mrn_query_geometry(mrn.MRN_OP_ADD_RMSNORM, 4096, 6655, mrn.MRN_F32, 2, 152)
+        with pytest.raises(mrn.MrnError):      # 224 x 8 loads per group: 1792 < 1801 granules
+            mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, 4096, 7200, mrn.MRN_F32, 2, 152)
+    finally:
+        mrn.mrn_force_geometry(None)

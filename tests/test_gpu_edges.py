@@ -372,3 +372,31 @@ def test_programmatic_launch_chain_matches(rows, n):
     b1, r1 = chain(mrn.MRN_LAUNCH_PDL)
     assert torch.equal(b0, b1) and torch.equal(r0, r1)
     assert mrn.mrn_wait_timeouts() == 0
+
+
+@pytest.mark.parametrize("rows", [1, 2, 4])
+def test_decode_sandwich_stream_that_cancels(rows):
+    """The f32 register kernel forms the stream's sum of squares from three
+    first-pass sums when they do not cancel, and reduces the stored stream
+    again when they do.  Rows whose block output nearly cancels the residual
+    (the stream about 1/50 of its summands) take the second reduction; the
+    rows between them do not; both match the oracle."""
+    n = 6656
+    g = np.random.default_rng(4401 + rows)
+    r = g.standard_normal((rows, n))
+    gp = 1 + 0.1 * g.standard_normal(n)
+    gq = 1 + 0.1 * g.standard_normal(n)
+    b = g.standard_normal((rows, n)) * 2.0
+    for i in range(0, rows, 2):                  # every other row cancels
+        b[i] = -r[i] * (1 + 1e-3 * g.standard_normal(n)) / gp * 3.0
+    f = [np.asarray(v, dtype=np.float32) for v in (b, r, gp, gq)]
+    geo = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, rows, n, mrn.MRN_F32, True)
+    assert geo["kind"] == mrn.MRN_GEOM_CTA and geo["cluster"] > 1
+    gu.parity_sandwich(*f, 1e-8, 1e-5, "f32", what=f"cancelling {rows}x{n}")
+    e1, e2 = float(np.float32(1e-8)), float(np.float32(1e-5))
+    s, _ = oracle.norm_residual_norm(*(v.astype(np.float64) for v in f), e1, e2)
+    p = oracle.rmsnorm(f[0].astype(np.float64), f[2].astype(np.float64), e1)
+    r64 = f[1].astype(np.float64)
+    mag = np.sum(p * p, axis=1) + 2 * np.abs(np.sum(p * r64, axis=1)) + np.sum(r64 * r64, axis=1)
+    ratio = np.sum(s * s, axis=1) / mag          # the kernel's test: at least 1/2 or not
+    assert np.all(ratio[0::2] < 0.1) and np.all(ratio[1::2] > 0.9)   # both paths taken
