@@ -156,8 +156,13 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
             g.ctas = 0;
             g.groups = 2;
             g.edge = 1;
+            // (measured on GB300, TB/s: 4096 x 6655 f32 sandwich 5.93 at 256 threads x
+            // 7 granules per group vs 5.86 at 224 x 8; 16384 x 4095 bf16 sandwich 5.87
+            // at 192 x 3 vs 5.68 at 96 x 6 and 4.18 at 288 x 2, where fewer CTAs fit
+            // on an SM)
             int per_group = 0;
-            pick_threads(gran, &g.k, &per_group, tma_group_cap, 128.0);
+            pick_threads(gran, &g.k, &per_group, tma_group_cap,
+                         n * elem_bytes(dt) > 16384 ? 256.0 : 192.0);
             g.threads = 2 * per_group;
             g.lanes = 0;
             g.rows_per_cta = 2;
@@ -302,9 +307,14 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     if (dt == MRN_F32 && rows >= sms && cl >= 2 && ceil_div(nvec, kCtaLoads / 2) <= 8)
         cl = ceil_div(nvec, kCtaLoads / 2);
     if (cl > mrn::kMaxCluster) {
+        // Rows past what registers and staged slices hold: the looped kernel, a
+        // cluster of 16 CTAs per row, each looping over 1/16 of it, so that few
+        // rows are in flight and each slice's second read comes from L2
+        // (measured on GB300: see the looped kernel's notes).
         g.kind = mrn::kStream;
         g.threads = mrn::kStreamMaxThreads;
         g.k = 1;
+        g.cluster = mrn::kMaxCluster;
         g.lanes = 0;
         g.rows_per_cta = 1;
         return g;
@@ -342,7 +352,8 @@ bool geometry_is_consistent(const Geometry &g) {
                g.cluster <= mrn::kMaxCluster;
     }
     if (g.kind == mrn::kStream) {
-        return g.threads >= 32 && g.threads % 32 == 0 && g.threads <= mrn::kStreamMaxThreads;
+        return g.threads >= 32 && g.threads % 32 == 0 && g.threads <= mrn::kStreamMaxThreads &&
+               g.cluster >= 1 && g.cluster <= mrn::kMaxCluster;
     }
     if (g.kind == mrn::kQ8Blocks) {
         if (g.k < 1 || g.k > mrn::kQ8BlockMaxK || g.threads < 32 || g.threads % 32 != 0)
@@ -428,9 +439,8 @@ bool resolve_forced(Geometry g, mrn::Op op, int64_t n, mrn_dtype dt, bool aligne
         if (static_cast<int64_t>(g.cluster) * g.threads * g.k < nvec) return false;
         g.lanes = 0;
         g.rows_per_cta = 1;
-    } else {
+    } else {   // the looped kernel: any width, one row per CTA or per cluster
         g.k = 1;
-        g.cluster = 1;
         g.lanes = 0;
         g.rows_per_cta = 1;
     }
@@ -847,8 +857,8 @@ mrn_status mrn_force_geometry(const mrn_geometry *geometry) {
         g.groups = 1;
     if (g.kind == mrn::kRowsPerWarp && g.threads == 0) g.threads = mrn::kWarpKernelThreads;
     if (g.kind == mrn::kStream) g.k = 1;
-    if (g.kind == mrn::kTma && g.cluster == 0) g.cluster = 1;
-    if (g.kind != mrn::kCta && g.kind != mrn::kTma) g.cluster = 1;
+    if ((g.kind == mrn::kTma || g.kind == mrn::kStream) && g.cluster == 0) g.cluster = 1;
+    if (g.kind != mrn::kCta && g.kind != mrn::kTma && g.kind != mrn::kStream) g.cluster = 1;
     if (!geometry_is_consistent(g) || g.vec < 0) return MRN_ERR_INVALID_GEOMETRY;
     t_forced_geometry = g;
     t_forced = true;

@@ -148,6 +148,22 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
     return r;
 }
+// Mixed-precision fma of the bf16 halves of two words into an f32 accumulator:
+// d = a * b + c with the bf16 operands taken exactly (their product is exact
+// in f32; one rounding with c), i.e. fmaf(float(a), float(b), c) without
+// widening the halves first.  lo: the low halves, hi: the high halves.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t wa, uint32_t wb, float c) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}" : "=f"(d) : "r"(wa), "r"(wb), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t wa, uint32_t wb, float c) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}" : "=f"(d) : "r"(wa), "r"(wb), "f"(c));
+    return d;
+}
 // Elements 2p and 2p + 1 of a 16-byte fragment as an f32 pair.
 __device__ __forceinline__ uint64_t frag_pair(const Frag<BF16, 8> &f, int p) {
     const uint32_t w = f.w[p];
@@ -174,6 +190,52 @@ __device__ __forceinline__ void ld_stream(Frag<F32, 1> &f, const void *p) {
 }
 __device__ __forceinline__ void ld_stream(Frag<BF16, 1> &f, const void *p) {
     asm volatile("ld.global.L1::no_allocate.u16 %0, [%1];" : "=h"(f.h) : "l"(p));
+}
+
+// Streaming loads and stores with an L2 eviction-priority policy (the looped
+// kernel: a slice read twice is kept in L2 by its first read and released by
+// its last).  The policy is a createpolicy descriptor.
+__device__ __forceinline__ uint64_t l2_policy_keep() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_drop() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void ld_hint(Frag<F32, 4> &f, const void *p, uint64_t pol) {
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void ld_hint(Frag<BF16, 8> &f, const void *p, uint64_t pol) {
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(f.w[0]), "=r"(f.w[1]), "=r"(f.w[2]), "=r"(f.w[3]) : "l"(p), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void ld_hint(Frag<F32, 1> &f, const void *p, uint64_t pol) {
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
+                 : "=r"(f.w) : "l"(p), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void ld_hint(Frag<BF16, 1> &f, const void *p, uint64_t pol) {
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.u16 %0, [%1], %2;"
+                 : "=h"(f.h) : "l"(p), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_hint(void *p, const Frag<F32, 4> &f, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+                 :: "l"(p), "r"(f.w[0]), "r"(f.w[1]), "r"(f.w[2]), "r"(f.w[3]), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_hint(void *p, const Frag<BF16, 8> &f, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+                 :: "l"(p), "r"(f.w[0]), "r"(f.w[1]), "r"(f.w[2]), "r"(f.w[3]), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_hint(void *p, const Frag<F32, 1> &f, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" :: "l"(p), "r"(f.w), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_hint(void *p, const Frag<BF16, 1> &f, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.u16 [%0], %1, %2;" :: "l"(p), "h"(f.h), "l"(pol) : "memory");
 }
 
 __device__ __forceinline__ void ld_ro(Frag<F32, 4> &f, const void *p) {
@@ -753,169 +815,7 @@ mrn_rows_per_warp_kernel(const KernelArgs a, const int lanes) {
     row_body<OP, T, VEC, K>(a, row, row < a.rows_end, lane_in_row, lanes, reduce, reduce);
 }
 
-// Looped fallback for rows wider than the register-resident geometries
-// hold: one row per CTA, the row is read once for the sum and once more for
-// the output (the second read comes from L2 while the rows in flight fit in
-// it; 256 rows of 1 MB do not, and read DRAM twice).  The sandwich's pre
-// norm re-reads the stream values this same thread stored.  Each iteration
-// handles kStreamUnroll loads per operand so that several are in flight.
-constexpr int kStreamUnroll = 4;
-
-template <int OP, class T, int VEC>
-__global__ void __launch_bounds__(kStreamMaxThreads)
-mrn_stream_kernel(const KernelArgs a) {
-    using Fr = Frag<T, VEC>;
-    constexpr int U = kStreamUnroll;
-    __shared__ ReduceSlots slots1;
-    __shared__ ReduceSlots slots2;
-    pdl_enter();
-    const int64_t row = a.row0 + blockIdx.x;
-    const int64_t row_elem = row * a.n;
-    const int64_t nt = blockDim.x;
-
-    const float sc = load_out_scale<OP, T>(a.scale);
-    float ss = 0.0f;
-    for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
-        Fr x[U], r[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = v0 + u * nt;
-            if (v < a.nvec) {
-                ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
-                if (OP == kAddRmsnorm) ld_stream(r[u], elem_ptr<T>(a.res, row_elem + v * VEC));
-            } else {
-                x[u].zero();
-                r[u].zero();
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (OP == kAddRmsnorm) {
-                const int64_t v = v0 + u * nt;
-                if (v >= a.nvec) continue;
-                x[u] = add_frags(x[u], r[u]);       // residual_out, stored and normed below
-                st_global(elem_ptr<T>(a.y, row_elem + v * VEC), x[u]);
-            }
-            ss += frag_sum_sq(x[u]);
-        }
-    }
-    const float inv1 = inv_rms(cta_allsum(ss, slots1, 1, 0, false), a.n, a.eps1);
-
-    if (OP == kAddRmsnorm) {
-        // re-read the sums this same thread stored
-        for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
-            Fr sm[U], g[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * nt;
-                if (v < a.nvec) {
-                    ld_plain(sm[u], elem_ptr<T>(a.y, row_elem + v * VEC));
-                    ld_ro(g[u], elem_ptr<T>(a.g1, v * VEC));
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * nt;
-                if (v < a.nvec)
-                    st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(sm[u], inv1, g[u]));
-            }
-        }
-        return;
-    }
-    if (OP == kRmsnormQ8) {
-        // The trip count is uniform across each warp (the q8 output shuffles).
-        char *blocks = q8_row_blocks(a, row);
-        const int64_t lane = threadIdx.x & 31;
-        for (int64_t v0 = threadIdx.x; v0 - lane < a.nvec; v0 += nt * U) {
-            Fr x[U], g[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * nt;
-                if (v < a.nvec) {
-                    ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
-                    ld_ro(g[u], elem_ptr<T>(a.g1, v * VEC));
-                } else {
-                    x[u].zero();
-                    g[u].zero();
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * nt;
-                q8_1_output(x[u], g[u], inv1, v < a.nvec, blocks, v);
-            }
-        }
-        return;
-    }
-    if (op_is_seam(OP)) {
-        for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
-            Fr x[U];
-            H16<VEC> g[U] = {};
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * nt;
-                if (v < a.nvec) {
-                    ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
-                    if (op_seam_weighted(OP))
-                        ld_h16(g[u], static_cast<const char *>(a.g1) + v * VEC * 2);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t v = v0 + u * nt;
-                if (v < a.nvec) seam_output<OP, T, VEC>(x[u], inv1, g[u], a.y, row_elem + v * VEC);
-            }
-        }
-        return;
-    }
-
-    float ss2 = 0.0f;
-    for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
-        Fr x[U], g[U], r[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = v0 + u * nt;
-            if (v < a.nvec) {
-                ld_stream(x[u], elem_ptr<T>(a.x, row_elem + v * VEC));
-                ld_ro(g[u], elem_ptr<T>(a.g1, v * VEC));
-                if (OP != kRmsnorm) ld_stream(r[u], elem_ptr<T>(a.res, row_elem + v * VEC));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = v0 + u * nt;
-            if (v >= a.nvec) continue;
-            const int64_t e = row_elem + v * VEC;
-            if (OP == kSandwich) {
-                const Fr o = apply_norm_add(x[u], inv1, g[u], r[u]);
-                st_global(elem_ptr<T>(a.y, e), o);
-                ss2 += frag_sum_sq(o);
-            } else {
-                st_global(elem_ptr<T>(a.y, e), single_norm_output<OP>(x[u], inv1, g[u], r[u], sc));
-            }
-        }
-    }
-    if (OP != kSandwich) return;
-
-    const float inv2 = inv_rms(cta_allsum(ss2, slots2, 1, 0, false), a.n, a.eps2);
-    for (int64_t v0 = threadIdx.x; v0 < a.nvec; v0 += nt * U) {
-        Fr s[U], g[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = v0 + u * nt;
-            if (v < a.nvec) {
-                ld_plain(s[u], elem_ptr<T>(a.y, row_elem + v * VEC));
-                ld_ro(g[u], elem_ptr<T>(a.g2, v * VEC));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t v = v0 + u * nt;
-            if (v < a.nvec)
-                st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(s[u], inv2, g[u]));
-        }
-    }
-}
+constexpr int kStreamUnroll = 4;   // loads per operand in flight per thread (looped kernel)
 
 // ---------------------------------------------------------------------------
 // Persistent, TMA-staged kernel.  Each CTA owns rows blockIdx.x, +gridDim.x,
@@ -943,6 +843,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                  :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+// One arrival (release at CTA scope: this thread's shared-memory writes are
+// visible to threads whose wait completes the phase).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
@@ -1172,35 +1077,23 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
         }
     }
 
+    // EDGE: every thread places part of the gammas and arrives on the gamma
+    // barrier once (thread 0 with its expect_tx arrive), so the gammas complete
+    // that barrier as a bulk copy does and are awaited at the same point.
+    const bool gamma_by_threads = EDGE && NG > 0;
     if (tid == 0) {
-        for (int s = 0; s <= stages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
+        mbar_init(&bars[stages], gamma_by_threads ? blockDim.x : 1u);
         for (int s = 0; s < kTmaMaxStages; ++s) issued[s] = consumed[s] = 0;
         abort_flag = 0;
         fence_mbar_init();
     }
-    if (EDGE && NG > 0 && my_rows > 0) {
+    if (gamma_by_threads && my_rows > 0) {
         for (uint32_t i = tid; i < NG * sb / 4u; i += blockDim.x)
             reinterpret_cast<uint32_t *>(gsm)[i] = 0u;
     }
     __syncthreads();
     pdl_enter();   // (the shared-memory set-up above overlapped the previous grid)
-    if (EDGE && NG > 0 && my_rows > 0) {
-        // gamma element j at byte mis + j * s of its (zeroed) slot
-#pragma unroll
-        for (int q = 0; q < NG; ++q) {
-            const void *gq = q == 0 ? a.g1 : a.g2;
-            unsigned char *dst = gsm + q * sb + mis;
-            for (int64_t j = tid; j < a.n; j += blockDim.x) {
-                if (T::kBytes == 4) {
-                    reinterpret_cast<uint32_t *>(dst)[j] = __ldg(static_cast<const unsigned int *>(gq) + j);
-                } else {
-                    reinterpret_cast<unsigned short *>(dst)[j] =
-                        __ldg(static_cast<const unsigned short *>(gq) + j);
-                }
-            }
-        }
-        __syncthreads();
-    }
     if (tid == 0 && my_rows > 0) {
         // The first rows' copies go out before the gammas', and the gammas are
         // awaited only after a group's first reduction: their arrival overlaps
@@ -1211,10 +1104,57 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
                           span, sb, &bars[s]);
             issued[s] = 1;
         }
-        // (NG == 0 or EDGE: completes at once; stall_bytes is a test hook, 0 in use)
-        mbar_arrive_expect_tx(&bars[stages], (EDGE ? 0u : NG * rb) + a.stall_bytes);
-        if (!EDGE && NG >= 1) bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
-        if (!EDGE && NG == 2) bulk_to_shared(gsm + rb, a.g2, rb, &bars[stages]);
+        if (!gamma_by_threads) {
+            // (NG == 0: completes at once; stall_bytes is a test hook, 0 in use)
+            mbar_arrive_expect_tx(&bars[stages], NG * rb + a.stall_bytes);
+            if (NG >= 1) bulk_to_shared(gsm, a.g1, rb, &bars[stages]);
+            if (NG == 2) bulk_to_shared(gsm + rb, a.g2, rb, &bars[stages]);
+        }
+    }
+    if (gamma_by_threads && my_rows > 0) {
+        // gamma element j to byte mis + j * s of its (zeroed) slot, while the
+        // first rows' copies are in flight: each thread reads whole 16-byte
+        // granules of gamma (the same over-read as for the rows), all its
+        // loads first, and places the elements that belong to gamma
+        constexpr int GL = 4;   // granule loads per gamma and thread in flight
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+            const uintptr_t g0 = reinterpret_cast<uintptr_t>(q == 0 ? a.g1 : a.g2);
+            const uint32_t gm = static_cast<uint32_t>(g0 & 15u);
+            const char *gbase = reinterpret_cast<const char *>(g0 - gm);
+            const int64_t gspan = (gm + rb + 15u) >> 4;
+            unsigned char *dst = gsm + q * sb + mis;   // gamma's byte b - gm goes to dst + b - gm
+            for (int64_t v0 = tid; v0 < gspan; v0 += GL * blockDim.x) {
+                Fr w[GL];
+#pragma unroll
+                for (int u = 0; u < GL; ++u) {
+                    const int64_t v = v0 + u * static_cast<int64_t>(blockDim.x);
+                    if (v < gspan) ld_ro(w[u], gbase + v * 16);
+                }
+#pragma unroll
+                for (int u = 0; u < GL; ++u) {
+                    const int64_t v = v0 + u * static_cast<int64_t>(blockDim.x);
+                    if (v >= gspan) continue;
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) {
+                        const int64_t b = v * 16 + i * T::kBytes;   // byte within gamma's granules
+                        if (b < gm || b >= gm + rb) continue;
+                        if (T::kBytes == 4) {
+                            *reinterpret_cast<uint32_t *>(dst + (b - gm)) = w[u].w[i & 3];
+                        } else {
+                            *reinterpret_cast<unsigned short *>(dst + (b - gm)) =
+                                static_cast<unsigned short>((i & 1) ? (w[u].w[i >> 1] >> 16)
+                                                                    : (w[u].w[i >> 1] & 0xFFFFu));
+                        }
+                    }
+                }
+            }
+        }
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&bars[stages], a.stall_bytes);   // (test hook: 0 in use)
+        } else {
+            mbar_arrive(&bars[stages]);
+        }
     }
     int failed = 0;
     bool gammas_in = my_rows == 0;   // the gamma copy awaited (by this thread)
@@ -1226,11 +1166,23 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
     }
     const float sc = load_out_scale<OP, T>(a.scale);
 
-    // Store granule v of an output row (out_base + row_byte0 is the row's
-    // first granule): whole vectors, element-wise at the edges (EDGE).
-    auto store = [&](void *out_base, int64_t row_byte0, int64_t v, const Fr &f) {
+    // EDGE: the register slots of this thread that hold a partial granule (at
+    // most the row's first and last); the same for every row of the CTA.
+    uint32_t edge_slots = 0;
+    if (EDGE) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+            uint32_t lo, hi;
+            granule_bounds(v, ngran, mis, rb, &lo, &hi);
+            if (v < ngran && (lo != 0u || hi != 16u)) edge_slots |= 1u << k;
+        }
+    }
+    // Store slot k (granule v) of an output row (out_base + row_byte0 is the
+    // row's first granule): whole vectors, element-wise for a partial granule.
+    auto store = [&](void *out_base, int64_t row_byte0, int64_t v, int k, const Fr &f) {
         char *p = static_cast<char *>(out_base) + row_byte0 + v * 16;
-        if (EDGE) {
+        if (EDGE && ((edge_slots >> k) & 1u)) {
             uint32_t lo, hi;
             granule_bounds(v, ngran, mis, rb, &lo, &hi);
             st_granule(p, f, lo, hi);
@@ -1254,13 +1206,11 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             if (v < ngran) {
                 ld_shared(xv[k], sp + v * 16);
                 if (NS == 2) ld_shared(rv[k], sp + sb + v * 16);
-                if (EDGE) {
+                if (EDGE && ((edge_slots >> k) & 1u)) {
                     uint32_t lo, hi;
                     granule_bounds(v, ngran, mis, rb, &lo, &hi);
-                    if (lo != 0u || hi != 16u) {
-                        mask_granule(xv[k], lo, hi);
-                        if (NS == 2) mask_granule(rv[k], lo, hi);
-                    }
+                    mask_granule(xv[k], lo, hi);
+                    if (NS == 2) mask_granule(rv[k], lo, hi);
                 }
             } else {
                 xv[k].zero();
@@ -1370,7 +1320,7 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
                 if (v >= ngran) continue;
                 Fr g;
                 ld_shared(g, gsm + v * 16);
-                store(a.y, row_byte0, v, single_norm_output<OP>(xv[k], inv1, g, rv[k], sc));
+                store(a.y, row_byte0, v, k, single_norm_output<OP>(xv[k], inv1, g, rv[k], sc));
             }
             continue;
         }
@@ -1382,7 +1332,7 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             Fr g;
             ld_shared(g, gsm + v * 16);
             rv[k] = apply_norm_add(xv[k], inv1, g, rv[k]);
-            store(a.y, row_byte0, v, rv[k]);
+            store(a.y, row_byte0, v, k, rv[k]);
             ss2 += frag_sum_sq(rv[k]);
         }
         const float inv2 = inv_rms(wg_allsum<false>(ss2, slots2[grp], bar_id, gsize, gtid, 0,
@@ -1394,7 +1344,7 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             if (v >= ngran) continue;
             Fr g;
             ld_shared(g, gsm + sb + v * 16);
-            store(a.y2, row_byte0, v, apply_norm(rv[k], inv2, g));
+            store(a.y2, row_byte0, v, k, apply_norm(rv[k], inv2, g));
         }
     }
 
@@ -1555,6 +1505,217 @@ __device__ __forceinline__ float cluster_mail_sum(float v, RowMail &m, unsigned 
     if (!mbar_wait_bounded_cluster(&m.bar, 0)) *timed_out = 1;
     const bool mine = lane < static_cast<int>(cl);
     return warp_allsum(mine ? (lane == static_cast<int>(crank) ? t : m.box[lane]) : 0.0f);
+}
+
+// ---------------------------------------------------------------------------
+// Looped kernel for rows wider than the register-resident and staged
+// geometries hold: one row per CTA, or per thread-block cluster of cl CTAs
+// (launched with a cluster dimension), CTA `crank` looping over its slice
+// [vlo, vhi) of the row's loads (a multiple of 32 loads, so a Q8_1 block
+// never straddles two CTAs).  The slice is read once for the sum and once more
+// for the output; the sandwich reads the stream it stored once more for the
+// second norm.  The second read comes from L2 while the rows in flight fit in
+// it: over a cluster of 16, a row's slices are 1/16 of it and only one row per
+// resident cluster is in flight (256 rows of 1 MB: tens of MB), where one row
+// per CTA put every row in flight at once and read DRAM twice.  A reduction
+// over the cluster is one exchange of st.async messages (cluster_mail_sum),
+// as in the register kernel.  Each iteration handles kStreamUnroll loads per
+// operand so that several are in flight.
+// ---------------------------------------------------------------------------
+template <int OP, class T, int VEC>
+__global__ void __launch_bounds__(kStreamMaxThreads)
+mrn_stream_kernel(const KernelArgs a) {
+    using Fr = Frag<T, VEC>;
+    constexpr int U = kStreamUnroll;
+    __shared__ ReduceSlots slots1;
+    __shared__ ReduceSlots slots2;
+    __shared__ __align__(8) RowMail mail1;
+    __shared__ __align__(8) RowMail mail2;
+    const unsigned cl = cluster_nctarank();
+    const unsigned crank = cluster_ctarank();
+    if (cl > 1) {
+        if (threadIdx.x == 0) {
+            mbar_init(&mail1.bar, 1);
+            mbar_init(&mail2.bar, 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        cluster_arrive_relaxed();   // (thread 0: after its initialisation and fence)
+    }
+    pdl_enter();
+    const int64_t row = a.row0 + cluster_index_x();
+    const int64_t row_elem = row * a.n;
+    const int64_t nt = blockDim.x;
+    const int64_t per = ((a.nvec + cl - 1) / cl + 31) / 32 * 32;
+    const int64_t vlo = min(a.nvec, static_cast<int64_t>(crank) * per);
+    const int64_t vhi = min(a.nvec, vlo + per);
+    int timed_out = 0;
+    auto reduce1 = [&](float v) {
+        return cl > 1 ? cluster_mail_sum(v, mail1, cl, crank, true, a.stall_bytes, &timed_out)
+                      : cta_allsum(v, slots1, 1, 0, false);
+    };
+    auto reduce2 = [&](float v) {
+        return cl > 1 ? cluster_mail_sum(v, mail2, cl, crank, false, 0u, &timed_out)
+                      : cta_allsum(v, slots2, 1, 0, false);
+    };
+
+    // A slice read twice stays in L2 between its reads: its first read marks
+    // the lines evict-last, its last read evict-first (as does the re-read of
+    // the sandwich's stream and of add + norm's sum, which are stored evict-last).
+    const uint64_t keep = l2_policy_keep();
+    const uint64_t drop = l2_policy_drop();
+    const float sc = load_out_scale<OP, T>(a.scale);
+    float ss = 0.0f;
+    for (int64_t v0 = vlo + threadIdx.x; v0 < vhi; v0 += nt * U) {
+        Fr x[U], r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = v0 + u * nt;
+            if (v < vhi) {
+                if (OP == kAddRmsnorm) {
+                    ld_hint(x[u], elem_ptr<T>(a.x, row_elem + v * VEC), drop);
+                    ld_stream(r[u], elem_ptr<T>(a.res, row_elem + v * VEC));
+                } else {
+                    ld_hint(x[u], elem_ptr<T>(a.x, row_elem + v * VEC), keep);
+                }
+            } else {
+                x[u].zero();
+                r[u].zero();
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (OP == kAddRmsnorm) {
+                const int64_t v = v0 + u * nt;
+                if (v >= vhi) continue;
+                x[u] = add_frags(x[u], r[u]);       // residual_out, stored and normed below
+                st_hint(elem_ptr<T>(a.y, row_elem + v * VEC), x[u], keep);
+            }
+            ss += frag_sum_sq(x[u]);
+        }
+    }
+    const float inv1 = inv_rms(reduce1(ss), a.n, a.eps1);
+
+    if (OP == kAddRmsnorm) {
+        // re-read the sums this same thread stored
+        for (int64_t v0 = vlo + threadIdx.x; v0 < vhi; v0 += nt * U) {
+            Fr sm[U], g[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < vhi) {
+                    ld_hint(sm[u], elem_ptr<T>(a.y, row_elem + v * VEC), drop);
+                    ld_ro(g[u], elem_ptr<T>(a.g1, v * VEC));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < vhi)
+                    st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(sm[u], inv1, g[u]));
+            }
+        }
+    } else if (OP == kRmsnormQ8) {
+        // The trip count is uniform across each warp (the q8 output shuffles):
+        // the slice starts at a multiple of 32 loads.
+        char *blocks = q8_row_blocks(a, row);
+        const int64_t lane = threadIdx.x & 31;
+        for (int64_t v0 = vlo + threadIdx.x; v0 - lane < vhi; v0 += nt * U) {
+            Fr x[U], g[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < vhi) {
+                    ld_hint(x[u], elem_ptr<T>(a.x, row_elem + v * VEC), drop);
+                    ld_ro(g[u], elem_ptr<T>(a.g1, v * VEC));
+                } else {
+                    x[u].zero();
+                    g[u].zero();
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                q8_1_output(x[u], g[u], inv1, v < vhi, blocks, v);
+            }
+        }
+    } else if (op_is_seam(OP)) {
+        for (int64_t v0 = vlo + threadIdx.x; v0 < vhi; v0 += nt * U) {
+            Fr x[U];
+            H16<VEC> g[U] = {};
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < vhi) {
+                    ld_hint(x[u], elem_ptr<T>(a.x, row_elem + v * VEC), drop);
+                    if (op_seam_weighted(OP))
+                        ld_h16(g[u], static_cast<const char *>(a.g1) + v * VEC * 2);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < vhi) seam_output<OP, T, VEC>(x[u], inv1, g[u], a.y, row_elem + v * VEC);
+            }
+        }
+    } else {
+        float ss2 = 0.0f;
+        for (int64_t v0 = vlo + threadIdx.x; v0 < vhi; v0 += nt * U) {
+            Fr x[U], g[U], r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v < vhi) {
+                    ld_hint(x[u], elem_ptr<T>(a.x, row_elem + v * VEC), drop);
+                    ld_ro(g[u], elem_ptr<T>(a.g1, v * VEC));
+                    if (OP != kRmsnorm) ld_stream(r[u], elem_ptr<T>(a.res, row_elem + v * VEC));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t v = v0 + u * nt;
+                if (v >= vhi) continue;
+                const int64_t e = row_elem + v * VEC;
+                if (OP == kSandwich) {
+                    const Fr o = apply_norm_add(x[u], inv1, g[u], r[u]);
+                    st_hint(elem_ptr<T>(a.y, e), o, keep);
+                    ss2 += frag_sum_sq(o);
+                } else {
+                    st_global(elem_ptr<T>(a.y, e), single_norm_output<OP>(x[u], inv1, g[u], r[u], sc));
+                }
+            }
+        }
+        if (OP == kSandwich) {
+            // the stream as stored, read back by the thread that stored it
+            const float inv2 = inv_rms(reduce2(ss2), a.n, a.eps2);
+            for (int64_t v0 = vlo + threadIdx.x; v0 < vhi; v0 += nt * U) {
+                Fr sv[U], g[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = v0 + u * nt;
+                    if (v < vhi) {
+                        ld_hint(sv[u], elem_ptr<T>(a.y, row_elem + v * VEC), drop);
+                        ld_ro(g[u], elem_ptr<T>(a.g2, v * VEC));
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t v = v0 + u * nt;
+                    if (v < vhi)
+                        st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(sv[u], inv2, g[u]));
+                }
+            }
+        }
+    }
+    if (timed_out) {
+        // A late message may still be landing in this CTA: wait once more
+        // (bounded) before leaving; count the timeout once per warp.
+        (void)mbar_wait_bounded_cluster(&mail1.bar, 0);
+        if (OP == kSandwich) (void)mbar_wait_bounded_cluster(&mail2.bar, 0);
+        const unsigned lanes = __activemask();
+        if ((threadIdx.x & 31) == static_cast<unsigned>(__ffs(lanes) - 1))
+            atomicAdd(&g_wait_timeouts, 1u);
+    }
 }
 
 // Four sums at once (the one-exchange sandwich below): each CTA's four
@@ -2029,6 +2190,59 @@ __device__ __forceinline__ void q8_chunk_words(const uint64_t *xn, bool fast, ui
     }
 }
 
+// Sum of squares of a thread's KB blocks (CH 16-byte chunks each): four
+// independent accumulators per half (short dependency chains), added in one
+// fixed order.  bf16 squares by the mixed-precision fma (the same sums in
+// fewer instructions: measured on GB300, 16384 x 4096 bf16, with the product
+// below, 5.38 -> 5.82 TB/s); f32 two lanes at a time.
+template <class T, int KB, int CH>
+__device__ __forceinline__ float q8_sum_sq(const Frag<T, 16 / T::kBytes> (&xv)[KB][CH]) {
+    constexpr int VEC = 16 / T::kBytes;
+    float acc_lo[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc_hi[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if constexpr (T::kBytes == 2) {
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+#pragma unroll
+                for (int p = 0; p < VEC / 2; ++p) {
+                    const uint32_t w = xv[kb][i].w[p];
+                    const int j = (i * (VEC / 2) + p) & 3;
+                    acc_lo[j] = fma_bf16_lo(w, w, acc_lo[j]);
+                    acc_hi[j] = fma_bf16_hi(w, w, acc_hi[j]);
+                }
+    } else {
+        uint64_t acc[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
+                           f2_pack(0.0f, 0.0f)};
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+#pragma unroll
+                for (int p = 0; p < VEC / 2; ++p) {
+                    const uint64_t xp = frag_pair(xv[kb][i], p);
+                    const int j = (i * (VEC / 2) + p) & 3;
+                    acc[j] = f2_fma(xp, xp, acc[j]);
+                }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f2_unpack(acc[j], acc_lo[j], acc_hi[j]);
+    }
+    return ((acc_lo[0] + acc_hi[0]) + (acc_lo[1] + acc_hi[1])) +
+           ((acc_lo[2] + acc_hi[2]) + (acc_lo[3] + acc_hi[3]));
+}
+
+// x * gamma of elements 2p and 2p + 1 of two chunks as an f32 pair, exact
+// (bf16: the mixed-precision fma with -0 keeps the sign of a zero product).
+template <class T>
+__device__ __forceinline__ uint64_t q8_x_gamma(const Frag<T, 16 / T::kBytes> &x,
+                                               const Frag<T, 16 / T::kBytes> &g, int p) {
+    if constexpr (T::kBytes == 2) {
+        return f2_pack(fma_bf16_lo(x.w[p], g.w[p], -0.0f), fma_bf16_hi(x.w[p], g.w[p], -0.0f));
+    } else {
+        return f2_mul(frag_pair(x, p), frag_pair(g, p));
+    }
+}
+
 template <class T, int KB>
 __global__ void __launch_bounds__(kQ8BlockMaxThreads)
 mrn_q8_block_kernel(const KernelArgs a) {
@@ -2057,24 +2271,7 @@ mrn_q8_block_kernel(const KernelArgs a) {
             }
         }
     }
-    // four independent accumulators (short dependency chains)
-    uint64_t acc[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
-                       f2_pack(0.0f, 0.0f)};
-#pragma unroll
-    for (int k = 0; k < KB; ++k)
-#pragma unroll
-        for (int c = 0; c < CH; ++c)
-#pragma unroll
-            for (int p = 0; p < VEC / 2; ++p) {
-                const uint64_t xp = frag_pair(xv[k][c], p);
-                const int j = (c * (VEC / 2) + p) & 3;
-                acc[j] = f2_fma(xp, xp, acc[j]);
-            }
-    float acc_lo[4], acc_hi[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) f2_unpack(acc[j], acc_lo[j], acc_hi[j]);
-    const float part = ((acc_lo[0] + acc_hi[0]) + (acc_lo[1] + acc_hi[1])) +
-                       ((acc_lo[2] + acc_hi[2]) + (acc_lo[3] + acc_hi[3]));
+    const float part = q8_sum_sq<T, KB, CH>(xv);
     const float inv = inv_rms(cta_allsum(part, slots, 1, 0, false), a.n, a.eps1);
     const uint64_t inv2 = f2_pack(inv, inv);
 
@@ -2091,7 +2288,7 @@ mrn_q8_block_kernel(const KernelArgs a) {
 #pragma unroll
             for (int p = 0; p < VEC / 2; ++p) {
                 // x_normed = (x * gamma) * inv, the page's product order
-                const uint64_t v = f2_mul(f2_mul(frag_pair(xv[k][c], p), frag_pair(g, p)), inv2);
+                const uint64_t v = f2_mul(q8_x_gamma<T>(xv[k][c], g, p), inv2);
                 xn[c * (VEC / 2) + p] = v;
                 float lo, hi;
                 f2_unpack(v, lo, hi);
@@ -2250,24 +2447,7 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
                 }
             }
         }
-        // four independent accumulators (short dependency chains)
-        uint64_t acc[4] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f),
-                           f2_pack(0.0f, 0.0f)};
-#pragma unroll
-        for (int kb = 0; kb < KB; ++kb)
-#pragma unroll
-            for (int i = 0; i < CH; ++i)
-#pragma unroll
-                for (int p = 0; p < VEC / 2; ++p) {
-                    const uint64_t xp = frag_pair(xv[kb][i], p);
-                    const int j = (i * (VEC / 2) + p) & 3;
-                    acc[j] = f2_fma(xp, xp, acc[j]);
-                }
-        float acc_lo[4], acc_hi[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) f2_unpack(acc[j], acc_lo[j], acc_hi[j]);
-        const float part = ((acc_lo[0] + acc_hi[0]) + (acc_lo[1] + acc_hi[1])) +
-                           ((acc_lo[2] + acc_hi[2]) + (acc_lo[3] + acc_hi[3]));
+        const float part = q8_sum_sq<T, KB, CH>(xv);
         int any_failed;
         const float tot = wg_allsum<true>(part, slots[grp], bar_id, gsize, gtid,
                                           failed | abort_flag, &any_failed);
@@ -2302,8 +2482,7 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
 #pragma unroll
                 for (int p = 0; p < VEC / 2; ++p) {
                     // x_normed = (x * gamma) * inv, the page's product order
-                    const uint64_t v =
-                        f2_mul(f2_mul(frag_pair(xv[kb][i], p), frag_pair(g, p)), inv2);
+                    const uint64_t v = f2_mul(q8_x_gamma<T>(xv[kb][i], g, p), inv2);
                     xn[i * (VEC / 2) + p] = v;
                     float lo, hi;
                     f2_unpack(v, lo, hi);
@@ -2683,7 +2862,19 @@ cudaError_t launch_typed(const Geometry &g, KernelArgs a, int64_t rows, cudaStre
             }
             err = cudaLaunchKernelEx(&cfg, fn, a);
         } else {
-            cfg.gridDim = dim3(static_cast<unsigned>(nrows), 1, 1);
+            cfg.gridDim = dim3(static_cast<unsigned>(nrows * g.cluster), 1, 1);
+            if (g.cluster > 1) {
+                if (g.cluster > 8) {
+                    err = cudaFuncSetAttribute(reinterpret_cast<const void *>(Tab::stream),
+                                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                    if (err != cudaSuccess) return err;
+                }
+                cudaLaunchAttribute &c = attr[cfg.numAttrs++];
+                c.id = cudaLaunchAttributeClusterDimension;
+                c.val.clusterDim.x = static_cast<unsigned>(g.cluster);
+                c.val.clusterDim.y = 1;
+                c.val.clusterDim.z = 1;
+            }
             err = cudaLaunchKernelEx(&cfg, Tab::stream, a);
         }
         if (err != cudaSuccess) return err;

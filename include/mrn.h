@@ -261,7 +261,8 @@ typedef enum mrn_geometry_kind {
                                    `cluster` CTAs whose partial sums travel as
                                    st.async messages to the peers' shared memory;
                                    row held in registers */
-    MRN_GEOM_STREAM = 3,        /* one row per CTA, looped over the row: any n */
+    MRN_GEOM_STREAM = 3,        /* one row per CTA, or per cluster of `cluster` CTAs
+                                   each looping over its slice of the row: any n */
     MRN_GEOM_TMA = 4,           /* persistent CTAs; `stages` future rows are copied
                                    into shared memory by cp.async.bulk while the
                                    current one is reduced; gammas kept in shared
@@ -280,7 +281,8 @@ typedef struct mrn_geometry {
     int32_t vec;           /* elements per load: 16 / element size, or 1 */
     int32_t k;             /* loads per operand per thread (register slots) */
     int32_t threads;       /* threads per CTA */
-    int32_t cluster;       /* CTAs per row, 1..16 (MRN_GEOM_CTA or MRN_GEOM_TMA) */
+    int32_t cluster;       /* CTAs per row, 1..16 (MRN_GEOM_CTA, MRN_GEOM_TMA or
+                              MRN_GEOM_STREAM) */
     int32_t lanes_per_row; /* threads per row for MRN_GEOM_ROWS_PER_WARP */
     int32_t rows_per_cta;  /* rows one CTA handles at a time */
     int32_t stages;        /* MRN_GEOM_TMA: rows staged in shared memory (1..8) */

@@ -158,6 +158,9 @@ FORCED = [
     ({"kind": 2, "k": 8, "threads": 256, "cluster": 16}, 32768),
     ({"kind": 3, "threads": 32}, 1999),
     ({"kind": 3, "threads": 512}, 7000),
+    ({"kind": 3, "threads": 64, "cluster": 3}, 1999),       # slices of 32-load multiples,
+    ({"kind": 3, "threads": 256, "cluster": 16}, 7000),     # the last ones short or empty
+    ({"kind": 3, "threads": 512, "cluster": 16}, 65536),
 ]
 
 
@@ -193,8 +196,20 @@ def test_cluster_split_decode_row(cluster):
                                      ("bf16", 270001)])
 def test_wide_rows_use_the_looped_fallback(dtype, n):
     g = mrn.mrn_query_geometry(0, 3, n, gu.code(dtype), True)
-    assert g["kind"] == mrn.MRN_GEOM_STREAM
+    assert g["kind"] == mrn.MRN_GEOM_STREAM and g["cluster"] == 16
     all_ops(rows_data(n, 3, n, dtype), dtype, f"wide n={n}")
+
+
+def test_widest_row_batch():
+    """256 rows of 1 MB (f32, n = 262144): the looped kernel over clusters of 16,
+    sampled rows of all three operations against the oracle, every output
+    written (guard bands, sentinels)."""
+    rows, n = 256, 262144
+    g = mrn.mrn_query_geometry(2, rows, n, mrn.MRN_F32, True)
+    assert g["kind"] == mrn.MRN_GEOM_STREAM and g["cluster"] == 16
+    d = rows_data(262144, rows, n, "f32")
+    sample = gu.sample_rows(rows, 12, 2621)
+    all_ops(d, "f32", f"widest {rows}x{n}", sample)
 
 
 @pytest.mark.parametrize("dtype,n,cluster", [("f32", 16384, 2), ("f32", 32768, 4),

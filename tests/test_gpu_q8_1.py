@@ -79,6 +79,7 @@ GEOMS = [   # (geometry, n for f32, n for bf16); 0 = not coverable
     ({"kind": 1, "lanes_per_row": 4, "k": 4}, 0, 128),
     ({"kind": 2, "k": 2, "threads": 64, "cluster": 4}, 2048, 4096),
     ({"kind": 3, "threads": 96}, 2560, 2560),
+    ({"kind": 3, "threads": 64, "cluster": 5}, 8192, 16384),   # blocks never straddle CTAs
     ({"kind": 4, "k": 1, "threads": 128, "stages": 2, "groups": 2, "ctas": 5}, 256, 512),
     ({"kind": 4, "k": 4, "threads": 256, "stages": 2, "groups": 2}, 2048, 4096),
     ({"kind": 5, "k": 1, "threads": 128}, 4096, 4096),

@@ -57,6 +57,7 @@ GEOMS = [
     {"kind": 2, "k": 3, "threads": 96, "cluster": 1},
     {"kind": 2, "k": 1, "threads": 64, "cluster": 4},
     {"kind": 3, "threads": 96},
+    {"kind": 3, "threads": 64, "cluster": 4},
 ]
 
 
