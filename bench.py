@@ -65,13 +65,15 @@ def parse_args(argv=None):
     p.add_argument("--profile-launches", type=int, default=0,
                    help="only run --warmup + this many launches of the timed call (for ncu)")
     p.add_argument("--profile-op", choices=("sandwich", "seam_f16", "q8_1", "wide_f32",
-                                            "decode", "qk_norm", "add_rmsnorm", "widest_f32"),
+                                            "decode", "qk_norm", "add_rmsnorm", "widest_f32",
+                                            "sandwich_n6655"),
                    default="sandwich",
                    help="with --profile-launches: the call to launch -- the timed sandwich, the "
                         "fused f16 seam at the same shape, RMSNorm + Q8_1 at 16384 x 4096 bf16, "
                         "plain f32 RMSNorm at 1024 x 65536, the decode sandwich (1 x 6656 f32), "
                         "QK-norm (163840 x 128 bf16), residual add + norm (4096 x 6656 f32), or "
-                        "plain f32 RMSNorm at 256 x 262144 (the looped kernel)")
+                        "plain f32 RMSNorm at 256 x 262144 (the looped kernel), or the sandwich "
+                        "at 4096 x 6655 f32 (rows not 16-byte aligned: the edge-staged kernel)")
     return p.parse_args(argv)
 
 
@@ -931,14 +933,16 @@ def profile_other(args, dev):
             return mrn.mrn_rmsnorm_seam(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), rows,
                                         n, 1e-5, mrn.MRN_F32, mrn.MRN_F16, sh)
         geometry = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM_SEAM, rows, n, mrn.MRN_F32, True)
-    elif args.profile_op in ("decode", "add_rmsnorm"):
-        # the decode sandwich tail (1 x 6656 f32, a cluster of 8 CTAs), or the
-        # residual add + norm at the prefill shape (the register batch kernel)
-        rows, n = (1, 6656) if args.profile_op == "decode" else (4096, 6656)
+    elif args.profile_op in ("decode", "add_rmsnorm", "sandwich_n6655"):
+        # the decode sandwich tail (1 x 6656 f32, a cluster of 8 CTAs), the
+        # residual add + norm at the prefill shape (the register batch kernel), or
+        # the sandwich one element narrower (4096 x 6655, the edge-staged kernel)
+        rows, n = {"decode": (1, 6656), "add_rmsnorm": (4096, 6656),
+                   "sandwich_n6655": (4096, 6655)}[args.profile_op]
         sets = [tuple(torch.randn(rows, n, device=dev, generator=gen) for _ in range(2)) +
                 tuple(1 + 0.1 * torch.randn(n, device=dev, generator=gen) for _ in range(2)) +
                 tuple(torch.empty(rows, n, device=dev) for _ in range(2)) for _ in range(2)]
-        if args.profile_op == "decode":
+        if args.profile_op in ("decode", "sandwich_n6655"):
             def call(t):
                 return mrn.mrn_norm_residual_norm(t[0].data_ptr(), t[1].data_ptr(),
                                                   t[2].data_ptr(), t[3].data_ptr(),

@@ -315,7 +315,8 @@ def test_geometry_covers_every_row_width():
                             ns = 1 if op in (0, 5, 6, 7) else 2
                             assert (ng + g["stages"] * ns) * n * e // cl <= 232448 - 1024
                         else:
-                            assert g["kind"] == mrn.MRN_GEOM_STREAM and g["cluster"] == 16
+                            assert g["kind"] == mrn.MRN_GEOM_STREAM
+                            assert g["cluster"] == (8 if rows >= 32 else 16)
                             assert nvec > 16 * 2048
 
 

@@ -196,17 +196,17 @@ def test_cluster_split_decode_row(cluster):
                                      ("bf16", 270001)])
 def test_wide_rows_use_the_looped_fallback(dtype, n):
     g = mrn.mrn_query_geometry(0, 3, n, gu.code(dtype), True)
-    assert g["kind"] == mrn.MRN_GEOM_STREAM and g["cluster"] == 16
+    assert g["kind"] == mrn.MRN_GEOM_STREAM and g["cluster"] == 16   # (few rows)
     all_ops(rows_data(n, 3, n, dtype), dtype, f"wide n={n}")
 
 
 def test_widest_row_batch():
-    """256 rows of 1 MB (f32, n = 262144): the looped kernel over clusters of 16,
+    """256 rows of 1 MB (f32, n = 262144): the looped kernel over clusters of 8,
     sampled rows of all three operations against the oracle, every output
     written (guard bands, sentinels)."""
     rows, n = 256, 262144
     g = mrn.mrn_query_geometry(2, rows, n, mrn.MRN_F32, True)
-    assert g["kind"] == mrn.MRN_GEOM_STREAM and g["cluster"] == 16
+    assert g["kind"] == mrn.MRN_GEOM_STREAM and g["cluster"] == 8
     d = rows_data(262144, rows, n, "f32")
     sample = gu.sample_rows(rows, 12, 2621)
     all_ops(d, "f32", f"widest {rows}x{n}", sample)
