@@ -233,7 +233,17 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     // Q8_1 pass has more arithmetic per byte; both run faster in the register
     // kernel with many CTAs per SM than in the staged one (measured on GB300:
     // add+norm 6.45 vs 6.03 TB/s at 4096 x 6656 f32).
-    const bool staged_pays = op != mrn::kAddRmsnorm && op != mrn::kRmsnormQ8;
+    // Batches of 2048 rows or more of the f32 sandwich run the register kernel
+    // too: there its two norms need only one reduction (the one-exchange form),
+    // and one row per CTA with many CTAs per SM beat the staged kernel.  Measured
+    // on GB300, back to back, register vs staged: 4096 x 6656 67.4 vs 69.9 us
+    // (torch's own copy of the same 436 MB: 66.9 us), 8192 x 6656 128.2 vs 136.8,
+    // 16384 x 4096 155.1 vs 170.7, 4096 x 8192 81.8 vs 86.2, 65536 x 2048 323.6
+    // vs 337.5; but 1216 x 6656 23.9 vs 22.8 (a fit over rows: 15.1 ns per row +
+    // 5.3 us against 16.4 ns + 2.6 us: equal at about 2060 rows).
+    const bool one_exchange_sandwich = op == mrn::kSandwich && dt == MRN_F32;
+    const bool staged_pays = op != mrn::kAddRmsnorm && op != mrn::kRmsnormQ8 &&
+                             !(one_exchange_sandwich && rows >= 2048);
     if (staged_pays && aligned16 && rows >= sms && nvec <= 2 * 1024) {
         // The seam from f32 rows reads twice the bytes it writes; a second
         // stage per group keeps more of those reads in flight (measured on
@@ -325,9 +335,14 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     if (rows * 2 <= sms) {
         // Few rows (decode): spread each row over up to 8 CTAs of a cluster,
         // keeping at least ~192 loads per CTA, so that more SMs pull it in.
+        // The f32 sandwich, with one exchange, goes to 16 CTAs of ~104 loads
+        // (measured on GB300, 1 x 6656 in a CUDA graph over rotating buffers:
+        // 16 x 128 threads 2.08 us, 8 x 224 threads 2.22 us per call).
+        const int64_t cap = one_exchange_sandwich ? 16 : 8;
         const int64_t by_rows = pow2_floor(std::max<int64_t>(1, sms / rows));
-        const int64_t by_width = pow2_floor(std::max<int64_t>(1, nvec / 192));
-        cl = std::max(cl, std::min<int64_t>(8, std::min(by_rows, by_width)));
+        const int64_t by_width =
+            pow2_floor(std::max<int64_t>(1, nvec / (one_exchange_sandwich ? 96 : 192)));
+        cl = std::max(cl, std::min(cap, std::min(by_rows, by_width)));
     }
     if (!staged_pays && rows >= sms) {
         pick_threads_batch(ceil_div(nvec, cl), &g.k, &g.threads,

@@ -976,6 +976,35 @@ __device__ __forceinline__ int group_sync_or(int id, int count, int flag) {
     return any;
 }
 
+// Four sums reduced together (the one-exchange sandwich): butterflies over
+// the warp (all lanes get the same bits), then one slot per warp.
+struct Sums4 {
+    float v[4];
+};
+__device__ __forceinline__ Sums4 warp_allsum4(Sums4 s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s.v[i] += __shfl_xor_sync(0xFFFFFFFFu, s.v[i], o);
+    return s;
+}
+// The same over one warp group (named barrier `id`), ORing a failure flag
+// across the group in the same barrier.
+__device__ __forceinline__ Sums4 wg_allsum4(Sums4 v, float4 *slots, int id, int count, int gtid,
+                                            int flag, int *any) {
+    v = warp_allsum4(v);
+    const int lane = gtid & 31;
+    const int warp = gtid >> 5;
+    if (lane == 0) slots[warp] = make_float4(v.v[0], v.v[1], v.v[2], v.v[3]);
+    *any = group_sync_or(id, count, flag);
+    Sums4 t = {{0.0f, 0.0f, 0.0f, 0.0f}};
+    if (lane < (count >> 5)) {
+        const float4 w = slots[lane];
+        t = Sums4{{w.x, w.y, w.z, w.w}};
+    }
+    return warp_allsum4(t);
+}
+
 // Sum of v over the `count` threads of one warp group (named barrier `id`),
 // optionally ORing a failure flag across the group in the same barrier.
 template <bool VOTE>
@@ -1029,6 +1058,12 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ ReduceSlots slots1[G];
     __shared__ ReduceSlots slots2[G];
+    // The f32 sandwich after a group's first row (gammas in shared memory): its
+    // stream's sum of squares from three first-pass sums, one reduction per row
+    // (as in the register kernel; the stored stream reduced again where those
+    // sums cancel).  Slot sets alternate by row as for single-reduction operations.
+    constexpr bool kOneExchange = OP == kSandwich && T::kBytes == 4;
+    __shared__ __align__(16) float4 slots4[kOneExchange ? 2 : 1][G][32];
     __shared__ __align__(8) uint64_t bars[kTmaMaxStages + 1];   // [stages] = the gammas
     __shared__ int issued[kTmaMaxStages];
     __shared__ int consumed[kTmaMaxStages];
@@ -1228,7 +1263,26 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
         const int64_t row_elem = row * a.n;
         const int64_t row_byte0 = row * row_bytes - mis;   // the row's first granule
         float ss = 0.0f;
-        if (OP == kAddRmsnorm) {
+        const bool fused = kOneExchange && gammas_in;       // (uniform over the group)
+        Sums4 part = {{0.0f, 0.0f, 0.0f, 0.0f}};            // sum b^2, (b g1)^2, (b g1) r, r^2
+        if (kOneExchange && fused) {
+#pragma unroll
+            for (int k = 0; k < K; ++k) {
+                const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
+                if (v >= ngran) continue;
+                Fr g;
+                ld_shared(g, gsm + v * 16);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) {
+                    const float bx = xv[k].get(i), r = rv[k].get(i);
+                    const float q = bx * g.get(i);
+                    part.v[0] = fmaf(bx, bx, part.v[0]);
+                    part.v[1] = fmaf(q, q, part.v[1]);
+                    part.v[2] = fmaf(q, r, part.v[2]);
+                    part.v[3] = fmaf(r, r, part.v[3]);
+                }
+            }
+        } else if (OP == kAddRmsnorm) {
 #pragma unroll
             for (int k = 0; k < K; ++k) {
                 const int64_t v = gtid + static_cast<int64_t>(k) * gsize;
@@ -1249,8 +1303,15 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
         // the uses of each set.
         ReduceSlots &rs1 = (OP != kSandwich && ((it / G) & 1)) ? slots2[grp] : slots1[grp];
         int any_failed;
-        const float tot = wg_allsum<true>(ss, rs1, bar_id, gsize, gtid, failed | abort_flag,
-                                             &any_failed);
+        Sums4 tot4 = {{0.0f, 0.0f, 0.0f, 0.0f}};
+        float tot;
+        if (kOneExchange && fused) {
+            tot4 = wg_allsum4(part, slots4[kOneExchange ? ((it / G) & 1) : 0][grp], bar_id, gsize,
+                              gtid, failed | abort_flag, &any_failed);
+            tot = tot4.v[0];
+        } else {
+            tot = wg_allsum<true>(ss, rs1, bar_id, gsize, gtid, failed | abort_flag, &any_failed);
+        }
         if (any_failed) {
             if (gtid == 0) abort_flag = 1;
             break;
@@ -1324,6 +1385,16 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             }
             continue;
         }
+        // (one exchange: sum s^2 = inv1^2 A + 2 inv1 B + C where those terms do not
+        // cancel -- their magnitudes sum to at most twice the result)
+        bool direct = true;
+        float est = 0.0f;
+        if (kOneExchange && fused) {
+            const float i2 = inv1 * inv1;
+            est = fmaf(i2, tot4.v[1], fmaf(2.0f * inv1, tot4.v[2], tot4.v[3]));
+            const float mag = fmaf(i2, tot4.v[1], fmaf(2.0f * inv1, fabsf(tot4.v[2]), tot4.v[3]));
+            direct = !(est >= 0.5f * mag);
+        }
         float ss2 = 0.0f;
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -1333,10 +1404,11 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             ld_shared(g, gsm + v * 16);
             rv[k] = apply_norm_add(xv[k], inv1, g, rv[k]);
             store(a.y, row_byte0, v, k, rv[k]);
-            ss2 += frag_sum_sq(rv[k]);
+            if (direct) ss2 += frag_sum_sq(rv[k]);
         }
-        const float inv2 = inv_rms(wg_allsum<false>(ss2, slots2[grp], bar_id, gsize, gtid, 0,
-                                                       nullptr),
+        const float inv2 = inv_rms(direct ? wg_allsum<false>(ss2, slots2[grp], bar_id, gsize, gtid,
+                                                              0, nullptr)
+                                          : est,
                                    a.n, a.eps2);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
@@ -1720,9 +1792,6 @@ mrn_stream_kernel(const KernelArgs a) {
 
 // Four sums at once (the one-exchange sandwich below): each CTA's four
 // partials travel as one 16-byte st.async message per peer.
-struct Sums4 {
-    float v[4];
-};
 struct RowMail4 {
     float4 warp[32];
     float4 box[kMaxCluster];   // [sender rank]
@@ -1732,13 +1801,6 @@ template <bool USED> struct RowMail4Slot {   // present only where the kernel us
     RowMail4 m;
 };
 template <> struct RowMail4Slot<false> {};
-__device__ __forceinline__ Sums4 warp_allsum4(Sums4 s) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) s.v[i] += __shfl_xor_sync(0xFFFFFFFFu, s.v[i], o);
-    return s;
-}
 __device__ __forceinline__ void send_f32x4(float4 *box, uint64_t *bar, unsigned rank,
                                            const Sums4 &t) {
     uint32_t rbox, rbar;

@@ -401,8 +401,14 @@ def test_force_geometry_validation():
     with pytest.raises(mrn.MrnError):          # (2 + 4*2) rows of 26 KB exceed 227 KB
         mrn.mrn_query_geometry(2, 4096, 6656, mrn.MRN_F32, True, 152)
     assert mrn.mrn_force_geometry(None) == 0
-    assert mrn.mrn_query_geometry(2, 4096, 6656, mrn.MRN_F32, True, 152)["kind"] == 4
-    assert mrn.mrn_query_geometry(2, 1, 6656, mrn.MRN_F32, True, 152)["kind"] == 2
+    # automatic: the f32 sandwich batch in the register kernel (one reduction per row),
+    # the bf16 one staged; decode over a cluster of 16 (f32) or 4 (bf16, 832 loads)
+    got = mrn.mrn_query_geometry(2, 4096, 6656, mrn.MRN_F32, True, 152)
+    assert (got["kind"], got["k"], got["threads"], got["cluster"]) == (2, 7, 256, 1)
+    assert mrn.mrn_query_geometry(2, 4096, 6656, mrn.MRN_BF16, True, 152)["kind"] == 4
+    got = mrn.mrn_query_geometry(2, 1, 6656, mrn.MRN_F32, True, 152)
+    assert (got["kind"], got["threads"], got["cluster"]) == (2, 128, 16)
+    assert mrn.mrn_query_geometry(2, 1, 6656, mrn.MRN_BF16, True, 152)["cluster"] == 4
 
 
 def test_launch_options():

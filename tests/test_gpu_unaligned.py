@@ -207,3 +207,30 @@ def test_prefill_width_minus_one_full_size():
     sample = gu.sample_rows(rows, 96, 9105)
     gu.parity_sandwich(a["block_out"], a["residual"], a["gamma_post"], a["gamma_pre"], w.eps,
                        w.eps_pre, "f32", rows_sample=sample, what="4096x6655 sandwich")
+
+
+@pytest.mark.parametrize("n,forced", [(6655, None), (6656, _edge_geometry(512, 7)),
+                                      (6656, dict(_edge_geometry(832, 4), edge=0))])
+def test_staged_sandwich_one_exchange_rows_that_cancel(n, forced):
+    """The staged f32 sandwich reduces the stream's three first-pass sums with
+    the first norm's (after each warp group's first row) and reduces the
+    stored stream again only where those sums cancel.  1216 rows (four per
+    warp group), every third row's block output nearly cancelling its
+    residual: both kinds of rows, and first rows, against the oracle."""
+    rows = 1216
+    g = np.random.default_rng(4500 + n)
+    r = g.standard_normal((rows, n))
+    gp = 1 + 0.1 * g.standard_normal(n)
+    gq = 1 + 0.1 * g.standard_normal(n)
+    b = g.standard_normal((rows, n)) * 2.0
+    for i in range(0, rows, 3):
+        b[i] = -r[i] * (1 + 1e-3 * g.standard_normal(n)) / gp * 3.0
+    f = [np.asarray(v, dtype=np.float32) for v in (b, r, gp, gq)]
+    if forced is not None:
+        assert mrn.mrn_force_geometry(forced) == 0
+    geo = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, rows, n, mrn.MRN_F32, True)
+    assert geo["kind"] == mrn.MRN_GEOM_TMA
+    try:
+        gu.parity_sandwich(*f, 1e-8, 1e-5, "f32", what=f"staged one exchange {rows}x{n}")
+    finally:
+        mrn.mrn_force_geometry(None)

@@ -47,19 +47,23 @@ def untouched(g: gu.Guarded) -> bool:
     return bool((g.raw == g.sentinel).all())
 
 
-def test_staged_kernel_stops_without_writing():
-    rows, n = 304, 6656
-    g = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, rows, n, mrn.MRN_F32, True)
-    assert (g["kind"], g["cluster"]) == (mrn.MRN_GEOM_TMA, 1)
-    d = wl.random_rows(41, rows, n, "f32")
-    b, r = gu.to_device(d["x"], "f32"), gu.to_device(d["residual"], "f32")
-    gp, gq = gu.to_device(d["gamma"], "f32"), gu.to_device(d["gamma2"], "f32")
-    s, o = gu.Guarded(rows, n, "f32"), gu.Guarded(rows, n, "f32")
+@pytest.mark.parametrize("dtype,n", [("bf16", 6656), ("f32", 6655)])
+def test_staged_kernel_stops_without_writing(dtype, n):
+    """The staged sandwich (bf16: both gammas by bulk copy; f32 at n = 6655: the
+    edge-staged kernel, whose threads place the gammas and arrive on the same
+    barrier) stops at the gamma wait's timeout before writing anything."""
+    rows = 304
+    g = mrn.mrn_query_geometry(mrn.MRN_OP_SANDWICH, rows, n, gu.code(dtype), True)
+    assert (g["kind"], g["cluster"], g["edge"]) == (mrn.MRN_GEOM_TMA, 1, int(dtype == "f32"))
+    d = wl.random_rows(41, rows, n, dtype)
+    b, r = gu.to_device(d["x"], dtype), gu.to_device(d["residual"], dtype)
+    gp, gq = gu.to_device(d["gamma"], dtype), gu.to_device(d["gamma2"], dtype)
+    s, o = gu.Guarded(rows, n, dtype), gu.Guarded(rows, n, dtype)
     st, seconds, count = stalled(
-        lambda: gu.call_sandwich(b, r, gp, gq, s, o, rows, n, 1e-8, 1e-5, "f32"))
+        lambda: gu.call_sandwich(b, r, gp, gq, s, o, rows, n, 1e-8, 1e-5, dtype))
     assert st == 0 and count >= 1 and seconds < 30, (st, count, seconds)
     assert untouched(s) and untouched(o)
-    gu.parity_sandwich(d["x"], d["residual"], d["gamma"], d["gamma2"], 1e-8, 1e-5, "f32",
+    gu.parity_sandwich(d["x"], d["residual"], d["gamma"], d["gamma2"], 1e-8, 1e-5, dtype,
                        what="staged sandwich after a timeout")
     assert mrn.mrn_wait_timeouts() == 0
 
