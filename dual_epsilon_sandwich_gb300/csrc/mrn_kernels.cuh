@@ -2430,7 +2430,9 @@ cudaError_t launch_q8_blocks(const Geometry &g, KernelArgs a, int64_t rows, cuda
 // so that the eight lanes of a 16-byte shared load touch eight different
 // bank groups; register slot i then holds chunk (i + rot) % CH, and its codes
 // are written at that chunk's offset.  Each group assembles its row's blocks
-// in its own shared-memory buffer, then copies them out with coalesced stores.
+// in its own shared-memory buffer; one thread then copies the row out with a
+// single bulk copy (cp.async.bulk shared -> global) when the row's bytes and
+// address are 16-byte multiples, else the group copies it word by word.
 
 template <class T, int KB, int G>
 __global__ void __launch_bounds__(G * kQ8TmaGroupThreads, 1)
@@ -2510,6 +2512,8 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
             }
         }
         const float part = q8_sum_sq<T, KB, CH>(xv);
+        // the previous row's bulk copy has read the group's block buffer
+        if (gtid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         int any_failed;
         const float tot = wg_allsum<true>(part, slots[grp], bar_id, gsize, gtid,
                                           failed | abort_flag, &any_failed);
@@ -2573,14 +2577,16 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
                     *reinterpret_cast<uint32_t *>(blk + 4 + cc * VEC + 4 * q) = w[q];
             }
         }
-        group_sync(bar_id, gsize);   // the group's blocks of this row are complete
         const int64_t bytes = static_cast<int64_t>(nb) * kQ8BlockBytes;
         char *const out = static_cast<char *>(a.y) + row * bytes;
-        if ((bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
-            for (int64_t i = gtid; i < bytes / 16; i += gsize) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(ob + i * 16);
-                asm volatile(MRN_ST_OP ".v4.u32 [%0], {%1,%2,%3,%4};"
-                             :: "l"(out + i * 16), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+        const bool bulk = (bytes & 15) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+        if (bulk) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        group_sync(bar_id, gsize);   // the group's blocks of this row are complete
+        if (bulk) {
+            if (gtid == 0) {
+                asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
+                             "cp.async.bulk.commit_group;"
+                             :: "l"(out), "r"(smem_addr(ob)), "r"(static_cast<uint32_t>(bytes))
                              : "memory");
             }
         } else {
@@ -2590,11 +2596,13 @@ mrn_q8_tma_kernel(const KernelArgs a, const int stages) {
             }
         }
         // (the next row writes this buffer only after its first reduction's
-        // barrier, which every thread of the group reaches after this copy)
+        // barrier, which every thread of the group reaches after this copy, and
+        // which the issuing thread enters only once the bulk copy has read it)
     }
 
     // Exit: as mrn_tma_kernel -- after a failure, wait (bounded) for the
     // copies still in flight before the CTA leaves its shared memory.
+    if (gtid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     __syncthreads();
     if (tid == 0 && my_rows > 0 && abort_flag) {
         atomicAdd(&g_wait_timeouts, 1u);
