@@ -176,15 +176,16 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     //   f32: staged (persistent, x bulk-copied two stages ahead) everywhere --
     //        n = 1024: 4.2, 2048: 6.4, 4096: 6.3 (2 blocks per thread),
     //        16384: 5.6 (one group: two do not fit in shared memory);
-    //   bf16: staged with 2 blocks per thread from n = 4096 (4.9 at 4096, 4.8
-    //        at 16384), one row per CTA at n = 2048 (4.9 vs 4.4 staged); below,
-    //        the lane-layout kernels (n = 1024: 4.0 vs 3.1).
+    //   bf16: staged from n = 2048 (1 block per thread at 2048: 5.1 vs 4.8 for
+    //        one row per CTA; 2 blocks per thread from 4096: 5.9 at 4096, 4.9 at
+    //        4096 rows of 6656); below, the lane-layout kernels (n = 1024: 4.0
+    //        vs 3.1 staged).
     const int64_t nblocks = n / mrn::kQ8Block;
     const int64_t max_staged = static_cast<int64_t>(mrn::kQ8BlockMaxK) * mrn::kQ8TmaGroupThreads;
     if (op == mrn::kRmsnormQ8 && aligned16 && rows >= sms && nblocks >= 32) {
         g.kind = mrn::kQ8Blocks;
         g.lanes = 0;
-        if ((dt == MRN_F32 || nblocks >= 128) && nblocks <= max_staged) {
+        if ((dt == MRN_F32 || nblocks >= 64) && nblocks <= max_staged) {
             g.k = nblocks >= 128 ? 2 : 1;
             const int per = static_cast<int>(ceil_div(ceil_div(nblocks, g.k), 32) * 32);
             for (int groups = 2; groups >= 1; --groups) {

@@ -458,11 +458,12 @@ def f16_ulps(a_bits, b_bits):
     return np.abs(ordered(a_bits) - ordered(b_bits))
 
 
-def parity_q8_1(x, gamma, eps, dtype, rows_sample=None, what="q8_1", x_offset=0):
+def parity_q8_1(x, gamma, eps, dtype, rows_sample=None, what="q8_1", x_offset=0, y_offset=0):
     """RMSNorm + Q8_1 against the oracle: header s == 0, d within one f16 ulp
     of the oracle's d, codes equal except within Q8_TIE_MARGIN of a tie (one
     off allowed there: the GPU's f32 norm may land on the other side of a
-    tie), zero blocks exactly zero.  64-byte guard bands around the blocks."""
+    tie), zero blocks exactly zero.  64-byte guard bands around the blocks,
+    which start y_offset bytes past a 16-byte boundary."""
     rows, n = x.shape
     if x_offset:
         base = to_device(np.concatenate([np.zeros(x_offset, x.dtype), x.ravel()]), dtype)
@@ -472,15 +473,18 @@ def parity_q8_1(x, gamma, eps, dtype, rows_sample=None, what="q8_1", x_offset=0)
     dg = to_device(gamma, dtype)
     nb = n // 32
     guard = 64
-    raw = torch.full((rows * nb * 36 + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
-    blocks = raw[guard:guard + rows * nb * 36]
+    raw = torch.full((rows * nb * 36 + 2 * guard + y_offset,), 0xA5, dtype=torch.uint8,
+                     device="cuda")
+    lo = guard + y_offset
+    blocks = raw[lo:lo + rows * nb * 36]
+    assert blocks.data_ptr() % 16 == y_offset % 16
     st = mrn.mrn_rmsnorm_q8_1(dx.data_ptr(), dg.data_ptr(), blocks.data_ptr(), rows, n, eps,
                               code(dtype), stream_handle())
     assert st == 0, f"{what}: status {mrn.STATUS.get(st)}"
     torch.cuda.synchronize()
     host = raw.cpu().numpy()
-    assert np.all(host[:guard] == 0xA5) and np.all(host[-guard:] == 0xA5), what + ": guard bands"
-    return check_q8_1_blocks(host[guard:-guard], x, gamma, eps, dtype, rows_sample, what)
+    assert np.all(host[:lo] == 0xA5) and np.all(host[-guard:] == 0xA5), what + ": guard bands"
+    return check_q8_1_blocks(host[lo:-guard], x, gamma, eps, dtype, rows_sample, what)
 
 
 def check_q8_1_blocks(host_blocks, x, gamma, eps, dtype, rows_sample=None, what="q8_1"):

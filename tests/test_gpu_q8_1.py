@@ -120,6 +120,18 @@ def test_unaligned_rows_and_wide_rows(dtype):
     gu.parity_q8_1(d["x"], d["gamma"], 1e-6, dtype, what="q8 wide")
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("y_offset", [4, 8, 12])
+def test_staged_blocks_at_unaligned_output(dtype, y_offset):
+    """Blocks written from 4 (8, 12) bytes past a 16-byte boundary: the staged
+    kernel copies such rows out word by word rather than by one bulk copy."""
+    rows, n = 300, 4096
+    assert mrn.mrn_query_geometry(5, rows, n, gu.code(dtype), True)["stages"] > 0
+    d = wl.random_rows(46 + y_offset, rows, n, dtype)
+    gu.parity_q8_1(d["x"], d["gamma"], 1e-6, dtype, what=f"q8 output +{y_offset}",
+                   y_offset=y_offset)
+
+
 def test_tensor_api_layout():
     d = wl.random_rows(45, 4, 128, "f32")
     x, g = gu.to_device(d["x"], "f32"), gu.to_device(d["gamma"], "f32")
