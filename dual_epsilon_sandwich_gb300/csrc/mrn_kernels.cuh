@@ -849,6 +849,26 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
 }
+// Raise the barrier's expected transaction bytes without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+// 4 bytes global -> shared without staging them in registers (cp.async; the
+// thread does not wait for them).
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_addr(dst)), "l"(src)
+                 : "memory");
+}
+// Arrive on the barrier once this thread's cp.async copies so far have landed
+// (one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_addr(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t done;
     asm volatile("{\n\t.reg .pred p;\n\t"
@@ -1113,8 +1133,10 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
     }
 
     // EDGE: every thread places part of the gammas and arrives on the gamma
-    // barrier once (thread 0 with its expect_tx arrive), so the gammas complete
-    // that barrier as a bulk copy does and are awaited at the same point.
+    // barrier once, so the gammas complete that barrier as a bulk copy does and
+    // are awaited at the same point.  f32: each element by a 4-byte cp.async,
+    // the thread's arrival made when its copies have landed (the threads go on
+    // to their first rows at once); bf16: loaded and stored by the threads.
     const bool gamma_by_threads = EDGE && NG > 0;
     if (tid == 0) {
         for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
@@ -1124,8 +1146,13 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
         fence_mbar_init();
     }
     if (gamma_by_threads && my_rows > 0) {
-        for (uint32_t i = tid; i < NG * sb / 4u; i += blockDim.x)
-            reinterpret_cast<uint32_t *>(gsm)[i] = 0u;
+        // the bytes of each gamma slot's first and last granule outside gamma
+        // must read as zero (the masked edge elements multiply them)
+        const uint32_t last = span - 16u;
+        for (uint32_t i = tid; i < NG * 8u; i += blockDim.x) {
+            const uint32_t q = i >> 3, w = i & 7u;
+            reinterpret_cast<uint32_t *>(gsm + q * sb + (w < 4u ? 0u : last))[w & 3u] = 0u;
+        }
     }
     __syncthreads();
     pdl_enter();   // (the shared-memory set-up above overlapped the previous grid)
@@ -1146,8 +1173,18 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
             if (NG == 2) bulk_to_shared(gsm + rb, a.g2, rb, &bars[stages]);
         }
     }
-    if (gamma_by_threads && my_rows > 0) {
-        // gamma element j to byte mis + j * s of its (zeroed) slot, while the
+    if (T::kBytes == 4 && gamma_by_threads && my_rows > 0) {
+        // gamma element j to byte mis + 4 j of its slot
+        if (tid == 0) mbar_expect_tx(&bars[stages], a.stall_bytes);   // (test hook: 0 in use)
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+            const char *src = static_cast<const char *>(q == 0 ? a.g1 : a.g2);
+            unsigned char *dst = gsm + q * sb + mis;
+            for (int64_t j = tid; j < a.n; j += blockDim.x) cp_async_4(dst + 4 * j, src + 4 * j);
+        }
+        cp_async_arrive(&bars[stages]);
+    } else if (gamma_by_threads && my_rows > 0) {
+        // gamma element j to byte mis + j * s of its slot, while the
         // first rows' copies are in flight: each thread reads whole 16-byte
         // granules of gamma (the same over-read as for the rows), all its
         // loads first, and places the elements that belong to gamma
@@ -1422,7 +1459,8 @@ mrn_tma_kernel(const KernelArgs a, const int stages) {
 
     // Exit: with no failure every issued copy was consumed.  After a failure,
     // wait (bounded) for the copies still in flight so that none lands after
-    // the CTA has left its shared memory.
+    // the CTA has left its shared memory (each thread its own cp.async first).
+    if (EDGE && T::kBytes == 4) cp_async_wait_all();
     __syncthreads();
     if (tid == 0 && my_rows > 0 && abort_flag) {
         atomicAdd(&g_wait_timeouts, 1u);
