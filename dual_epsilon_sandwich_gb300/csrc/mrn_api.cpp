@@ -117,6 +117,41 @@ void pick_threads_batch(int64_t per, int *k_out, int *t_out, double target) {
     if (best > 1e29) pick_threads(per, k_out, t_out);
 }
 
+// Batches (rows >= #SMs, aligned rows of at most 2048 loads) that run faster
+// in the register kernel -- one row per CTA, many CTAs per SM, no persistent
+// grid to drain -- than in the staged one.  From sweeps on GB300 (CUDA events,
+// back to back; register vs staged or rows-per-warp, TB/s):
+//  * always: the residual add + norm and the Q8_1 pass (they store or compute
+//    more per byte); the f32 sandwich from 2048 rows (one reduction per row);
+//  * rows of at most 512 loads, any batch: 16384 x 4096 bf16 plain 6.47 vs
+//    6.16, then-add 6.90 vs 6.47, sandwich 6.30 vs 6.03; 65536 x 2048 f32
+//    plain 7.04 vs 6.57, then-add 7.12 vs 6.73; 1216 x 4096 bf16 then-add
+//    6.22 vs 5.28; rows of 129..256 loads too, against rows per warp (65536 x
+//    2048 bf16: plain 6.81 vs 6.32, then-add 7.02 vs 5.02, sandwich 6.76 vs 5.30);
+//  * wider rows from 2048 rows: then-add up to 1664 loads (16384 x 8192 bf16
+//    7.01 vs 6.51, 65536 x 6656 f32 6.95 vs 6.84; at 2048 loads staged, 6.86
+//    vs 6.11), then-add-scale the same in bf16 but up to 1280 loads in f32
+//    (at 1664, 4096 x 6656: 58.8 us against 50.8 for the staged then-add);
+//    plain and the f32 seam up to 1280 loads in f32 (65536 x 5120 6.88 vs
+//    6.08) and 896 in bf16 (4096 x 6656 5.45 vs 4.21); the bf16 seam from 4096
+//    rows up to 896 loads (16384 x 4096 6.57 vs 6.20).  The bf16 sandwich
+//    keeps the staged kernel past 512 loads (4096 x 8192: 4.71 vs 6.01).
+bool register_batch_pays(mrn::Op op, mrn_dtype dt, int64_t nvec, int64_t rows) {
+    if (op == mrn::kAddRmsnorm || op == mrn::kRmsnormQ8) return true;
+    if (op == mrn::kSandwich && dt == MRN_F32 && rows >= 2048) return true;
+    if (nvec > 2048) return false;
+    const bool f32 = dt == MRN_F32;
+    if (mrn::op_is_seam(op)) {
+        if (f32) return nvec <= 1280 && (nvec <= 512 || rows >= 2048);
+        return nvec <= 896 && rows >= 4096;
+    }
+    if (nvec <= 512) return true;
+    if (rows < 2048 || op == mrn::kSandwich) return false;
+    if (op == mrn::kThenAdd) return nvec <= 1664;
+    if (op == mrn::kThenAddScale) return nvec <= (f32 ? 1280 : 1664);
+    return nvec <= (f32 ? 1280 : 896);
+}
+
 // Dynamic shared memory the staged kernel may use (the rest of the 227 KB
 // holds its static reduction slots and barriers).
 constexpr int64_t kTmaSharedBudget = mrn::kSharedBytesPerCta - 1024;
@@ -211,7 +246,8 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
         g.vec = natural_vec(dt);
         g.cluster = 1;
     }
-    if (nvec <= 32 * mrn::kMaxK) {
+    const bool register_batch = aligned16 && rows >= sms && register_batch_pays(op, dt, nvec, rows);
+    if (nvec <= 32 * mrn::kMaxK && !(register_batch && nvec > 128)) {
         // About four loads per thread (measured on GB300: per-head n = 128 rows
         // run ~15% faster with 4 slots x 4..8 lanes than with 1 slot x 16..32).
         g.kind = mrn::kRowsPerWarp;
@@ -243,9 +279,7 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     // vs 337.5; but 1216 x 6656 23.9 vs 22.8 (a fit over rows: 15.1 ns per row +
     // 5.3 us against 16.4 ns + 2.6 us: equal at about 2060 rows).
     const bool one_exchange_sandwich = op == mrn::kSandwich && dt == MRN_F32;
-    const bool staged_pays = op != mrn::kAddRmsnorm && op != mrn::kRmsnormQ8 &&
-                             !(one_exchange_sandwich && rows >= 2048);
-    if (staged_pays && aligned16 && rows >= sms && nvec <= 2 * 1024) {
+    if (!register_batch && aligned16 && rows >= sms && nvec <= 2 * 1024) {
         // The seam from f32 rows reads twice the bytes it writes; a second
         // stage per group keeps more of those reads in flight (measured on
         // GB300, 4096 rows: 5.56 vs 4.75 TB/s at n = 6656, 5.45 vs 5.22 at
@@ -345,9 +379,15 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
             pow2_floor(std::max<int64_t>(1, nvec / (one_exchange_sandwich ? 96 : 192)));
         cl = std::max(cl, std::min(cap, std::min(by_rows, by_width)));
     }
-    if (!staged_pays && rows >= sms) {
-        pick_threads_batch(ceil_div(nvec, cl), &g.k, &g.threads,
-                           op == mrn::kRmsnormQ8 ? 128.0 : 256.0);
+    if (register_batch) {
+        // about four register slots per thread (two for the bf16 sandwich, whose
+        // slots hold more), 64..256 threads; 256 for the residual add + norm,
+        // 128 for the Q8_1 pass (measured best)
+        double target = std::min(256.0, std::max(64.0, static_cast<double>(nvec) /
+                                     (op == mrn::kSandwich && dt == MRN_BF16 ? 2.0 : 4.0)));
+        if (op == mrn::kAddRmsnorm) target = 256.0;
+        if (op == mrn::kRmsnormQ8) target = 128.0;
+        pick_threads_batch(ceil_div(nvec, cl), &g.k, &g.threads, target);
     } else {
         pick_threads(ceil_div(nvec, cl), &g.k, &g.threads);
     }

@@ -184,8 +184,10 @@ def test_seam_geometry():
     for op in (mrn.MRN_OP_RMSNORM_SEAM, mrn.MRN_OP_RMSNORM_UNWEIGHTED):
         got = mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True, 152)
         assert (got["kind"], got["stages"], got["groups"]) == (4, 4, 2)
-        got = mrn.mrn_query_geometry(op, 16384, 4096, mrn.MRN_BF16, True, 152)
+        got = mrn.mrn_query_geometry(op, 2048, 4096, mrn.MRN_BF16, True, 152)
         assert (got["kind"], got["stages"], got["groups"]) == (4, 2, 2)
+        got = mrn.mrn_query_geometry(op, 16384, 4096, mrn.MRN_BF16, True, 152)
+        assert (got["kind"], got["threads"], got["k"]) == (2, 128, 4)   # register batch
         assert mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, False, 152)["kind"] == 2
         assert mrn.mrn_query_geometry(op, 4096, 128, mrn.MRN_BF16, True, 152)["kind"] == 1
         # staged: one row operand per stage, no gamma in shared memory (read through L1)
@@ -195,6 +197,46 @@ def test_seam_geometry():
         assert mrn.mrn_force_geometry(None) == 0
     with pytest.raises(mrn.MrnError):
         mrn.mrn_query_geometry(8, 4, 64, mrn.MRN_F32, True, 152)
+
+
+# (op, rows, n, dtype) -> (kind, threads, k) of the automatic choice for batches:
+# the register kernel where the sweeps measured it faster, else the staged
+# kernel (kind 4) or rows per warp (kind 1); threads and k only for kind 2.
+BATCH_CHOICES = [
+    (mrn.MRN_OP_RMSNORM, 16384, 4096, mrn.MRN_BF16, (2, 128, 4)),
+    (mrn.MRN_OP_THEN_ADD, 16384, 4096, mrn.MRN_BF16, (2, 128, 4)),
+    (mrn.MRN_OP_THEN_ADD_SCALE, 16384, 4096, mrn.MRN_BF16, (2, 128, 4)),
+    (mrn.MRN_OP_SANDWICH, 16384, 4096, mrn.MRN_BF16, (2, 256, 2)),
+    (mrn.MRN_OP_SANDWICH, 4096, 8192, mrn.MRN_BF16, (4,)),
+    (mrn.MRN_OP_SANDWICH, 4096, 6656, mrn.MRN_F32, (2, 256, 7)),
+    (mrn.MRN_OP_SANDWICH, 1216, 6656, mrn.MRN_F32, (4,)),
+    (mrn.MRN_OP_SANDWICH, 1216, 2048, mrn.MRN_F32, (2, 128, 4)),
+    (mrn.MRN_OP_RMSNORM, 65536, 2048, mrn.MRN_BF16, (2, 64, 4)),    # was rows per warp
+    (mrn.MRN_OP_THEN_ADD, 65536, 2048, mrn.MRN_BF16, (2, 64, 4)),
+    (mrn.MRN_OP_RMSNORM, 65536, 512, mrn.MRN_F32, (1,)),            # 128 loads: rows per warp
+    (mrn.MRN_OP_RMSNORM, 163840, 128, mrn.MRN_BF16, (1,)),          # per-head QK-norm
+    (mrn.MRN_OP_RMSNORM, 4096, 6656, mrn.MRN_F32, (4,)),
+    (mrn.MRN_OP_THEN_ADD, 4096, 6656, mrn.MRN_F32, (2, 256, 7)),
+    (mrn.MRN_OP_THEN_ADD, 65536, 8192, mrn.MRN_F32, (4,)),
+    (mrn.MRN_OP_THEN_ADD_SCALE, 4096, 6656, mrn.MRN_F32, (4,)),
+    (mrn.MRN_OP_THEN_ADD_SCALE, 65536, 5120, mrn.MRN_F32, (2, 256, 5)),
+    (mrn.MRN_OP_THEN_ADD_SCALE, 4096, 6656, mrn.MRN_BF16, (2, 224, 4)),
+    (mrn.MRN_OP_RMSNORM, 65536, 5120, mrn.MRN_F32, (2, 256, 5)),
+    (mrn.MRN_OP_RMSNORM, 1216, 4096, mrn.MRN_F32, (4,)),            # rows < 2048, 1024 loads
+    (mrn.MRN_OP_RMSNORM, 1216, 2048, mrn.MRN_F32, (2, 128, 4)),
+    (mrn.MRN_OP_RMSNORM, 4096, 6656, mrn.MRN_BF16, (2, 224, 4)),
+    (mrn.MRN_OP_RMSNORM, 16384, 8192, mrn.MRN_BF16, (4,)),
+    (mrn.MRN_OP_THEN_ADD, 16384, 8192, mrn.MRN_BF16, (2, 256, 4)),
+    (mrn.MRN_OP_ADD_RMSNORM, 4096, 6656, mrn.MRN_F32, (2, 256, 7)),
+    (mrn.MRN_OP_RMSNORM, 100, 4096, mrn.MRN_BF16, (2,)),            # fewer rows than SMs
+]
+
+
+@pytest.mark.parametrize("op,rows,n,dt,want", BATCH_CHOICES,
+                         ids=[f"{c[0]}-{c[1]}x{c[2]}-{c[3]}" for c in BATCH_CHOICES])
+def test_register_batch_choice(op, rows, n, dt, want):
+    got = mrn.mrn_query_geometry(op, rows, n, dt, True, 152)
+    assert (got["kind"], got["threads"], got["k"])[:len(want)] == want, got
 
 
 def test_size_validation():

@@ -351,17 +351,26 @@ def test_forced_staged_kernel(geom, nvec, rows, dtype):
     assert mrn.mrn_wait_timeouts() == 0
 
 
-def test_staged_kernel_is_the_automatic_choice_for_batches():
-    """Batches of aligned rows run staged, except the f32 sandwich, whose single
-    reduction per row (the one-exchange form) makes the register kernel faster."""
+def test_batch_kernel_choice_and_both_kernels():
+    """Batches of aligned rows take the register kernel where it measured faster
+    (the f32 sandwich and then-add at n = 6656 from 2048 rows, every operation
+    at 512 loads per row) and the staged kernel elsewhere (plain f32 at 6656);
+    the same 2048 x 6656 batch through the automatic choice and through the
+    staged kernel forced, every operation against the oracle."""
+    assert [mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True)["kind"]
+            for op in (0, 1, 2)] == [mrn.MRN_GEOM_TMA, mrn.MRN_GEOM_CTA, mrn.MRN_GEOM_CTA]
     for op in (0, 1, 2):
-        want = mrn.MRN_GEOM_CTA if op == 2 else mrn.MRN_GEOM_TMA
-        assert mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True)["kind"] == want
         assert mrn.mrn_query_geometry(op, 16384, 4096, mrn.MRN_BF16, True)["kind"] == \
-            mrn.MRN_GEOM_TMA
+            mrn.MRN_GEOM_CTA
     assert mrn.mrn_query_geometry(2, 1, 6656, mrn.MRN_F32, True)["kind"] == mrn.MRN_GEOM_CTA
     d = rows_data(14, 2048, 6656, "f32")
-    all_ops(d, "f32", "auto staged 2048x6656")
+    all_ops(d, "f32", "auto 2048x6656")
+    assert mrn.mrn_force_geometry({"kind": 4, "k": 4, "threads": 832, "stages": 2,
+                                   "groups": 2}) == 0
+    try:
+        all_ops(d, "f32", "staged 2048x6656")
+    finally:
+        mrn.mrn_force_geometry(None)
     assert mrn.mrn_wait_timeouts() == 0
 
 

@@ -38,11 +38,13 @@ def test_shapes(n, dtype):
 
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_batches(dtype):
-    """Batch shapes in the automatic geometry (register kernel for add+norm,
-    staged kernel for then-add-scale) and add+norm forced into the staged one."""
+    """Batch shapes in the automatic geometry (the register kernel, except the
+    f32 then-add-scale at 1664 loads per row, which stays staged) and both
+    operations forced into the staged kernel."""
     for rows, n in ((4096, 6656), (2048, 4096)):
         assert mrn.mrn_query_geometry(3, rows, n, gu.code(dtype), True)["kind"] == mrn.MRN_GEOM_CTA
-        assert mrn.mrn_query_geometry(4, rows, n, gu.code(dtype), True)["kind"] == mrn.MRN_GEOM_TMA
+        want = mrn.MRN_GEOM_TMA if (dtype, n) == ("f32", 6656) else mrn.MRN_GEOM_CTA
+        assert mrn.mrn_query_geometry(4, rows, n, gu.code(dtype), True)["kind"] == want
         d = wl.random_rows(rows + n, rows, n, dtype)
         sample = gu.sample_rows(rows, 128, seed=n)
         both(d, dtype, f"batch {rows}x{n}", sample=sample)
@@ -50,9 +52,10 @@ def test_batches(dtype):
         k = -(-nvec // 416)
         assert mrn.mrn_force_geometry({"kind": 4, "k": k, "threads": 832, "stages": 2,
                                        "groups": 2}) == 0
-        gu.parity_add_rmsnorm(d["x"], d["residual"], d["gamma"], 1e-5, dtype, sample,
-                              what=f"staged add_rmsnorm {rows}x{n}")
-        mrn.mrn_force_geometry(None)
+        try:
+            both(d, dtype, f"staged {rows}x{n}", sample=sample)
+        finally:
+            mrn.mrn_force_geometry(None)
 
 
 GEOMS = [

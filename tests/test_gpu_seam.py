@@ -35,9 +35,11 @@ def test_widths(n, dtype, seam):
 
 @pytest.mark.parametrize("seam", SEAMS)
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_batch(dtype, seam):
-    """Many rows (the persistent staged kernel), rows of very different scales
-    and a few zero rows."""
+@pytest.mark.parametrize("kernel", ["auto", "staged"])
+def test_batch(dtype, seam, kernel):
+    """Many rows (the register kernel by the automatic choice at this width, and
+    the persistent staged kernel forced), rows of very different scales and a
+    few zero rows."""
     rows, n = 4096, 2560
     g = np.random.Generator(np.random.PCG64(61))
     x = g.standard_normal((rows, n)) * 10.0 ** g.uniform(-3, 3, size=(rows, 1))
@@ -45,9 +47,17 @@ def test_batch(dtype, seam):
     x = wl.to_f32(x) if dtype == "f32" else wl.to_bf16_bits(x)
     gamma = wl.to_seam_bits(1.0 + 0.1 * g.standard_normal(n), seam)
     assert mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM_SEAM, rows, n, gu.code(dtype), True)["kind"] \
-        == mrn.MRN_GEOM_TMA
-    flips, near = gu.parity_seam(x, gamma, 1e-6, dtype, seam, what=f"seam batch {dtype}/{seam}")
-    print(f"seam {dtype}->{seam}: {flips} of {near} near-tie elements took the other side")
+        == mrn.MRN_GEOM_CTA
+    if kernel == "staged":
+        per_group = -(-(n // (4 if dtype == "f32" else 8) // 4) // 32) * 32
+        assert mrn.mrn_force_geometry({"kind": 4, "k": 4, "threads": 2 * per_group, "stages": 2,
+                                       "groups": 2}) == 0
+    try:
+        flips, near = gu.parity_seam(x, gamma, 1e-6, dtype, seam,
+                                     what=f"seam batch {dtype}/{seam} {kernel}")
+    finally:
+        mrn.mrn_force_geometry(None)
+    print(f"seam {dtype}->{seam} {kernel}: {flips} of {near} near-tie elements took the other side")
 
 
 GEOMS = [
