@@ -249,10 +249,15 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
     const bool register_batch = aligned16 && rows >= sms && register_batch_pays(op, dt, nvec, rows);
     if (nvec <= 32 * mrn::kMaxK && !(register_batch && nvec > 128)) {
         // About four loads per thread (measured on GB300: per-head n = 128 rows
-        // run ~15% faster with 4 slots x 4..8 lanes than with 1 slot x 16..32).
+        // run ~15% faster with 4 slots x 4..8 lanes than with 1 slot x 16..32),
+        // at least 4 lanes from 8 loads (163840 x 64 bf16: 4 x 2 7.0 us, 2 x 4
+        // 8.1 us), in CTAs of 128 threads (163840 x 128 bf16: 13.8 us against
+        // 14.6 us with 256; 655360 rows 49.0 vs 52.3 us: smaller CTAs drain
+        // the grid's tail sooner).
         g.kind = mrn::kRowsPerWarp;
-        g.threads = mrn::kWarpKernelThreads;
+        g.threads = mrn::kWarpKernelCtaThreads;
         g.lanes = static_cast<int>(std::min<int64_t>(32, pow2_ceil(ceil_div(nvec, 4))));
+        if (nvec >= 8 && g.lanes < 4) g.lanes = 4;
         if (op == mrn::kRmsnormQ8)   // a Q8_1 block must sit on consecutive lanes
             g.lanes = std::max(g.lanes, mrn::kQ8Block / g.vec);
         g.k = static_cast<int>(ceil_div(nvec, g.lanes));
@@ -403,7 +408,8 @@ bool geometry_is_consistent(const Geometry &g) {
     if (g.edge && (g.kind != mrn::kTma || g.groups != 2 || g.cluster != 1)) return false;
     if (g.kind == mrn::kRowsPerWarp) {
         const bool pow2 = g.lanes >= 1 && g.lanes <= 32 && (g.lanes & (g.lanes - 1)) == 0;
-        return pow2 && g.k >= 1 && g.k <= mrn::kMaxK && g.threads == mrn::kWarpKernelThreads;
+        return pow2 && g.k >= 1 && g.k <= mrn::kMaxK && g.threads >= 32 && g.threads % 32 == 0 &&
+               g.threads <= mrn::kWarpKernelThreads;
     }
     if (g.kind == mrn::kCta) {
         return g.k >= 1 && g.k <= mrn::kMaxK && g.threads >= 32 && g.threads % 32 == 0 &&

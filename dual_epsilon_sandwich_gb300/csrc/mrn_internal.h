@@ -95,7 +95,8 @@ struct Geometry {
 // Register-slot limits per thread count: the kernels are compiled with these
 // launch bounds so that every (k, threads <= max) pair can launch.
 constexpr int kMaxK = 8;
-constexpr int kWarpKernelThreads = 256;
+constexpr int kWarpKernelThreads = 256;     // rows-per-warp kernel: at most (launch bounds)
+constexpr int kWarpKernelCtaThreads = 128;  // ... and the automatic choice
 constexpr int kStreamMaxThreads = 512;
 constexpr int kMaxCluster = 16;
 constexpr int kTmaMaxStages = 8;

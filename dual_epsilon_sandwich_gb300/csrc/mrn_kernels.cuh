@@ -803,7 +803,7 @@ __device__ __forceinline__ void row_body(const KernelArgs &a, int64_t row, bool 
 }
 
 // Several rows per warp: `lanes` (power of two <= 32) threads per row, K
-// register slots each; 256 threads per CTA.
+// register slots each; up to 256 threads per CTA (128 by the automatic choice).
 template <int OP, class T, int VEC, int K>
 __global__ void __launch_bounds__(kWarpKernelThreads)
 mrn_rows_per_warp_kernel(const KernelArgs a, const int lanes) {

@@ -256,7 +256,8 @@ typedef enum mrn_op {
 typedef enum mrn_geometry_kind {
     MRN_GEOM_AUTO = 0,          /* (for mrn_force_geometry) let the library choose */
     MRN_GEOM_ROWS_PER_WARP = 1, /* lanes_per_row (1..32) lanes per row, several rows
-                                   per CTA, shuffle-only reduction */
+                                   per CTA of `threads` (a multiple of 32 up to 256;
+                                   0 when forced: 256), shuffle-only reduction */
     MRN_GEOM_CTA = 2,           /* one row per CTA, or per thread-block cluster of
                                    `cluster` CTAs whose partial sums travel as
                                    st.async messages to the peers' shared memory;

@@ -327,7 +327,7 @@ def test_geometry_covers_every_row_width():
                             assert g["lanes_per_row"] * g["k"] >= nvec
                             if op == 5:
                                 assert g["lanes_per_row"] >= 32 // vec
-                            assert g["threads"] == 256 and 32 % g["lanes_per_row"] == 0
+                            assert g["threads"] == 128 and 32 % g["lanes_per_row"] == 0
                         elif g["kind"] == mrn.MRN_GEOM_CTA:
                             assert g["cluster"] * g["threads"] * g["k"] >= nvec
                             assert g["threads"] % 32 == 0 and 1 <= g["cluster"] <= 16
