@@ -1904,10 +1904,15 @@ __device__ __forceinline__ void sandwich_one_exchange(const KernelArgs &a, int64
                                                       Reduce4 reduce4, Reduce2 reduce2,
                                                       bool *second) {
     using Fr = Frag<T, VEC>;
+    // With few slots per thread (decode) gamma_pre is loaded with everything
+    // else, so that no load waits behind the exchange; with many (batches)
+    // it reuses gamma_post's registers after the stream is formed.
+    constexpr bool kEarlyG2 = K <= 2;
     const int64_t row_elem = row * a.n;
     Fr xv[K];
     Fr rv[K];
     Fr gv[K];
+    Fr g2v[kEarlyG2 ? K : 1];
     bool ok[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -1926,6 +1931,7 @@ __device__ __forceinline__ void sandwich_one_exchange(const KernelArgs &a, int64
     for (int k = 0; k < K; ++k) {
         if (ok[k]) {
             ld_ro(gv[k], elem_ptr<T>(a.g1, (first + k * stride) * VEC));
+            if constexpr (kEarlyG2) ld_ro(g2v[k], elem_ptr<T>(a.g2, (first + k * stride) * VEC));
         } else {
             gv[k].zero();
         }
@@ -1957,9 +1963,11 @@ __device__ __forceinline__ void sandwich_one_exchange(const KernelArgs &a, int64
         st_global(elem_ptr<T>(a.y, row_elem + v * VEC), rv[k]);
         if (direct) ss2 += frag_sum_sq(rv[k]);
     }
+    if constexpr (!kEarlyG2) {
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-        if (ok[k]) ld_ro(gv[k], elem_ptr<T>(a.g2, (first + k * stride) * VEC));
+        for (int k = 0; k < K; ++k) {
+            if (ok[k]) ld_ro(gv[k], elem_ptr<T>(a.g2, (first + k * stride) * VEC));
+        }
     }
     *second = direct;
     const float inv2 = inv_rms(direct ? reduce2(ss2) : est, a.n, a.eps2);
@@ -1967,7 +1975,8 @@ __device__ __forceinline__ void sandwich_one_exchange(const KernelArgs &a, int64
     for (int k = 0; k < K; ++k) {
         if (!ok[k]) continue;
         const int64_t v = first + k * stride;
-        st_global(elem_ptr<T>(a.y2, row_elem + v * VEC), apply_norm(rv[k], inv2, gv[k]));
+        st_global(elem_ptr<T>(a.y2, row_elem + v * VEC),
+                  apply_norm(rv[k], inv2, kEarlyG2 ? g2v[kEarlyG2 ? k : 0] : gv[k]));
     }
 }
 
