@@ -831,7 +831,7 @@ def secondary_workloads(dev, stream):
 
 
 def more_ops(dev, stream):
-    """The operations beyond the three of the benchmark spec, timed the same way
+    """The operations beyond plain RMSNorm, then-add and the sandwich, timed the same way
     (GB/s of algorithmic bytes, two rotating buffer sets larger than L2,
     seeded torch inputs): residual add + norm at the benchmark's width, the
     sandwich and plain RMSNorm at one element less (rows not 16-byte aligned),

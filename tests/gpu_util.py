@@ -245,7 +245,7 @@ def sandwich_normed_scale(want_s, stream_err, gq, eps_pre):
     return inv2 * np.abs(gq) * (stream_err + np.abs(want_s) * rel)
 
 
-# Strict gate on `normed`: the north star's plain "<= 1e-5 relative" (f32) or
+# Strict gate on `normed`: the stated plain "<= 1e-5 relative" (f32) or
 # "<= 1 bf16 ulp" (bf16), asserted on every element whose problem is well
 # conditioned.  The condition number of normed_j with respect to the stream,
 # kappa_j = carried_j / (1e-5 |o_j|) with `carried` the stream's 1e-5-of-the-
