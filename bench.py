@@ -631,6 +631,10 @@ def workload_summary(line: dict, peak: float) -> dict:
     out["5_sweep_f32_GB_per_s_rmsnorm_then_add"] = {
         shape: [r(e.get("rmsnorm", {}).get("GB_per_s"), 0), r(e.get("then_add", {}).get("GB_per_s"), 0)]
         for shape, e in sweep.items()} or None
+    small = sec.get("sweep_small_f32_us_per_call_graph") or {}
+    out["5_sweep_small_f32_us_per_call_graph_rmsnorm_then_add"] = {
+        shape: [r(e.get("rmsnorm"), 2), r(e.get("then_add"), 2)]
+        for shape, e in small.items()} or None
     nxt = {}
     for name in ("add_rmsnorm_f32_rows4096_n6656", "then_add_scale_bf16_rows16384_n4096",
                  "rmsnorm_q8_1_bf16_rows16384_n4096", "qk_norm_bf16_rows163840_n128",
@@ -745,10 +749,11 @@ def decode_latency(args, dev, stream):
 
 
 def secondary_workloads(dev, stream):
-    """The other two measured workloads: Llama-style bf16 plain RMSNorm and
-    then-add at 16384 x 4096 (GB/s, two rotating buffer sets of >= 268 MB), and
+    """The other measured workloads: Llama-style bf16 plain RMSNorm and
+    then-add at 16384 x 4096 (GB/s, two rotating buffer sets of >= 268 MB),
     plain f32 RMSNorm at 4 x 6656 (us/call in a CUDA graph over 512 rotating
-    buffer sets, 122 MB > L2)."""
+    buffer sets, 122 MB > L2), the sweep's shapes (GB/s from rows x n >= 2^26,
+    us/call in a CUDA graph below), and the operations beyond the base three."""
     import torch
 
     from dual_epsilon_sandwich_gb300 import mrn
@@ -796,6 +801,7 @@ def secondary_workloads(dev, stream):
     out.update(more_ops(dev, stream))
     out.update(seam_ops(dev, stream))
     out["sweep_large_f32"] = sweep_large(dev, stream)
+    out["sweep_small_f32_us_per_call_graph"] = sweep_small(dev, stream)
 
     w = wl.plain_decode_rows()
     nsets = 512
@@ -1055,6 +1061,68 @@ def sweep_large(dev, stream):
                                                    True)
         out[f"rows{rows}_n{n}"] = entry
         del x, r, y
+        torch.cuda.empty_cache()
+    return out
+
+
+def sweep_small(dev, stream):
+    """The sweep workload's shapes with rows x n < 2^26 (f32, plain and
+    then-add, eps 1e-5): us per call in a CUDA graph over rotating buffer sets
+    (at least 300 MB in all where at most 512 sets reach it; the smallest
+    shapes stay L2-resident), seeded device-side random inputs."""
+    import torch
+
+    from dual_epsilon_sandwich_gb300 import mrn
+    from dual_epsilon_sandwich_gb300 import workloads as wl
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(20261206)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    side = torch.cuda.Stream()
+    out = {}
+    for n, rows in wl.sweep_shapes():
+        if rows * n >= 2 ** 26:
+            continue
+        per_set = 3 * rows * n * 4
+        sets = max(2, min(512, -(-300 * 2 ** 20 // per_set)))
+        calls = max(sets, 64)
+        x = torch.randn(sets, rows, n, device=dev, generator=gen)
+        r = torch.randn(sets, rows, n, device=dev, generator=gen)
+        g = 1 + 0.1 * torch.randn(n, device=dev, generator=gen)
+        y = torch.empty_like(x)
+        entry = {}
+        for op in ("rmsnorm", "then_add"):
+            def call(i, handle):
+                j = i % sets
+                if op == "rmsnorm":
+                    st = mrn.mrn_rmsnorm(x[j].data_ptr(), g.data_ptr(), y[j].data_ptr(), rows, n,
+                                         1e-5, mrn.MRN_F32, handle)
+                else:
+                    st = mrn.mrn_rmsnorm_then_add(x[j].data_ptr(), g.data_ptr(), r[j].data_ptr(),
+                                                  y[j].data_ptr(), rows, n, 1e-5, mrn.MRN_F32,
+                                                  handle)
+                if st != 0:
+                    raise mrn.MrnError(st, f"sweep {rows}x{n} {op}")
+            side.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                for i in range(4):
+                    call(i, side.cuda_stream)
+                with torch.cuda.graph(graph, stream=side):
+                    for i in range(calls):
+                        call(i, side.cuda_stream)
+            stream.wait_stream(side)
+            graph.replay()
+            torch.cuda.synchronize()
+            reps = 3
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            entry[op] = e0.elapsed_time(e1) * 1e3 / (reps * calls)
+        entry["sets"] = sets
+        out[f"{rows}x{n}"] = entry
+        del x, r, y, graph
         torch.cuda.empty_cache()
     return out
 
