@@ -315,11 +315,13 @@ def test_geometry_covers_every_row_width():
                             assert vec == 16 // e and rows >= 152 and n > 256
                             gran = (n * e + 15) // 16 + 1
                             assert g["threads"] // 2 * g["k"] >= gran and g["cluster"] == 1
-                            assert g["threads"] // 2 % 32 == 0 and g["stages"] == 2
+                            assert g["threads"] // 2 % 32 == 0
                             stage = gran * 16
+                            four = (op, e) == (0, 4) and stage * 5 <= 232448 - 1024
+                            assert g["stages"] == (4 if four else 2)
                             ng = 2 if op == 2 else 1
                             nin = 1 if op == 0 else 2
-                            assert stage * (ng + 2 * nin) <= 232448 - 1024
+                            assert stage * (ng + g["stages"] * nin) <= 232448 - 1024
                             continue
                         assert vec == (16 // e if a16 and (n * e) % 16 == 0 else 1)
                         nvec = -(-n // vec)
