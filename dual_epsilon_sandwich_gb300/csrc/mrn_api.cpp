@@ -128,6 +128,9 @@ void pick_threads_batch(int64_t per, int *k_out, int *t_out, double target) {
 //    plain 7.04 vs 6.57, then-add 7.12 vs 6.73; 1216 x 4096 bf16 then-add
 //    6.22 vs 5.28; rows of 129..256 loads too, against rows per warp (65536 x
 //    2048 bf16: plain 6.81 vs 6.32, then-add 7.02 vs 5.02, sandwich 6.76 vs 5.30);
+//  * plain f32 rows from 2048 rows up to 2048 loads, eight slots per thread
+//    (65536 x 6656 7.08 vs 6.47; 65536 x 8192 7.13 vs 6.73; 4096 x 6656 6.41
+//    vs 5.84);
 //  * wider rows from 2048 rows: then-add up to 1664 loads (16384 x 8192 bf16
 //    7.01 vs 6.51, 65536 x 6656 f32 6.95 vs 6.84; at 2048 loads staged, 6.86
 //    vs 6.11), then-add-scale the same in bf16 but up to 1280 loads in f32
@@ -149,6 +152,7 @@ bool register_batch_pays(mrn::Op op, mrn_dtype dt, int64_t nvec, int64_t rows) {
     if (rows < 2048 || op == mrn::kSandwich) return false;
     if (op == mrn::kThenAdd) return nvec <= 1664;
     if (op == mrn::kThenAddScale) return nvec <= (f32 ? 1280 : 1664);
+    if (op == mrn::kRmsnorm && f32) return true;   // (eight slots per thread, below)
     return nvec <= (f32 ? 1280 : 896);
 }
 
@@ -394,6 +398,14 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
         // 128 for the Q8_1 pass (measured best)
         double target = std::min(256.0, std::max(64.0, static_cast<double>(nvec) /
                                      (op == mrn::kSandwich && dt == MRN_BF16 ? 2.0 : 4.0)));
+        // plain f32 rows past 512 loads: eight slots per thread, the kernel then
+        // fitting three CTAs per SM (65536 x 6656: 224 x 8 492.8 us, 256 x 7 551.6,
+        // staged 539.5; 65536 x 5120: 160 x 8 378.0 vs 256 x 5 395.5); then-add up
+        // to 512 threads of four slots (65536 x 6656: 416 x 4 743.8 us, 256 x 7 764.9)
+        if (op == mrn::kRmsnorm && dt == MRN_F32 && nvec > 512)
+            target = std::min(256.0, static_cast<double>(nvec) / 8.0);
+        if (op == mrn::kThenAdd)
+            target = std::min(512.0, std::max(64.0, static_cast<double>(nvec) / 4.0));
         if (op == mrn::kAddRmsnorm) target = 256.0;
         if (op == mrn::kRmsnormQ8) target = 128.0;
         pick_threads_batch(ceil_div(nvec, cl), &g.k, &g.threads, target);

@@ -215,13 +215,14 @@ BATCH_CHOICES = [
     (mrn.MRN_OP_THEN_ADD, 65536, 2048, mrn.MRN_BF16, (2, 64, 4)),
     (mrn.MRN_OP_RMSNORM, 65536, 512, mrn.MRN_F32, (1,)),            # 128 loads: rows per warp
     (mrn.MRN_OP_RMSNORM, 163840, 128, mrn.MRN_BF16, (1,)),          # per-head QK-norm
-    (mrn.MRN_OP_RMSNORM, 4096, 6656, mrn.MRN_F32, (4,)),
-    (mrn.MRN_OP_THEN_ADD, 4096, 6656, mrn.MRN_F32, (2, 256, 7)),
+    (mrn.MRN_OP_RMSNORM, 4096, 6656, mrn.MRN_F32, (2, 224, 8)),     # eight slots, 3 CTAs/SM
+    (mrn.MRN_OP_RMSNORM, 65536, 8192, mrn.MRN_F32, (2, 256, 8)),
+    (mrn.MRN_OP_THEN_ADD, 4096, 6656, mrn.MRN_F32, (2, 416, 4)),
     (mrn.MRN_OP_THEN_ADD, 65536, 8192, mrn.MRN_F32, (4,)),
     (mrn.MRN_OP_THEN_ADD_SCALE, 4096, 6656, mrn.MRN_F32, (4,)),
     (mrn.MRN_OP_THEN_ADD_SCALE, 65536, 5120, mrn.MRN_F32, (2, 256, 5)),
     (mrn.MRN_OP_THEN_ADD_SCALE, 4096, 6656, mrn.MRN_BF16, (2, 224, 4)),
-    (mrn.MRN_OP_RMSNORM, 65536, 5120, mrn.MRN_F32, (2, 256, 5)),
+    (mrn.MRN_OP_RMSNORM, 65536, 5120, mrn.MRN_F32, (2, 160, 8)),
     (mrn.MRN_OP_RMSNORM, 1216, 4096, mrn.MRN_F32, (4,)),            # rows < 2048, 1024 loads
     (mrn.MRN_OP_RMSNORM, 1216, 2048, mrn.MRN_F32, (2, 128, 4)),
     (mrn.MRN_OP_RMSNORM, 4096, 6656, mrn.MRN_BF16, (2, 224, 4)),

@@ -353,12 +353,14 @@ def test_forced_staged_kernel(geom, nvec, rows, dtype):
 
 def test_batch_kernel_choice_and_both_kernels():
     """Batches of aligned rows take the register kernel where it measured faster
-    (the f32 sandwich and then-add at n = 6656 from 2048 rows, every operation
-    at 512 loads per row) and the staged kernel elsewhere (plain f32 at 6656);
-    the same 2048 x 6656 batch through the automatic choice and through the
-    staged kernel forced, every operation against the oracle."""
+    (f32 plain, then-add and sandwich at n = 6656 from 2048 rows, every
+    operation at 512 loads per row) and the staged kernel elsewhere (the bf16
+    sandwich past 512 loads); the same 2048 x 6656 batch through the automatic
+    choice and through the staged kernel forced, every operation against the
+    oracle."""
     assert [mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True)["kind"]
-            for op in (0, 1, 2)] == [mrn.MRN_GEOM_TMA, mrn.MRN_GEOM_CTA, mrn.MRN_GEOM_CTA]
+            for op in (0, 1, 2)] == [mrn.MRN_GEOM_CTA] * 3
+    assert mrn.mrn_query_geometry(2, 4096, 8192, mrn.MRN_BF16, True)["kind"] == mrn.MRN_GEOM_TMA
     for op in (0, 1, 2):
         assert mrn.mrn_query_geometry(op, 16384, 4096, mrn.MRN_BF16, True)["kind"] == \
             mrn.MRN_GEOM_CTA
