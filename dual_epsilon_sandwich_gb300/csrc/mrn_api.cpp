@@ -130,13 +130,13 @@ void pick_threads_batch(int64_t per, int *k_out, int *t_out, double target) {
 //    2048 bf16: plain 6.81 vs 6.32, then-add 7.02 vs 5.02, sandwich 6.76 vs 5.30);
 //  * plain f32 rows from 2048 rows up to 2048 loads, eight slots per thread
 //    (65536 x 6656 7.08 vs 6.47; 65536 x 8192 7.13 vs 6.73; 4096 x 6656 6.41
-//    vs 5.84);
+//    vs 5.84); the f32 seam the same way (16384 x 8192 7.03 vs 6.41, 16384 x
+//    6656 6.68 vs 6.48);
 //  * wider rows from 2048 rows: then-add up to 1664 loads (16384 x 8192 bf16
 //    7.01 vs 6.51, 65536 x 6656 f32 6.95 vs 6.84; at 2048 loads staged, 6.86
 //    vs 6.11), then-add-scale the same in bf16 but up to 1280 loads in f32
 //    (at 1664, 4096 x 6656: 58.8 us against 50.8 for the staged then-add);
-//    plain and the f32 seam up to 1280 loads in f32 (65536 x 5120 6.88 vs
-//    6.08) and 896 in bf16 (4096 x 6656 5.45 vs 4.21); the bf16 seam from 4096
+//    bf16 plain up to 896 loads (4096 x 6656 5.45 vs 4.21); the bf16 seam from 4096
 //    rows up to 896 loads (16384 x 4096 6.57 vs 6.20).  The bf16 sandwich
 //    keeps the staged kernel past 512 loads (4096 x 8192: 4.71 vs 6.01).
 bool register_batch_pays(mrn::Op op, mrn_dtype dt, int64_t nvec, int64_t rows) {
@@ -145,7 +145,7 @@ bool register_batch_pays(mrn::Op op, mrn_dtype dt, int64_t nvec, int64_t rows) {
     if (nvec > 2048) return false;
     const bool f32 = dt == MRN_F32;
     if (mrn::op_is_seam(op)) {
-        if (f32) return nvec <= 1280 && (nvec <= 512 || rows >= 2048);
+        if (f32) return nvec <= 2048 && (nvec <= 512 || rows >= 2048);
         return nvec <= 896 && rows >= 4096;
     }
     if (nvec <= 512) return true;
@@ -402,7 +402,7 @@ Geometry choose_geometry(mrn::Op op, int64_t rows, int64_t n, mrn_dtype dt, bool
         // fitting three CTAs per SM (65536 x 6656: 224 x 8 492.8 us, 256 x 7 551.6,
         // staged 539.5; 65536 x 5120: 160 x 8 378.0 vs 256 x 5 395.5); then-add up
         // to 512 threads of four slots (65536 x 6656: 416 x 4 743.8 us, 256 x 7 764.9)
-        if (op == mrn::kRmsnorm && dt == MRN_F32 && nvec > 512)
+        if ((op == mrn::kRmsnorm || mrn::op_is_seam(op)) && dt == MRN_F32 && nvec > 512)
             target = std::min(256.0, static_cast<double>(nvec) / 8.0);
         if (op == mrn::kThenAdd)
             target = std::min(512.0, std::max(64.0, static_cast<double>(nvec) / 4.0));

@@ -182,8 +182,10 @@ def test_seam_validation():
 
 def test_seam_geometry():
     for op in (mrn.MRN_OP_RMSNORM_SEAM, mrn.MRN_OP_RMSNORM_UNWEIGHTED):
+        got = mrn.mrn_query_geometry(op, 1216, 6656, mrn.MRN_F32, True, 152)
+        assert (got["kind"], got["stages"], got["groups"]) == (4, 4, 2)   # staged, 4 stages
         got = mrn.mrn_query_geometry(op, 4096, 6656, mrn.MRN_F32, True, 152)
-        assert (got["kind"], got["stages"], got["groups"]) == (4, 4, 2)
+        assert (got["kind"], got["threads"], got["k"]) == (2, 224, 8)     # register batch
         got = mrn.mrn_query_geometry(op, 2048, 4096, mrn.MRN_BF16, True, 152)
         assert (got["kind"], got["stages"], got["groups"]) == (4, 2, 2)
         got = mrn.mrn_query_geometry(op, 16384, 4096, mrn.MRN_BF16, True, 152)
