@@ -371,12 +371,13 @@ def test_geometry_covers_every_row_width():
 # as measured best on GB300: slices of at most 2048 loads; plain 3 stages at C = 2,
 # else 2; then-add (and -scale) 3 stages from C = 8; the sandwich doubles C from 8.
 CLUSTER_STAGED = [
-    ((0, 4096, 16384, 0), (2, 3, 256, 8)),
+    ((0, 1024, 16384, 0), (2, 3, 256, 8)),   # (plain f32 from 2048 rows: the register kernel)
     ((1, 4096, 16384, 0), (2, 2, 256, 8)),
     ((2, 16384, 16384, 0), (2, 2, 256, 8)),
-    ((0, 8192, 32768, 0), (4, 2, 256, 8)),
+    ((0, 1024, 32768, 0), (4, 2, 256, 8)),
     ((1, 8192, 32768, 0), (4, 2, 256, 8)),
-    ((0, 4096, 65536, 0), (8, 2, 256, 8)),
+    ((0, 1024, 65536, 0), (8, 2, 256, 8)),
+    ((0, 4096, 65536, 0), (8, 2, 256, 8)),   # (past 8 x 1024 loads plain f32 stays staged)
     ((1, 4096, 65536, 0), (8, 3, 256, 8)),
     ((4, 4096, 65536, 0), (8, 3, 256, 8)),
     ((2, 4096, 65536, 0), (16, 2, 256, 4)),
@@ -384,6 +385,20 @@ CLUSTER_STAGED = [
     ((2, 8192, 32768, 1), (2, 2, 256, 8)),
     ((0, 4096, 131072, 0), (16, 2, 256, 8)),
 ]
+
+
+# Plain f32 batches of 2048 rows or more with rows of 2049 .. 8 x 1024 loads: the
+# register kernel at eight slots per thread in clusters of ceil(loads / 1024) CTAs.
+REGISTER_CLUSTER = [((4096, 16384), (4, 128)), ((65536, 16384), (4, 128)),
+                    ((4096, 32768), (8, 128)), ((4096, 10240), (3, 128)),
+                    ((2048, 8196), (3, 96))]
+
+
+@pytest.mark.parametrize("shape,want", REGISTER_CLUSTER, ids=[str(c) for c, _ in REGISTER_CLUSTER])
+def test_plain_f32_wide_batches_use_the_register_cluster_kernel(shape, want):
+    g = mrn.mrn_query_geometry(0, shape[0], shape[1], mrn.MRN_F32, True, 152)
+    assert (g["kind"], g["cluster"], g["threads"], g["k"]) == (mrn.MRN_GEOM_CTA, *want, 8)
+    assert g["threads"] * g["k"] * g["cluster"] >= shape[1] // 4
 
 
 @pytest.mark.parametrize("call,want", CLUSTER_STAGED, ids=[str(c) for c, _ in CLUSTER_STAGED])

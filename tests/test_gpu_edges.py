@@ -232,6 +232,20 @@ def test_wide_row_batches_use_the_cluster_staged_kernel(dtype, n, cluster):
     assert mrn.mrn_wait_timeouts() == 0
 
 
+@pytest.mark.parametrize("rows,n,cluster", [(2048, 16384, 4), (2048, 10240, 3), (2048, 8196, 3)])
+def test_plain_f32_wide_batches_in_register_clusters(rows, n, cluster):
+    """Plain f32 batches of 2048+ rows wider than 2048 loads: the register kernel
+    at eight slots per thread, a cluster of ceil(loads / 1024) CTAs per row (3 at
+    n = 10240 and 8196: slices of 864 / 704 loads, the last one shorter); sampled
+    rows against the oracle."""
+    g = mrn.mrn_query_geometry(0, rows, n, mrn.MRN_F32, True)
+    assert (g["kind"], g["cluster"], g["k"]) == (mrn.MRN_GEOM_CTA, cluster, 8)
+    d = rows_data(n + 21, rows, n, "f32")
+    gu.parity_rmsnorm(d["x"], d["gamma"], 1e-5, "f32", gu.sample_rows(rows, 48, n),
+                      what=f"register cluster {rows}x{n}")
+    assert mrn.mrn_wait_timeouts() == 0
+
+
 def test_epsilon_routing_is_visible():
     """Block output of mean square 1e-8 and a stream of mean square ~1e-6:
     eps_post = 1e-8 and eps_pre = 1e-5 both move the outputs, and an oracle with
