@@ -66,14 +66,15 @@ def parse_args(argv=None):
                    help="only run --warmup + this many launches of the timed call (for ncu)")
     p.add_argument("--profile-op", choices=("sandwich", "seam_f16", "q8_1", "wide_f32",
                                             "decode", "qk_norm", "add_rmsnorm", "widest_f32",
-                                            "sandwich_n6655"),
+                                            "sandwich_n6655", "plain_f32"),
                    default="sandwich",
                    help="with --profile-launches: the call to launch -- the timed sandwich, the "
                         "fused f16 seam at the same shape, RMSNorm + Q8_1 at 16384 x 4096 bf16, "
                         "plain f32 RMSNorm at 1024 x 65536, the decode sandwich (1 x 6656 f32), "
                         "QK-norm (163840 x 128 bf16), residual add + norm (4096 x 6656 f32), or "
-                        "plain f32 RMSNorm at 256 x 262144 (the looped kernel), or the sandwich "
-                        "at 4096 x 6655 f32 (rows not 16-byte aligned: the edge-staged kernel)")
+                        "plain f32 RMSNorm at 256 x 262144 (the looped kernel), the sandwich "
+                        "at 4096 x 6655 f32 (rows not 16-byte aligned: the edge-staged kernel), "
+                        "or plain f32 RMSNorm at 4096 x 6656 (eight slots, three CTAs per SM)")
     return p.parse_args(argv)
 
 
@@ -984,9 +985,10 @@ def profile_other(args, dev):
             return mrn.mrn_rmsnorm(t[0].data_ptr(), t[1].data_ptr(), t[2].data_ptr(), rows, n,
                                    1e-5, mrn.MRN_F32, sh)
         geometry = mrn.mrn_query_geometry(mrn.MRN_OP_RMSNORM, rows, n, mrn.MRN_F32, True)
-    elif args.profile_op == "wide_f32":
-        # plain f32 RMSNorm of 256 KB rows (the cluster-staged kernel, 8 CTAs a row)
-        rows, n = 1024, 65536
+    elif args.profile_op in ("wide_f32", "plain_f32"):
+        # plain f32 RMSNorm of 256 KB rows (the cluster-staged kernel, 8 CTAs a row),
+        # or at the benchmark's shape (the register kernel at eight slots per thread)
+        rows, n = (1024, 65536) if args.profile_op == "wide_f32" else (4096, 6656)
         sets = [(torch.randn(rows, n, device=dev, generator=gen),
                  1 + 0.1 * torch.randn(n, device=dev, generator=gen),
                  torch.empty(rows, n, device=dev)) for _ in range(2)]
