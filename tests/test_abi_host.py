@@ -235,6 +235,28 @@ BATCH_CHOICES = [
 ]
 
 
+# The same choice on both sides of each threshold of the rule (loads per row,
+# rows): (op, rows, n, dtype) -> kind.
+BATCH_THRESHOLDS = [
+    ((0, 2048, 2048, mrn.MRN_F32), 2), ((0, 2047, 2052, mrn.MRN_F32), 4),
+    ((0, 2048, 2052, mrn.MRN_F32), 2), ((0, 2048, 8192, mrn.MRN_F32), 2),
+    ((1, 2048, 6656, mrn.MRN_F32), 2), ((1, 2048, 6660, mrn.MRN_F32), 4),
+    ((4, 2048, 5120, mrn.MRN_F32), 2), ((4, 2048, 5124, mrn.MRN_F32), 4),
+    ((4, 2048, 13312, mrn.MRN_BF16), 2), ((4, 2048, 13320, mrn.MRN_BF16), 4),
+    ((0, 2048, 7168, mrn.MRN_BF16), 2), ((0, 2048, 7176, mrn.MRN_BF16), 4),
+    ((6, 4095, 4096, mrn.MRN_BF16), 4), ((6, 4096, 4096, mrn.MRN_BF16), 2),
+    ((6, 2047, 8192, mrn.MRN_F32), 4), ((6, 2048, 8192, mrn.MRN_F32), 2),
+    ((2, 2048, 4096, mrn.MRN_BF16), 2), ((2, 2048, 4104, mrn.MRN_BF16), 4),
+    ((2, 2047, 6656, mrn.MRN_F32), 4), ((2, 2048, 6656, mrn.MRN_F32), 2),
+]
+
+
+@pytest.mark.parametrize("call,kind", BATCH_THRESHOLDS, ids=[str(c) for c, _ in BATCH_THRESHOLDS])
+def test_register_batch_thresholds(call, kind):
+    op, rows, n, dt = call
+    assert mrn.mrn_query_geometry(op, rows, n, dt, True, 152)["kind"] == kind
+
+
 @pytest.mark.parametrize("op,rows,n,dt,want", BATCH_CHOICES,
                          ids=[f"{c[0]}-{c[1]}x{c[2]}-{c[3]}" for c in BATCH_CHOICES])
 def test_register_batch_choice(op, rows, n, dt, want):
